@@ -1,0 +1,354 @@
+/*
+ * moe_oracle.c -- plain FP64 CPU oracle for the local MoE forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, calls or
+ * includes this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with the
+ * CUDA path.
+ *
+ * Every step is the plain definition of what the pages specify, written for a
+ * reader to check by eye: no blocking, no fusion, no reordering.  All
+ * arithmetic is double precision; inputs stored as F32/F16/BF16 are decoded
+ * exactly to double here.  Loops parallelised with OpenMP only over
+ * independent outputs (each output element is computed by one thread in a
+ * fixed order), so results do not depend on the thread count.
+ *
+ * Sources (page title, section):
+ *   [UG4]  ruDNN Benutzerhandbuch, section 4 "Routing-Vertrag": FP32 softmax
+ *          over all experts before top-k, ties to the lower expert id,
+ *          optional renormalisation then cast to the logits dtype, NaN weights
+ *          for rows holding NaN, +inf or only -inf; indices U32 [T, top_k].
+ *   [UG5]  same page, section 5 "Expertengewichte und Verteilung": input
+ *          [T,H], gate/up [E,I,H], down [E,H,I]; dispatch drops no token;
+ *          a stored map restores token order.
+ *   [UG6]  same page, section 6 "MoE aufrufen": combine restores token order
+ *          and sums expert outputs with the routing weights.
+ *   [EXP]  ruDNN 0.1.25 source view, src/moe/experts.rs,
+ *          SwiGluExperts::forward_dispatched_with_strategy: gate and up
+ *          segmented grouped products (out = in . W[e]^T), silu(gate)*up,
+ *          then the down product.  SwiGluExperts::new: bias-free weights.
+ *   [SILU] MindSpeed-Ops PR 163 diffs, rms_norm_gated notes: silu(x) is
+ *          x * sigmoid(x).
+ *
+ * Readings where the pages leave a step open (the same list is kept in the
+ * design notes):
+ *   R1 the selection key is the logit itself (softmax is strictly monotone,
+ *      so this is top-k of the softmax); equal logits -> lower id; +0 == -0.
+ *   R2 slot order of idx[t,:]: descending weight, ties -> lower id.
+ *   R3 a poisoned row (any NaN, any +inf, or every entry -inf) is all-tied:
+ *      idx = 0..k-1 and every weight NaN; it is still dispatched.
+ *   R4 weights are always stored in the logits dtype (cast by round to
+ *      nearest even), with or without renormalisation.
+ *   R7 no intermediate rounding in the oracle.
+ *   R8 the combine uses the cast weights.
+ *
+ * Parity status: every function below is pinned by the CPU test suite
+ * (brute-force top-k enumeration, closed-form softmax cases, the NaN rule,
+ * dispatch invariants and a library stable sort, a dense masked per-token
+ * evaluation and the E=1/k=1 plain SwiGLU MLP).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* storage codes: 0 = F32, 1 = F16, 2 = BF16 */
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2 };
+
+/* ------------------------------------------------------------------------ */
+/* exact decoding of stored elements to double                              */
+/* ------------------------------------------------------------------------ */
+
+static double decode_f16(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int mant = h & 0x3ff;
+    double v;
+    if (expo == 0x1f) {
+        v = mant ? NAN : INFINITY;
+    } else if (expo == 0) {
+        v = ldexp((double)mant, -24); /* subnormal: mant * 2^-24 */
+    } else {
+        v = ldexp((double)(mant | 0x400), expo - 25); /* 1.mant * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+static double decode_bf16(uint16_t b) {
+    uint32_t bits = (uint32_t)b << 16; /* bf16 is the top half of an f32 */
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static double load_elem(const void* base, int dtype, int64_t i) {
+    switch (dtype) {
+    case OR_F32: return (double)((const float*)base)[i];
+    case OR_F16: return decode_f16(((const uint16_t*)base)[i]);
+    default:     return decode_bf16(((const uint16_t*)base)[i]);
+    }
+}
+
+/* Round a double to the nearest value of the storage format (ties to even),
+ * returned as a double.  Formats: precision p bits, minimum normal exponent
+ * emin, maximum finite value fmax.  Overflow beyond the rounding threshold
+ * gives infinity, as IEEE round-to-nearest does. */
+double oracle_round_to_dtype(double v, int dtype) {
+    if (isnan(v) || isinf(v) || v == 0.0) return v;
+    int p, emin;
+    double fmax;
+    if (dtype == OR_F32) { p = 24; emin = -126; fmax = ldexp(2.0 - ldexp(1.0, -23), 127); }
+    else if (dtype == OR_F16) { p = 11; emin = -14; fmax = 65504.0; }
+    else { p = 8; emin = -126; fmax = ldexp(2.0 - ldexp(1.0, -7), 127); }
+    int ex;
+    frexp(fabs(v), &ex);          /* |v| = m * 2^ex, m in [0.5, 1) */
+    int lead = ex - 1;            /* exponent of the leading bit */
+    if (lead < emin) lead = emin; /* subnormal range: fixed quantum */
+    double quantum = ldexp(1.0, lead - (p - 1));
+    double r = rint(v / quantum) * quantum; /* rint: ties to even (default mode) */
+    if (fabs(r) > fmax) return v > 0 ? INFINITY : -INFINITY;
+    return r;
+}
+
+/* ------------------------------------------------------------------------ */
+/* routing  [UG4]                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* "a beats b" for selection: larger logit first, equal logits -> lower id. */
+static int beats(double la, int64_t a, double lb, int64_t b) {
+    if (la > lb) return 1;
+    if (la < lb) return 0;
+    return a < b; /* equal (including +0 vs -0) */
+}
+
+/* One row of the routing contract.
+ *   l[0..E-1]      logits of the row, exact in double
+ *   idx[0..k-1]    selected experts, descending weight (R2)
+ *   w_pre[0..k-1]  weights before the cast (softmax value, optionally
+ *                  renormalised over the selected set)
+ *   w_cast[0..k-1] weights rounded to the logits dtype (R4)            */
+static void route_row(const double* l, int64_t E, int k, int renorm, int wdtype,
+                      uint32_t* idx, double* w_pre, double* w_cast) {
+    int has_nan = 0, has_pinf = 0, all_ninf = 1;
+    for (int64_t e = 0; e < E; ++e) {
+        if (isnan(l[e])) has_nan = 1;
+        if (l[e] == INFINITY) has_pinf = 1;
+        if (l[e] != -INFINITY) all_ninf = 0;
+    }
+    if (has_nan || has_pinf || all_ninf) { /* R3: NaN weights, all-tied row */
+        for (int j = 0; j < k; ++j) {
+            idx[j] = (uint32_t)j;
+            w_pre[j] = NAN;
+            w_cast[j] = NAN;
+        }
+        return;
+    }
+    /* softmax over all experts: p_e = exp(l_e - m) / sum_i exp(l_i - m) */
+    double m = -INFINITY;
+    for (int64_t e = 0; e < E; ++e) if (l[e] > m) m = l[e];
+    double s = 0.0;
+    for (int64_t e = 0; e < E; ++e) s += exp(l[e] - m);
+
+    /* top-k by (logit desc, id asc): k passes, each taking the best unused */
+    char* used = (char*)calloc((size_t)E, 1);
+    for (int j = 0; j < k; ++j) {
+        int64_t best = -1;
+        for (int64_t e = 0; e < E; ++e) {
+            if (used[e]) continue;
+            if (best < 0 || beats(l[e], e, l[best], best)) best = e;
+        }
+        used[best] = 1;
+        idx[j] = (uint32_t)best;
+        w_pre[j] = exp(l[best] - m) / s;
+    }
+    free(used);
+    if (renorm) {
+        double tot = 0.0;
+        for (int j = 0; j < k; ++j) tot += w_pre[j];
+        for (int j = 0; j < k; ++j) w_pre[j] = w_pre[j] / tot;
+    }
+    for (int j = 0; j < k; ++j) w_cast[j] = oracle_round_to_dtype(w_pre[j], wdtype);
+}
+
+/* logits: T*E stored elements of dtype ldt.  Outputs idx [T*k] u32,
+ * w_pre [T*k], w_cast [T*k]. */
+void oracle_route(const void* logits, int ldt, int64_t T, int64_t E, int k, int renorm,
+                  uint32_t* idx, double* w_pre, double* w_cast) {
+#pragma omp parallel
+    {
+        double* row = (double*)malloc((size_t)E * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < T; ++t) {
+            for (int64_t e = 0; e < E; ++e) row[e] = load_elem(logits, ldt, t * E + e);
+            route_row(row, E, k, renorm, ldt, idx + t * k, w_pre + t * k, w_cast + t * k);
+        }
+        free(row);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* dispatch  [UG5]                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* Capacity-free dispatch into contiguous per-expert segments.
+ *   c_e = number of slots (t,j) with idx[t,j] == e
+ *   offsets[0] = 0, offsets[e+1] = offsets[e] + c_e
+ *   segment e lists its slots in ascending flat slot index s = t*k + j
+ *   (a stable counting sort of the slots by expert id)
+ *   perm[r] = s, row_experts[r] = e for the r-th dispatched row.
+ * Slots whose index is >= E are not dispatched; they are counted in
+ * *invalid and the unused tail of perm/row_experts is set to 0xFFFFFFFF. */
+void oracle_dispatch(const uint32_t* idx, int64_t T, int64_t E, int k,
+                     uint32_t* offsets, uint32_t* row_experts, uint32_t* perm,
+                     int64_t* invalid) {
+    int64_t n = T * (int64_t)k;
+    int64_t bad = 0;
+    for (int64_t e = 0; e <= E; ++e) offsets[e] = 0;
+    for (int64_t s = 0; s < n; ++s) {
+        if (idx[s] < (uint64_t)E) offsets[idx[s] + 1] += 1;
+        else ++bad;
+    }
+    for (int64_t e = 0; e < E; ++e) offsets[e + 1] += offsets[e];
+    uint64_t* fill = (uint64_t*)calloc((size_t)E, sizeof(uint64_t));
+    for (int64_t s = 0; s < n; ++s) { /* ascending s: stable */
+        uint32_t e = idx[s];
+        if (e >= (uint64_t)E) continue;
+        uint64_t r = offsets[e] + fill[e]++;
+        perm[r] = (uint32_t)s;
+        row_experts[r] = e;
+    }
+    free(fill);
+    for (int64_t r = n - bad; r < n; ++r) { perm[r] = 0xFFFFFFFFu; row_experts[r] = 0xFFFFFFFFu; }
+    *invalid = bad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* experts  [EXP], [SILU]                                                    */
+/* ------------------------------------------------------------------------ */
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* One bias-free SwiGLU expert on one row:
+ *   g_i = sum_h W_gate[e,i,h] x_h,  u_i = sum_h W_up[e,i,h] x_h
+ *   a_i = silu(g_i) * u_i
+ *   o_c = sum_i W_down[e,c,i] a_i                                        */
+static void expert_row(const double* x, int64_t e, int64_t H, int64_t I,
+                       const void* gate, const void* up, const void* down, int wdt,
+                       double* a /* scratch [I] */, double* o /* [H] */) {
+    for (int64_t i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        int64_t base = (e * I + i) * H;
+        for (int64_t h = 0; h < H; ++h) {
+            g += load_elem(gate, wdt, base + h) * x[h];
+            u += load_elem(up, wdt, base + h) * x[h];
+        }
+        a[i] = silu(g) * u;
+    }
+    for (int64_t c = 0; c < H; ++c) {
+        double acc = 0.0;
+        int64_t base = (e * H + c) * I;
+        for (int64_t i = 0; i < I; ++i) acc += load_elem(down, wdt, base + i) * a[i];
+        o[c] = acc;
+    }
+}
+
+/* Experts on dispatched rows: out[r,:] = expert_{row_experts[r]}(x_disp[r,:])
+ * for r < offsets[E]; rows beyond are left untouched.  x_disp is given in
+ * double (the caller decodes it), out is [N,H] double. */
+void oracle_experts(const double* x_disp, const uint32_t* offsets, int64_t E,
+                    const void* gate, const void* up, const void* down, int wdt,
+                    int64_t H, int64_t I, double* out) {
+    int64_t nrows = offsets[E];
+#pragma omp parallel
+    {
+        double* a = (double*)malloc((size_t)I * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r) {
+            int64_t e = 0;
+            while (!(offsets[e] <= (uint64_t)r && (uint64_t)r < offsets[e + 1])) ++e;
+            expert_row(x_disp + r * H, e, H, I, gate, up, down, wdt, a, out + r * H);
+        }
+        free(a);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* combine  [UG6]                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* y[t,:] = sum_j w_cast[t,j] * expert_out[r(t,j),:], where r(t,j) is the
+ * dispatched row holding slot s = t*k+j (the inverse of perm), summed in
+ * ascending j.  A slot that was not dispatched makes its token's row NaN. */
+void oracle_combine(const double* expert_out, const uint32_t* perm, const double* w_cast,
+                    int64_t T, int k, int64_t H, double* y) {
+    int64_t n = T * (int64_t)k;
+    int64_t* row_of = (int64_t*)malloc((size_t)(n > 0 ? n : 1) * sizeof(int64_t));
+    for (int64_t s = 0; s < n; ++s) row_of[s] = -1;
+    for (int64_t r = 0; r < n; ++r)
+        if (perm[r] != 0xFFFFFFFFu) row_of[perm[r]] = r;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t c = 0; c < H; ++c) y[t * H + c] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int64_t r = row_of[t * k + j];
+            for (int64_t c = 0; c < H; ++c)
+                y[t * H + c] += (r < 0) ? NAN : w_cast[t * k + j] * expert_out[r * H + c];
+        }
+    }
+    free(row_of);
+}
+
+/* ------------------------------------------------------------------------ */
+/* whole forward for a sample of tokens (route -> experts -> weighted sum)   */
+/* ------------------------------------------------------------------------ */
+
+/* For each listed token t: route its logits row, evaluate its k selected
+ * experts on x[t,:] and sum them with the cast weights in slot order.
+ * This is the per-token meaning of dispatch + experts + combine, used to
+ * check large problems on a sample of tokens.  Outputs for sample i:
+ * idx_out[i*k..], w_out[i*k..] (pre-cast), y_out[i*H..]. */
+void oracle_forward_tokens(const void* x, const void* logits, int ldt, int xdt,
+                           int64_t T, int64_t E, int k, int renorm, int64_t H, int64_t I,
+                           const void* gate, const void* up, const void* down,
+                           const int64_t* tokens, int64_t ntok,
+                           uint32_t* idx_out, double* w_out, double* y_out) {
+    (void)T;
+#pragma omp parallel
+    {
+        double* row = (double*)malloc((size_t)E * sizeof(double));
+        double* xt = (double*)malloc((size_t)H * sizeof(double));
+        double* a = (double*)malloc((size_t)I * sizeof(double));
+        double* o = (double*)malloc((size_t)H * sizeof(double));
+        double* wc = (double*)malloc((size_t)k * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < ntok; ++i) {
+            int64_t t = tokens[i];
+            for (int64_t e = 0; e < E; ++e) row[e] = load_elem(logits, ldt, t * E + e);
+            route_row(row, E, k, renorm, ldt, idx_out + i * k, w_out + i * k, wc);
+            for (int64_t h = 0; h < H; ++h) xt[h] = load_elem(x, xdt, t * H + h);
+            double* y = y_out + i * H;
+            for (int64_t h = 0; h < H; ++h) y[h] = 0.0;
+            for (int j = 0; j < k; ++j) {
+                expert_row(xt, idx_out[i * k + j], H, I, gate, up, down, xdt, a, o);
+                for (int64_t h = 0; h < H; ++h) y[h] += wc[j] * o[h];
+            }
+        }
+        free(row); free(xt); free(a); free(o); free(wc);
+    }
+}
+
+/* decoding helper for the Python side: n stored elements -> double */
+void oracle_decode(const void* src, int dtype, int64_t n, double* dst) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) dst[i] = load_elem(src, dtype, i);
+}
+
+int oracle_num_threads(void);
+#ifdef _OPENMP
+#include <omp.h>
+int oracle_num_threads(void) { return omp_get_max_threads(); }
+void oracle_set_threads(int n) { omp_set_num_threads(n); }
+#else
+int oracle_num_threads(void) { return 1; }
+void oracle_set_threads(int n) { (void)n; }
+#endif
