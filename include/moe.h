@@ -1,0 +1,224 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) local Mixture-of-Experts forward.
+ *
+ * The pipeline follows the ruDNN user guide ("ruDNN Benutzerhandbuch"),
+ * section 3 "MoE-Workflow": router logits -> FP32 softmax / top-k ->
+ * capacity-free dispatch -> bias-free SwiGLU experts -> weighted combine.
+ * The staged calls mirror section 6 "MoE aufrufen" (route, dispatch,
+ * forward_dispatched, combine) and the fused call mirrors
+ * SwiGluExperts::forward in the ruDNN 0.1.25 source view of src/moe/experts.rs.
+ *
+ * Conventions for every call
+ *   - Tensors are caller-owned, dense, row-major DEVICE pointers on the
+ *     current CUDA device (unless a parameter says "host").  Floating-point
+ *     tensors other than logits/weights must be 16-byte aligned; workspaces
+ *     must be 256-byte aligned.  The library never allocates device memory
+ *     during a call and never frees caller memory.
+ *   - Work is enqueued on `stream` and the call returns without waiting for
+ *     the device (except moe_get_device_status, which synchronises that
+ *     stream).  Calls are therefore capturable in a CUDA graph, except
+ *     moe_get_device_status and moe_forward_host with pageable memory.
+ *   - Shapes are element counts.  T = tokens, E = experts, k = top_k,
+ *     H = hidden size, I = expert intermediate size, N = T*k dispatched rows.
+ *   - Every call returns a moe_status.  On any status other than MOE_OK,
+ *     nothing was enqueued, and moe_last_error() returns a message for the
+ *     calling thread.  T == 0 is valid and enqueues nothing.
+ *   - Limits: 1 <= E <= 1024, 1 <= k <= min(E, 64), N < 2^31, H and I in
+ *     [1, 2^20].  Outside them MOE_ERR_UNSUPPORTED (k outside [1, E] is
+ *     MOE_ERR_INVALID_ARG, as the routing contract requires 1 <= top_k <= E).
+ *   - There is no CPU fallback: every step runs in this library's CUDA kernels.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,    /* null pointer, bad top_k, small workspace, misalignment */
+    MOE_ERR_SHAPE = 2,          /* dimension zero or mismatched, element count overflow */
+    MOE_ERR_DTYPE = 3,          /* dtype not F32/F16/BF16 or operands disagree */
+    MOE_ERR_UNSUPPORTED = 4,    /* outside the stated limits */
+    MOE_ERR_CUDA = 5,           /* a CUDA runtime/driver call or launch failed */
+    MOE_ERR_INVALID_INDEX = 6,  /* device-side: an expert index >= E reached dispatch */
+    MOE_ERR_DEVICE_TIMEOUT = 7  /* device-side: a bounded wait inside a kernel gave up */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_F16 = 1, MOE_BF16 = 2 } moe_dtype;
+
+typedef struct moe_experts* moe_experts_t;
+
+/* Message for the last failing call on this thread ("" if none).  The
+ * pointer stays valid until the next call on the same thread. */
+const char* moe_last_error(void);
+
+/* Static name of a status code. */
+const char* moe_status_string(moe_status status);
+
+/* ------------------------------------------------------------------------
+ * Routing.  ruDNN Benutzerhandbuch, section 4 "Routing-Vertrag".
+ *
+ * For each of the T rows of `logits` [T,E] (dtype F32, F16 or BF16, any
+ * element alignment): softmax over all E experts in FP32; the top_k experts
+ * by logit (ties go to the lower expert id; +0 and -0 are equal), listed in
+ * descending weight; weights = the selected softmax values, divided by their
+ * FP32 sum (added in slot order) when `renormalize` is non-zero, then rounded
+ * to the logits dtype (round to nearest even).  A row holding a NaN, a +inf,
+ * or only -inf entries gets idx = 0..top_k-1 and NaN weights.
+ *
+ *   idx          out [T,top_k] uint32 (device)
+ *   weights      out [T,top_k] in the logits dtype (device)
+ *   weights_f32  out [T,top_k] float, the same weights before the final
+ *                rounding (device; may be NULL)
+ * ---------------------------------------------------------------------- */
+moe_status moe_route(const void* logits, moe_dtype logits_dtype, int64_t T, int64_t E,
+                     int32_t top_k, int renormalize, uint32_t* idx, void* weights,
+                     float* weights_f32, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Dispatch.  ruDNN Benutzerhandbuch, section 5 "Expertengewichte und
+ * Verteilung" (no token dropped; a stored map restores token order) and
+ * the DispatchedTokens invariant in src/moe/experts.rs ("complete, monotone
+ * expert segments without token dropping").
+ *
+ * Slot s = t*top_k + j holds expert idx[t,j].  Rows are grouped into
+ * contiguous per-expert segments: offsets[e]..offsets[e+1] holds expert e's
+ * slots in ascending s (a stable sort of the slots by expert id, so the
+ * result is bit-reproducible).  For dispatched row r:
+ *   perm[r] = s, row_experts[r] = e, x_disp[r,:] = x[s / top_k, :].
+ *
+ *   idx          in  [T,top_k] uint32 (device)
+ *   x            in  [T,H] (device; may be NULL, then x_disp must be NULL)
+ *   offsets      out [E+1] uint32;  row_experts, perm  out [T*top_k] uint32
+ *   x_disp       out [T*top_k, H] in x's dtype (may be NULL)
+ *   workspace    device scratch of moe_dispatch_workspace_size() bytes; its
+ *                first word receives the device status (see
+ *                moe_get_device_status).
+ * An index >= E is not dispatched (no out-of-bounds access): offsets[E] then
+ * counts only valid slots, the unused tail of perm/row_experts is set to
+ * 0xFFFFFFFF and the device status becomes MOE_ERR_INVALID_INDEX.
+ * ---------------------------------------------------------------------- */
+size_t moe_dispatch_workspace_size(int64_t T, int64_t E, int32_t top_k);
+moe_status moe_dispatch(const uint32_t* idx, int64_t T, int64_t E, int32_t top_k,
+                        const void* x, moe_dtype x_dtype, int64_t H,
+                        uint32_t* offsets, uint32_t* row_experts, uint32_t* perm,
+                        void* x_disp, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Experts.  SwiGluExperts::new in src/moe/experts.rs and the user guide,
+ * section 5: bias-free gate and up [E,I,H], down [E,H,I], one float dtype,
+ * one device, every dimension non-zero.
+ *
+ * The handle does not own the weights: they must stay alive and unchanged
+ * while the handle is used.  It records shapes and prebuilt TMA descriptors
+ * and is reusable across batches.  Errors: MOE_ERR_DTYPE for a bad dtype,
+ * MOE_ERR_SHAPE for a zero dimension or an element-count overflow,
+ * MOE_ERR_INVALID_ARG for null or misaligned pointers or pointers that are
+ * not device memory of one device.
+ * ---------------------------------------------------------------------- */
+moe_status moe_experts_create(const void* gate, const void* up, const void* down,
+                              moe_dtype dtype, int64_t E, int64_t I, int64_t H,
+                              moe_experts_t* out);
+void moe_experts_destroy(moe_experts_t experts);
+
+/* SwiGluExperts::forward_dispatched_with_strategy in src/moe/experts.rs:
+ * for each dispatched row r of expert e (offsets[e] <= r < offsets[e+1]):
+ *   g = x_disp[r] . W_gate[e]^T, u = x_disp[r] . W_up[e]^T,
+ *   h = silu(g) * u  (rounded to the weight dtype),
+ *   expert_out[r] = h . W_down[e]^T  (FP32 accumulation, stored in the
+ *   weight dtype).
+ * x_disp [N,H] and expert_out [N,H] are in the weight dtype; offsets [E+1]
+ * on the device (never read by the host).  Rows at or beyond offsets[E] are
+ * not written.  workspace: moe_experts_workspace_size(experts, N) bytes. */
+size_t moe_experts_workspace_size(moe_experts_t experts, int64_t N);
+moe_status moe_experts_forward(moe_experts_t experts, const void* x_disp, int64_t N,
+                               const uint32_t* offsets, void* expert_out,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Combine.  User guide, section 6: the dispatch map restores token order and
+ * the expert outputs are summed with the routing weights:
+ *   y[t,:] = sum_{j=0..k-1} weights[t,j] * expert_out[r(t,j), :]
+ * where r(t,j) is the row with perm[r] = t*k+j; the sum runs in ascending j
+ * with FP32 accumulation and is rounded once to `dtype`.  A slot that no row
+ * holds makes y[t,:] NaN.
+ *   expert_out [T*k, H] and y [T,H] in `dtype`; weights [T,k] in
+ *   `weights_dtype`; perm [T*k] uint32.  workspace:
+ *   moe_combine_workspace_size(T, k) bytes.
+ * ---------------------------------------------------------------------- */
+size_t moe_combine_workspace_size(int64_t T, int32_t top_k);
+moe_status moe_combine(const void* expert_out, moe_dtype dtype, const uint32_t* perm,
+                       const void* weights, moe_dtype weights_dtype, int64_t T,
+                       int32_t top_k, int64_t H, void* y, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Fused forward.  SwiGluExperts::forward in src/moe/experts.rs: route ->
+ * dispatch -> experts -> combine for precomputed logits, all on `stream`
+ * with no host synchronisation.  x [T,H] and y [T,H] in the weight dtype;
+ * logits [T,E] in F32/F16/BF16.  The down projection's epilogue multiplies
+ * each row by its routing weight and stores it at its token slot; a final
+ * pass sums each token's k slots in ascending j.  Results equal the staged
+ * calls up to the rounding of the weighted slot values.
+ * workspace: moe_forward_workspace_size(...) bytes (intermediates live there;
+ * see moe_forward_layout).
+ * ---------------------------------------------------------------------- */
+size_t moe_forward_workspace_size(moe_experts_t experts, int64_t T, int32_t top_k,
+                                  moe_dtype logits_dtype);
+moe_status moe_forward(moe_experts_t experts, const void* x, const void* logits,
+                       moe_dtype logits_dtype, int64_t T, int32_t top_k, int renormalize,
+                       void* y, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Same as moe_forward, and records CUDA events on `stream` at the stage
+ * boundaries: events[0] before routing, [1] after routing, [2] after
+ * dispatch, [3] after the gate/up projection, [4] after the down projection,
+ * [5] after the combine.  `events` holds n_events (>= 6) cudaEvent_t handles
+ * created by the caller; the library records them and nothing else. */
+moe_status moe_forward_timed(moe_experts_t experts, const void* x, const void* logits,
+                             moe_dtype logits_dtype, int64_t T, int32_t top_k, int renormalize,
+                             void* y, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream, void* const* events, int n_events);
+
+/* Same computation with HOST buffers: x_host [T,H], logits_host [T,E] and
+ * y_host [T,H] live in host memory (page-locked memory makes the copies
+ * asynchronous).  The call enqueues the host-to-device copies into staging
+ * space inside the workspace, the forward, and the device-to-host copy of y;
+ * the caller synchronises `stream` before reading y_host.  workspace:
+ * moe_forward_host_workspace_size(...) bytes. */
+size_t moe_forward_host_workspace_size(moe_experts_t experts, int64_t T, int32_t top_k,
+                                       moe_dtype logits_dtype);
+moe_status moe_forward_host(moe_experts_t experts, const void* x_host, const void* logits_host,
+                            moe_dtype logits_dtype, int64_t T, int32_t top_k, int renormalize,
+                            void* y_host, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+/* Byte offsets of the intermediates moe_forward leaves in its workspace, so
+ * that a caller can inspect them after the stream has finished:
+ *   idx [T,k] u32, weights [T,k] logits dtype, offsets [E+1] u32,
+ *   perm [T*k] u32, x_disp [T*k,H], h [T*k,I], slots [T*k,H] (weighted
+ *   expert outputs at token-slot order).  Returns MOE_ERR_INVALID_ARG for a
+ *   null handle or output. */
+typedef struct {
+    size_t idx, weights, offsets, perm, x_disp, h, slots, total;
+} moe_forward_layout_t;
+moe_status moe_forward_layout(moe_experts_t experts, int64_t T, int32_t top_k,
+                              moe_dtype logits_dtype, moe_forward_layout_t* out);
+
+/* Reads the device status word at the start of `workspace` after
+ * synchronising `stream`: MOE_OK, MOE_ERR_INVALID_INDEX (dispatch met an
+ * index >= E) or MOE_ERR_DEVICE_TIMEOUT (a kernel's bounded wait expired and
+ * the kernel returned early; its outputs are undefined).  MOE_ERR_CUDA if
+ * the synchronisation itself fails. */
+moe_status moe_get_device_status(const void* workspace, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -306,10 +306,14 @@ void oracle_combine(const double* expert_out, const uint32_t* perm, const double
  * experts on x[t,:] and sum them with the cast weights in slot order.
  * This is the per-token meaning of dispatch + experts + combine, used to
  * check large problems on a sample of tokens.  Outputs for sample i:
- * idx_out[i*k..], w_out[i*k..] (pre-cast), y_out[i*H..]. */
+ * idx_out[i*k..], w_out[i*k..] (pre-cast), y_out[i*H..].
+ * expert_slot (may be NULL): expert e's weights sit at position
+ * expert_slot[e] of gate/up/down, so that a caller can pass only the
+ * experts its sample touches; NULL means position e. */
 void oracle_forward_tokens(const void* x, const void* logits, int ldt, int xdt,
                            int64_t T, int64_t E, int k, int renorm, int64_t H, int64_t I,
                            const void* gate, const void* up, const void* down,
+                           const int64_t* expert_slot,
                            const int64_t* tokens, int64_t ntok,
                            uint32_t* idx_out, double* w_out, double* y_out) {
     (void)T;
@@ -329,7 +333,13 @@ void oracle_forward_tokens(const void* x, const void* logits, int ldt, int xdt,
             double* y = y_out + i * H;
             for (int64_t h = 0; h < H; ++h) y[h] = 0.0;
             for (int j = 0; j < k; ++j) {
-                expert_row(xt, idx_out[i * k + j], H, I, gate, up, down, xdt, a, o);
+                int64_t e = idx_out[i * k + j];
+                if (expert_slot) e = expert_slot[e];
+                if (e < 0) { /* caller did not pass this expert */
+                    for (int64_t h = 0; h < H; ++h) o[h] = NAN;
+                } else {
+                    expert_row(xt, e, H, I, gate, up, down, xdt, a, o);
+                }
                 for (int64_t h = 0; h < H; ++h) y[h] += wc[j] * o[h];
             }
         }

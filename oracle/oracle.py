@@ -53,7 +53,7 @@ def _load():
         lib.oracle_experts.argtypes = [P, P, I64, P, P, P, I32, I64, I64, P]
         lib.oracle_combine.argtypes = [P, P, P, I64, I32, I64, P]
         lib.oracle_forward_tokens.argtypes = [P, P, I32, I32, I64, I64, I32, I32, I64, I64,
-                                              P, P, P, P, I64, P, P, P]
+                                              P, P, P, P, P, I64, P, P, P]
         lib.oracle_decode.argtypes = [P, I32, I64, P]
         lib.oracle_round_to_dtype.argtypes = [ctypes.c_double, I32]
         lib.oracle_round_to_dtype.restype = ctypes.c_double
@@ -148,13 +148,21 @@ def combine(expert_out: np.ndarray, perm: np.ndarray, w_cast: np.ndarray) -> np.
 
 def forward_tokens(x: np.ndarray, logits: np.ndarray, gate: np.ndarray, up: np.ndarray,
                    down: np.ndarray, dtype: str, logits_dtype: str, top_k: int,
-                   renormalize: bool, tokens) -> tuple:
-    """Per-token forward for a sample of tokens: returns (idx, w_pre, y) for those tokens."""
+                   renormalize: bool, tokens, experts_held=None) -> tuple:
+    """Per-token forward for a sample of tokens: returns (idx, w_pre, y) for those tokens.
+
+    ``experts_held``: when given, gate/up/down hold only these expert ids, in
+    this order (the sample's experts must be among them)."""
     xs = _stored(x, dtype)
     ls = _stored(logits, logits_dtype)
     g, u, d = (_stored(a, dtype) for a in (gate, up, down))
     T, H = xs.shape
-    E, I, _ = g.shape
+    E = ls.shape[1]
+    I = g.shape[1]
+    slot = None
+    if experts_held is not None:
+        slot = np.full(E, -1, np.int64)
+        slot[np.asarray(experts_held, np.int64)] = np.arange(len(experts_held))
     toks = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
     n = toks.size
     idx = np.empty((n, top_k), np.uint32)
@@ -162,6 +170,7 @@ def forward_tokens(x: np.ndarray, logits: np.ndarray, gate: np.ndarray, up: np.n
     y = np.empty((n, H), np.float64)
     _load().oracle_forward_tokens(_ptr(xs), _ptr(ls), DTYPE_CODES[logits_dtype], DTYPE_CODES[dtype],
                                   T, E, top_k, int(bool(renormalize)), H, I,
-                                  _ptr(g), _ptr(u), _ptr(d), _ptr(toks), n,
+                                  _ptr(g), _ptr(u), _ptr(d),
+                                  _ptr(slot) if slot is not None else None, _ptr(toks), n,
                                   _ptr(idx), _ptr(w), _ptr(y))
     return idx, w, y

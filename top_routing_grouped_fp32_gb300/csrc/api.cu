@@ -1,0 +1,479 @@
+// api.cu -- the C ABI declared in include/moe.h: argument validation, the
+// workspace layouts and the order of kernel launches on the caller's stream.
+//
+// Validation follows the rules of SwiGluExperts::new and
+// forward_dispatched_with_strategy in src/moe/experts.rs (rank-3 weights of
+// one float dtype, non-zero dimensions, up shape == gate shape, down ==
+// [E,H,I], dispatch/expert agreement) and the routing contract of the user
+// guide, section 4 (F32/F16/BF16 logits, 1 <= top_k <= E).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "common.cuh"
+#include "internal.h"
+
+struct moe_experts {
+  const void* gate;
+  const void* up;
+  const void* down;
+  moe_dtype dt;
+  int64_t E, I, H;
+  int device;
+  int num_sms;
+  moe::TcWeights* tc;  // null when the tcgen05 path does not apply (FP32, odd sizes)
+};
+
+namespace {
+
+using moe::align_up;
+using moe::dtype_size;
+using moe::kWsHeader;
+
+thread_local std::string g_error;
+
+moe_status fail(moe_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_error = buf;
+  return st;
+}
+
+moe_status ok() {
+  g_error.clear();
+  return MOE_OK;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define MOE_TRY_CUDA(expr, what)                   \
+  do {                                             \
+    cudaError_t _e = (expr);                       \
+    if (_e != cudaSuccess) return cuda_fail(_e, what); \
+  } while (0)
+
+constexpr int64_t kMaxE = 1024, kMaxK = 64, kMaxDim = int64_t(1) << 20;
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
+
+bool valid_dtype(moe_dtype d) { return d == MOE_F32 || d == MOE_F16 || d == MOE_BF16; }
+bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+bool aligned256(const void* p) { return reinterpret_cast<uintptr_t>(p) % 256 == 0; }
+
+// Checks shared by the calls that take (T, E, top_k).
+moe_status check_tek(int64_t T, int64_t E, int32_t k) {
+  if (T < 0) return fail(MOE_ERR_SHAPE, "T must be >= 0 (got %lld)", (long long)T);
+  if (E < 1) return fail(MOE_ERR_SHAPE, "E must be >= 1 (got %lld)", (long long)E);
+  if (k < 1 || k > E)
+    return fail(MOE_ERR_INVALID_ARG, "top_k must satisfy 1 <= top_k <= E (top_k=%d, E=%lld)", k,
+                (long long)E);
+  if (E > kMaxE) return fail(MOE_ERR_UNSUPPORTED, "E=%lld exceeds the supported 1024", (long long)E);
+  if (k > kMaxK) return fail(MOE_ERR_UNSUPPORTED, "top_k=%d exceeds the supported 64", k);
+  if (T > kMaxRows / k)
+    return fail(MOE_ERR_UNSUPPORTED, "T*top_k=%lld exceeds 2^31-1", (long long)T * k);
+  return MOE_OK;
+}
+
+moe_status check_dim(int64_t v, const char* name) {
+  if (v < 1) return fail(MOE_ERR_SHAPE, "%s must be >= 1 (got %lld)", name, (long long)v);
+  if (v > kMaxDim) return fail(MOE_ERR_UNSUPPORTED, "%s=%lld exceeds 2^20", name, (long long)v);
+  return MOE_OK;
+}
+
+moe_status check_ws(const void* ws, size_t have, size_t need) {
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  if (!aligned256(ws)) return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (have < need)
+    return fail(MOE_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", have, need);
+  return MOE_OK;
+}
+
+moe_status check_handle(const moe_experts* x) {
+  if (!x) return fail(MOE_ERR_INVALID_ARG, "experts handle is NULL");
+  int dev = -1;
+  MOE_TRY_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev != x->device)
+    return fail(MOE_ERR_INVALID_ARG, "experts live on device %d but device %d is current", x->device,
+                dev);
+  return MOE_OK;
+}
+
+// ---- workspace layouts -----------------------------------------------------
+struct Cursor {
+  size_t off = kWsHeader;
+  size_t take(size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 1024);
+    return at;
+  }
+};
+
+struct ForwardLayout {
+  size_t idx, weights, offsets, perm, scratch, x_disp, h, slots, total;
+};
+
+ForwardLayout forward_layout(const moe_experts* x, int64_t T, int32_t k, moe_dtype ldt) {
+  const size_t N = (size_t)T * k, s = dtype_size(x->dt);
+  Cursor c;
+  ForwardLayout L;
+  L.idx = c.take(N * 4);
+  L.weights = c.take(N * dtype_size(ldt));
+  L.offsets = c.take((size_t)(x->E + 1) * 4);
+  L.perm = c.take(N * 4);
+  L.scratch = c.take(moe::dispatch_scratch_bytes(T, (int)x->E));
+  L.x_disp = c.take(N * (size_t)x->H * s);
+  L.h = c.take(N * (size_t)x->I * s);
+  L.slots = c.take(N * (size_t)x->H * s);
+  L.total = c.off;
+  return L;
+}
+
+template <typename P>
+P* at(void* base, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(base) + off);
+}
+
+uint32_t* status_word(void* ws) { return static_cast<uint32_t*>(ws); }
+
+// Runs the two expert GEMMs: gate/up + SwiGLU into h, then down.
+moe_status run_experts(const moe_experts* x, const void* x_disp, int64_t N, const uint32_t* offsets,
+                       void* h, void* out, int down_mode, const uint32_t* perm, const void* weights,
+                       moe_dtype wdt, uint32_t* status, cudaStream_t s, void* ev_mid) {
+  moe::GemmArgs g{};
+  g.dt = x->dt;
+  g.E = (int)x->E;
+  g.N = N;
+  g.offsets = offsets;
+  g.status = status;
+  g.mode = moe::kGateUpSwiglu;
+  g.A = x_disp;
+  g.K = x->H;
+  g.n_out = x->I;
+  g.B0 = x->gate;
+  g.B1 = x->up;
+  g.out = h;
+  cudaError_t e = x->tc ? moe::launch_gemm_tc(g, x->tc, x->num_sms, s) : moe::launch_gemm_simt(g, s);
+  if (e != cudaSuccess) return cuda_fail(e, "gate/up grouped GEMM launch");
+  if (ev_mid) MOE_TRY_CUDA(cudaEventRecord((cudaEvent_t)ev_mid, s), "cudaEventRecord");
+  g.mode = down_mode;
+  g.A = h;
+  g.K = x->I;
+  g.n_out = x->H;
+  g.B0 = x->down;
+  g.B1 = nullptr;
+  g.out = out;
+  g.perm = perm;
+  g.weights = weights;
+  g.wdt = wdt;
+  e = x->tc ? moe::launch_gemm_tc(g, x->tc, x->num_sms, s) : moe::launch_gemm_simt(g, s);
+  if (e != cudaSuccess) return cuda_fail(e, "down grouped GEMM launch");
+  return MOE_OK;
+}
+
+moe_status forward_impl(moe_experts_t x, const void* xin, const void* logits, moe_dtype ldt,
+                        int64_t T, int32_t k, int renorm, void* y, void* ws, size_t ws_bytes,
+                        cudaStream_t s, void* const* ev) {
+  moe_status st = check_handle(x);
+  if (st != MOE_OK) return st;
+  if (!valid_dtype(ldt)) return fail(MOE_ERR_DTYPE, "logits dtype %d is not F32/F16/BF16", (int)ldt);
+  if ((st = check_tek(T, x->E, k)) != MOE_OK) return st;
+  if (T == 0) return ok();
+  if (!xin || !logits || !y) return fail(MOE_ERR_INVALID_ARG, "x, logits and y must be non-NULL");
+  if (!aligned16(xin) || !aligned16(y))
+    return fail(MOE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
+  const ForwardLayout L = forward_layout(x, T, k, ldt);
+  if ((st = check_ws(ws, ws_bytes, L.total)) != MOE_OK) return st;
+  const int64_t N = T * k;
+  const int E = (int)x->E;
+  uint32_t* status = status_word(ws);
+  uint32_t* idx = at<uint32_t>(ws, L.idx);
+  void* w = at<void>(ws, L.weights);
+  uint32_t* offsets = at<uint32_t>(ws, L.offsets);
+  uint32_t* perm = at<uint32_t>(ws, L.perm);
+
+  auto rec = [&](int i) -> cudaError_t {
+    return ev ? cudaEventRecord((cudaEvent_t)ev[i], s) : cudaSuccess;
+  };
+  MOE_TRY_CUDA(rec(0), "cudaEventRecord");
+  MOE_TRY_CUDA(moe::launch_route(logits, ldt, T, E, k, renorm, idx, w, nullptr, nullptr, s),
+               "routing kernel launch");
+  MOE_TRY_CUDA(rec(1), "cudaEventRecord");
+  MOE_TRY_CUDA(moe::launch_dispatch(idx, T, E, k, offsets, nullptr, perm, at<void>(ws, L.scratch),
+                                    status, s),
+               "dispatch kernel launch");
+  MOE_TRY_CUDA(moe::launch_gather(xin, x->dt, x->H, k, perm, offsets, E, N, at<void>(ws, L.x_disp), s),
+               "gather kernel launch");
+  MOE_TRY_CUDA(rec(2), "cudaEventRecord");
+  st = run_experts(x, at<void>(ws, L.x_disp), N, offsets, at<void>(ws, L.h), at<void>(ws, L.slots),
+                   moe::kDownWeighted, perm, w, ldt, status, s, ev ? ev[3] : nullptr);
+  if (st != MOE_OK) return st;
+  MOE_TRY_CUDA(rec(4), "cudaEventRecord");
+  MOE_TRY_CUDA(moe::launch_slot_sum(at<void>(ws, L.slots), x->dt, T, k, x->H, y, s),
+               "combine kernel launch");
+  MOE_TRY_CUDA(rec(5), "cudaEventRecord");
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_error.c_str(); }
+
+const char* moe_status_string(moe_status st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_SHAPE: return "MOE_ERR_SHAPE";
+    case MOE_ERR_DTYPE: return "MOE_ERR_DTYPE";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_INVALID_INDEX: return "MOE_ERR_INVALID_INDEX";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+  }
+  return "unknown moe_status";
+}
+
+// ---- routing -------------------------------------------------------------
+moe_status moe_route(const void* logits, moe_dtype ldt, int64_t T, int64_t E, int32_t top_k,
+                     int renormalize, uint32_t* idx, void* weights, float* weights_f32,
+                     cudaStream_t stream) {
+  if (!valid_dtype(ldt)) return fail(MOE_ERR_DTYPE, "logits dtype %d is not F32/F16/BF16", (int)ldt);
+  moe_status st = check_tek(T, E, top_k);
+  if (st != MOE_OK) return st;
+  if (T == 0) return ok();
+  if (!logits || !idx || !weights) return fail(MOE_ERR_INVALID_ARG, "logits, idx and weights must be non-NULL");
+  MOE_TRY_CUDA(moe::launch_route(logits, ldt, T, (int)E, top_k, renormalize, idx, weights,
+                                 weights_f32, nullptr, stream),
+               "routing kernel launch");
+  return ok();
+}
+
+// ---- dispatch ------------------------------------------------------------
+size_t moe_dispatch_workspace_size(int64_t T, int64_t E, int32_t top_k) {
+  (void)top_k;
+  if (T < 0 || E < 1 || E > kMaxE) return 0;
+  return kWsHeader + align_up(moe::dispatch_scratch_bytes(T, (int)E), 1024);
+}
+
+moe_status moe_dispatch(const uint32_t* idx, int64_t T, int64_t E, int32_t top_k, const void* x,
+                        moe_dtype x_dtype, int64_t H, uint32_t* offsets, uint32_t* row_experts,
+                        uint32_t* perm, void* x_disp, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  moe_status st = check_tek(T, E, top_k);
+  if (st != MOE_OK) return st;
+  if ((x == nullptr) != (x_disp == nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "x and x_disp must both be given or both be NULL");
+  if (x) {
+    if (!valid_dtype(x_dtype)) return fail(MOE_ERR_DTYPE, "x dtype %d is not F32/F16/BF16", (int)x_dtype);
+    if ((st = check_dim(H, "H")) != MOE_OK) return st;
+  }
+  if (!offsets || !perm) return fail(MOE_ERR_INVALID_ARG, "offsets and perm must be non-NULL");
+  if (T == 0) {
+    // no rows: offsets are all zero
+    MOE_TRY_CUDA(cudaMemsetAsync(offsets, 0, (size_t)(E + 1) * 4, stream), "cudaMemsetAsync");
+    return ok();
+  }
+  if (!idx) return fail(MOE_ERR_INVALID_ARG, "idx must be non-NULL");
+  if ((st = check_ws(ws, ws_bytes, moe_dispatch_workspace_size(T, E, top_k))) != MOE_OK) return st;
+  MOE_TRY_CUDA(moe::launch_dispatch(idx, T, (int)E, top_k, offsets, row_experts, perm,
+                                    static_cast<char*>(ws) + kWsHeader, status_word(ws), stream),
+               "dispatch kernel launch");
+  if (x)
+    MOE_TRY_CUDA(moe::launch_gather(x, x_dtype, H, top_k, perm, offsets, (int)E, T * top_k, x_disp,
+                                    stream),
+                 "gather kernel launch");
+  return ok();
+}
+
+// ---- experts -------------------------------------------------------------
+moe_status moe_experts_create(const void* gate, const void* up, const void* down, moe_dtype dt,
+                              int64_t E, int64_t I, int64_t H, moe_experts_t* out) {
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "out handle pointer is NULL");
+  *out = nullptr;
+  if (!valid_dtype(dt)) return fail(MOE_ERR_DTYPE, "expert weight dtype %d is not F32/F16/BF16", (int)dt);
+  if (E < 1 || I < 1 || H < 1)
+    return fail(MOE_ERR_SHAPE, "MoE expert weight dimensions must be non-zero (E=%lld I=%lld H=%lld)",
+                (long long)E, (long long)I, (long long)H);
+  if (E > kMaxE) return fail(MOE_ERR_UNSUPPORTED, "E=%lld exceeds the supported 1024", (long long)E);
+  moe_status st;
+  if ((st = check_dim(I, "I")) != MOE_OK || (st = check_dim(H, "H")) != MOE_OK) return st;
+  if ((unsigned __int128)E * I * H * dtype_size(dt) >= ((unsigned __int128)1 << 62))
+    return fail(MOE_ERR_SHAPE, "expert weight element count overflows");
+  if (!gate || !up || !down) return fail(MOE_ERR_INVALID_ARG, "gate, up and down must be non-NULL");
+  if (!aligned16(gate) || !aligned16(up) || !aligned16(down))
+    return fail(MOE_ERR_INVALID_ARG, "expert weights must be 16-byte aligned");
+  int dev = -1;
+  MOE_TRY_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  const void* ptrs[3] = {gate, up, down};
+  for (const void* p : ptrs) {
+    cudaPointerAttributes a{};
+    MOE_TRY_CUDA(cudaPointerGetAttributes(&a, p), "cudaPointerGetAttributes");
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+      return fail(MOE_ERR_INVALID_ARG, "expert weights must be device memory");
+    if (a.device != dev)
+      return fail(MOE_ERR_INVALID_ARG, "expert weights must live on the current device %d", dev);
+  }
+  int sms = 0;
+  MOE_TRY_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute");
+  moe_experts* x = new moe_experts{gate, up, down, dt, E, I, H, dev, sms, nullptr};
+  if (moe::tc_supported(dt, I, H)) {
+    const char* err = "";
+    x->tc = moe::tc_weights_create(gate, up, down, dt, E, I, H, &err);
+    if (!x->tc) {
+      delete x;
+      return fail(MOE_ERR_CUDA, "%s", err);
+    }
+  }
+  *out = x;
+  return ok();
+}
+
+void moe_experts_destroy(moe_experts_t x) {
+  if (!x) return;
+  moe::tc_weights_destroy(x->tc);
+  delete x;
+}
+
+size_t moe_experts_workspace_size(moe_experts_t x, int64_t N) {
+  if (!x || N < 0) return 0;
+  return kWsHeader + align_up((size_t)N * x->I * dtype_size(x->dt), 1024);
+}
+
+moe_status moe_experts_forward(moe_experts_t x, const void* x_disp, int64_t N, const uint32_t* offsets,
+                               void* expert_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  moe_status st = check_handle(x);
+  if (st != MOE_OK) return st;
+  if (N < 0 || N > kMaxRows) return fail(MOE_ERR_SHAPE, "N=%lld out of range", (long long)N);
+  if (N == 0) return ok();
+  if (!x_disp || !offsets || !expert_out)
+    return fail(MOE_ERR_INVALID_ARG, "x_disp, offsets and expert_out must be non-NULL");
+  if (!aligned16(x_disp) || !aligned16(expert_out))
+    return fail(MOE_ERR_INVALID_ARG, "x_disp and expert_out must be 16-byte aligned");
+  if ((st = check_ws(ws, ws_bytes, moe_experts_workspace_size(x, N))) != MOE_OK) return st;
+  MOE_TRY_CUDA(cudaMemsetAsync(ws, 0, 4, stream), "cudaMemsetAsync");
+  st = run_experts(x, x_disp, N, offsets, static_cast<char*>(ws) + kWsHeader, expert_out,
+                   moe::kDownPlain, nullptr, nullptr, MOE_F32, status_word(ws), stream, nullptr);
+  return st == MOE_OK ? ok() : st;
+}
+
+// ---- combine -------------------------------------------------------------
+size_t moe_combine_workspace_size(int64_t T, int32_t top_k) {
+  if (T < 0 || top_k < 1) return 0;
+  return kWsHeader + align_up((size_t)T * top_k * 4, 1024);
+}
+
+moe_status moe_combine(const void* expert_out, moe_dtype dt, const uint32_t* perm, const void* weights,
+                       moe_dtype wdt, int64_t T, int32_t top_k, int64_t H, void* y, void* ws,
+                       size_t ws_bytes, cudaStream_t stream) {
+  if (!valid_dtype(dt) || !valid_dtype(wdt)) return fail(MOE_ERR_DTYPE, "dtype is not F32/F16/BF16");
+  if (T < 0) return fail(MOE_ERR_SHAPE, "T must be >= 0");
+  if (top_k < 1) return fail(MOE_ERR_INVALID_ARG, "top_k must be >= 1");
+  if (top_k > kMaxK) return fail(MOE_ERR_UNSUPPORTED, "top_k=%d exceeds the supported 64", top_k);
+  if (T > kMaxRows / top_k) return fail(MOE_ERR_UNSUPPORTED, "T*top_k exceeds 2^31-1");
+  moe_status st = check_dim(H, "H");
+  if (st != MOE_OK) return st;
+  if (T == 0) return ok();
+  if (!expert_out || !perm || !weights || !y)
+    return fail(MOE_ERR_INVALID_ARG, "expert_out, perm, weights and y must be non-NULL");
+  if (!aligned16(expert_out) || !aligned16(y))
+    return fail(MOE_ERR_INVALID_ARG, "expert_out and y must be 16-byte aligned");
+  if ((st = check_ws(ws, ws_bytes, moe_combine_workspace_size(T, top_k))) != MOE_OK) return st;
+  uint32_t* slot_row = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + kWsHeader);
+  MOE_TRY_CUDA(moe::launch_invert_perm(perm, T * top_k, slot_row, stream), "perm inversion launch");
+  MOE_TRY_CUDA(moe::launch_combine(expert_out, dt, slot_row, weights, wdt, T, top_k, H, y, stream),
+               "combine kernel launch");
+  return ok();
+}
+
+// ---- fused forward -------------------------------------------------------
+size_t moe_forward_workspace_size(moe_experts_t x, int64_t T, int32_t top_k, moe_dtype ldt) {
+  if (!x || T < 0 || top_k < 1 || !valid_dtype(ldt)) return 0;
+  return forward_layout(x, T, top_k, ldt).total;
+}
+
+moe_status moe_forward_layout(moe_experts_t x, int64_t T, int32_t top_k, moe_dtype ldt,
+                              moe_forward_layout_t* out) {
+  if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "NULL handle or output");
+  if (T < 0 || top_k < 1 || !valid_dtype(ldt)) return fail(MOE_ERR_INVALID_ARG, "bad T, top_k or dtype");
+  const ForwardLayout L = forward_layout(x, T, top_k, ldt);
+  out->idx = L.idx;
+  out->weights = L.weights;
+  out->offsets = L.offsets;
+  out->perm = L.perm;
+  out->x_disp = L.x_disp;
+  out->h = L.h;
+  out->slots = L.slots;
+  out->total = L.total;
+  return ok();
+}
+
+moe_status moe_forward(moe_experts_t x, const void* xin, const void* logits, moe_dtype ldt, int64_t T,
+                       int32_t top_k, int renormalize, void* y, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+  return forward_impl(x, xin, logits, ldt, T, top_k, renormalize, y, ws, ws_bytes, stream, nullptr);
+}
+
+moe_status moe_forward_timed(moe_experts_t x, const void* xin, const void* logits, moe_dtype ldt,
+                             int64_t T, int32_t top_k, int renormalize, void* y, void* ws,
+                             size_t ws_bytes, cudaStream_t stream, void* const* events, int n_events) {
+  if (!events || n_events < 6) return fail(MOE_ERR_INVALID_ARG, "moe_forward_timed needs 6 events");
+  for (int i = 0; i < 6; ++i)
+    if (!events[i]) return fail(MOE_ERR_INVALID_ARG, "event %d is NULL", i);
+  return forward_impl(x, xin, logits, ldt, T, top_k, renormalize, y, ws, ws_bytes, stream, events);
+}
+
+size_t moe_forward_host_workspace_size(moe_experts_t x, int64_t T, int32_t top_k, moe_dtype ldt) {
+  if (!x || T < 0 || top_k < 1 || !valid_dtype(ldt)) return 0;
+  size_t total = forward_layout(x, T, top_k, ldt).total;
+  total += align_up((size_t)T * x->H * dtype_size(x->dt), 1024) * 2;
+  total += align_up((size_t)T * x->E * dtype_size(ldt), 1024);
+  return total;
+}
+
+moe_status moe_forward_host(moe_experts_t x, const void* x_host, const void* logits_host, moe_dtype ldt,
+                            int64_t T, int32_t top_k, int renormalize, void* y_host, void* ws,
+                            size_t ws_bytes, cudaStream_t stream) {
+  moe_status st = check_handle(x);
+  if (st != MOE_OK) return st;
+  if (!valid_dtype(ldt)) return fail(MOE_ERR_DTYPE, "logits dtype %d is not F32/F16/BF16", (int)ldt);
+  if ((st = check_tek(T, x->E, top_k)) != MOE_OK) return st;
+  if (T == 0) return ok();
+  if (!x_host || !logits_host || !y_host)
+    return fail(MOE_ERR_INVALID_ARG, "x_host, logits_host and y_host must be non-NULL");
+  if ((st = check_ws(ws, ws_bytes, moe_forward_host_workspace_size(x, T, top_k, ldt))) != MOE_OK)
+    return st;
+  const size_t base = forward_layout(x, T, top_k, ldt).total;
+  const size_t xb = (size_t)T * x->H * dtype_size(x->dt), lb = (size_t)T * x->E * dtype_size(ldt);
+  char* xs = static_cast<char*>(ws) + base;
+  char* ys = xs + align_up(xb, 1024);
+  char* ls = ys + align_up(xb, 1024);
+  MOE_TRY_CUDA(cudaMemcpyAsync(xs, x_host, xb, cudaMemcpyHostToDevice, stream), "cudaMemcpyAsync x");
+  MOE_TRY_CUDA(cudaMemcpyAsync(ls, logits_host, lb, cudaMemcpyHostToDevice, stream),
+               "cudaMemcpyAsync logits");
+  st = forward_impl(x, xs, ls, ldt, T, top_k, renormalize, ys, ws, base, stream, nullptr);
+  if (st != MOE_OK) return st;
+  MOE_TRY_CUDA(cudaMemcpyAsync(y_host, ys, xb, cudaMemcpyDeviceToHost, stream), "cudaMemcpyAsync y");
+  return ok();
+}
+
+moe_status moe_get_device_status(const void* ws, cudaStream_t stream) {
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  uint32_t v = 0;
+  MOE_TRY_CUDA(cudaMemcpyAsync(&v, ws, 4, cudaMemcpyDeviceToHost, stream), "cudaMemcpyAsync status");
+  MOE_TRY_CUDA(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
+  if (v == MOE_OK) return ok();
+  if (v == MOE_ERR_INVALID_INDEX) return fail(MOE_ERR_INVALID_INDEX, "an expert index >= E reached dispatch");
+  if (v == MOE_ERR_DEVICE_TIMEOUT)
+    return fail(MOE_ERR_DEVICE_TIMEOUT, "a bounded wait inside a kernel expired");
+  return fail(MOE_ERR_CUDA, "unknown device status %u", v);
+}
+
+}  // extern "C"

@@ -1,0 +1,143 @@
+// combine.cu -- weighted combine back to token order.
+//
+// ruDNN user guide ("ruDNN Benutzerhandbuch"), section 6 "MoE aufrufen":
+// combine uses the dispatch map to restore token order and merges the expert
+// outputs with the routing weights.  Here y[t,:] = sum_j w[t,j] * out[r(t,j),:]
+// with FP32 accumulation in ascending j (a fixed order, so the result is
+// bit-reproducible), rounded once to the output dtype.
+//
+// All kernels are HBM-bound streaming passes: each thread owns 8 consecutive
+// columns of one token (one 16-byte vector for 16-bit types, two for FP32)
+// and reads the k source rows of that token.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// slot_row[perm[r]] = r for every dispatched row (slot_row pre-filled with kInvalid)
+__global__ void invert_perm_kernel(const uint32_t* __restrict__ perm, int64_t N,
+                                   uint32_t* __restrict__ slot_row) {
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= N) return;
+  const uint32_t s = perm[r];
+  if (s < (uint64_t)N) slot_row[s] = (uint32_t)r;
+}
+
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float* f) {
+  if constexpr (sizeof(T) == 2) {
+    unpack8<T>(__ldg(reinterpret_cast<const uint4*>(p)), f);
+  } else {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void store8(T* p, const float* f) {
+  if constexpr (sizeof(T) == 2) {
+    *reinterpret_cast<uint4*>(p) = pack8<T>(f);
+  } else {
+    reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+  }
+}
+
+// WEIGHTED: y[t] = sum_j w[t,j] * src[slot_row[t*k+j]]   (moe_combine)
+// !WEIGHTED: y[t] = sum_j src[t*k+j]                      (fused forward)
+// VEC: H % 8 == 0 and 16-byte aligned rows, else one column per thread.
+template <typename T, bool WEIGHTED, bool VEC>
+__global__ void __launch_bounds__(256)
+combine_kernel(const T* __restrict__ src, const uint32_t* __restrict__ slot_row,
+               const void* __restrict__ w, int wdt, int64_t T_rows, int k, int64_t H,
+               T* __restrict__ y) {
+  constexpr int C = VEC ? 8 : 1;
+  const int64_t groups = H / C;
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= T_rows * groups) return;
+  const int64_t t = gid / groups;
+  const int64_t c0 = (gid - t * groups) * C;
+  float acc[C];
+#pragma unroll
+  for (int i = 0; i < C; ++i) acc[i] = 0.f;
+  for (int j = 0; j < k; ++j) {
+    int64_t row;
+    float wj = 1.f;
+    if constexpr (WEIGHTED) {
+      const uint32_t r = __ldg(slot_row + t * k + j);
+      wj = load_dyn(w, wdt, (size_t)(t * k + j));
+      if (r == kInvalid) {
+#pragma unroll
+        for (int i = 0; i < C; ++i) acc[i] = NAN;
+        continue;
+      }
+      row = r;
+    } else {
+      row = t * k + j;
+    }
+    float v[C];
+    if constexpr (VEC) {
+      load8<T>(src + row * H + c0, v);
+    } else {
+      v[0] = to_f32<T>(src[row * H + c0]);
+    }
+#pragma unroll
+    for (int i = 0; i < C; ++i) acc[i] += WEIGHTED ? wj * v[i] : v[i];
+  }
+  if constexpr (VEC) {
+    store8<T>(y + t * H + c0, acc);
+  } else {
+    y[t * H + c0] = from_f32<T>(acc[0]);
+  }
+}
+
+template <typename T, bool WEIGHTED>
+cudaError_t launch_combine_t(const void* src, const uint32_t* slot_row, const void* w, moe_dtype wdt,
+                             int64_t T_rows, int k, int64_t H, void* y, cudaStream_t s) {
+  const bool vec = H % 8 == 0 && reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(y) % 16 == 0;
+  const int64_t work = T_rows * (vec ? H / 8 : H);
+  const unsigned grid = (unsigned)((work + 255) / 256);
+  if (vec)
+    combine_kernel<T, WEIGHTED, true><<<grid, 256, 0, s>>>(
+        static_cast<const T*>(src), slot_row, w, (int)wdt, T_rows, k, H, static_cast<T*>(y));
+  else
+    combine_kernel<T, WEIGHTED, false><<<grid, 256, 0, s>>>(
+        static_cast<const T*>(src), slot_row, w, (int)wdt, T_rows, k, H, static_cast<T*>(y));
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_invert_perm(const uint32_t* perm, int64_t N, uint32_t* slot_row, cudaStream_t s) {
+  cudaError_t err = cudaMemsetAsync(slot_row, 0xFF, (size_t)N * sizeof(uint32_t), s);
+  if (err != cudaSuccess) return err;
+  invert_perm_kernel<<<(unsigned)((N + 255) / 256), 256, 0, s>>>(perm, N, slot_row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* expert_out, moe_dtype dt, const uint32_t* slot_row,
+                           const void* weights, moe_dtype wdt, int64_t T, int k, int64_t H,
+                           void* y, cudaStream_t s) {
+  switch (dt) {
+    case MOE_F32: return launch_combine_t<float, true>(expert_out, slot_row, weights, wdt, T, k, H, y, s);
+    case MOE_F16: return launch_combine_t<__half, true>(expert_out, slot_row, weights, wdt, T, k, H, y, s);
+    default: return launch_combine_t<__nv_bfloat16, true>(expert_out, slot_row, weights, wdt, T, k, H, y, s);
+  }
+}
+
+cudaError_t launch_slot_sum(const void* slots, moe_dtype dt, int64_t T, int k, int64_t H, void* y,
+                            cudaStream_t s) {
+  switch (dt) {
+    case MOE_F32: return launch_combine_t<float, false>(slots, nullptr, nullptr, dt, T, k, H, y, s);
+    case MOE_F16: return launch_combine_t<__half, false>(slots, nullptr, nullptr, dt, T, k, H, y, s);
+    default: return launch_combine_t<__nv_bfloat16, false>(slots, nullptr, nullptr, dt, T, k, H, y, s);
+  }
+}
+
+}  // namespace moe

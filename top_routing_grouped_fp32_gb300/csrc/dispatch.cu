@@ -1,0 +1,245 @@
+// dispatch.cu -- deterministic capacity-free dispatch.
+//
+// The ruDNN user guide ("ruDNN Benutzerhandbuch"), section 5 "Expertengewichte
+// und Verteilung", asks for a dispatch that drops no token and keeps a stored
+// map that restores token order; its own slot order inside an expert is left
+// unspecified (atomic).  The DispatchedTokens comment in src/moe/experts.rs
+// states the invariant: complete, monotone expert segments.  Here the slot
+// order is fixed: segment e lists its slots s = t*k + j in ascending s, i.e. a
+// stable counting sort of the slots by expert id, so the result is
+// bit-reproducible.
+//
+// Three kernels:
+//  1. count:   per 256-token chunk, a shared-memory histogram of experts
+//              (column E counts indices >= E).  Order-independent atomics.
+//  2. scan:    one block turns the chunk histograms into offsets[E+1] and the
+//              first row of every (chunk, expert) pair; it also writes the
+//              device status and fills the unused tail of perm/row_experts.
+//  3. scatter: each warp walks its 32 tokens in order; lanes hold the k slots
+//              of one token and __match_any_sync ranks equal experts among
+//              them, so ranks follow s exactly, duplicates included.  A first
+//              pass counts per warp, a second writes perm/row_experts.
+// A fourth kernel gathers x rows into x_disp, one warp per dispatched row.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = kDispatchChunk / 32;  // 8 warps, 32 tokens each
+
+__global__ void __launch_bounds__(256)
+count_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
+             uint32_t* __restrict__ chunk_counts) {
+  extern __shared__ uint32_t cnt[];  // E + 1
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const int64_t t0 = (int64_t)blockIdx.x * kDispatchChunk;
+  const int64_t t1 = min(T, t0 + kDispatchChunk);
+  const int64_t s0 = t0 * k, s1 = t1 * k;
+  for (int64_t s = s0 + threadIdx.x; s < s1; s += blockDim.x) {
+    const uint32_t e = __ldg(idx + s);
+    atomicAdd(&cnt[e < (uint32_t)E ? e : (uint32_t)E], 1u);
+  }
+  __syncthreads();
+  uint32_t* out = chunk_counts + (size_t)blockIdx.x * (E + 1);
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) out[i] = cnt[i];
+}
+
+// Inclusive block scan of one value per thread (blockDim.x <= 1024).
+__device__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* warp_sums) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    uint32_t o = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v += o;
+  }
+  if (lane == 31) warp_sums[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    const int nw = (blockDim.x + 31) >> 5;
+    uint32_t x = lane < nw ? warp_sums[lane] : 0u;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      uint32_t o = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += o;
+    }
+    if (lane < nw) warp_sums[lane] = x;
+  }
+  __syncthreads();
+  if (w > 0) v += warp_sums[w - 1];
+  __syncthreads();
+  return v;
+}
+
+__global__ void __launch_bounds__(1024)
+scan_kernel(const uint32_t* __restrict__ chunk_counts, int nchunks, int E, int64_t N,
+            uint32_t* __restrict__ offsets, uint32_t* __restrict__ chunk_base,
+            uint32_t* __restrict__ perm, uint32_t* __restrict__ row_experts,
+            uint32_t* __restrict__ status) {
+  __shared__ uint32_t warp_sums[32];
+  __shared__ uint32_t s_total_valid;
+  // E <= 1024 = blockDim.x: thread e owns expert e
+  const int e = threadIdx.x;
+  uint32_t total = 0;
+  if (e < E)
+    for (int b = 0; b < nchunks; ++b) total += chunk_counts[(size_t)b * (E + 1) + e];
+  const uint32_t incl = block_inclusive_scan(total, warp_sums);
+  if (e < E) {
+    const uint32_t start = incl - total;
+    offsets[e] = start;
+    uint32_t run = start;
+    for (int b = 0; b < nchunks; ++b) {
+      chunk_base[(size_t)b * E + e] = run;
+      run += chunk_counts[(size_t)b * (E + 1) + e];
+    }
+    if (e == E - 1) {
+      offsets[E] = incl;
+      s_total_valid = incl;
+    }
+  }
+  if (threadIdx.x == 0) {  // column E counts indices >= E
+    uint32_t invalid = 0;
+    for (int b = 0; b < nchunks; ++b) invalid += chunk_counts[(size_t)b * (E + 1) + E];
+    if (status) *status = invalid ? (uint32_t)MOE_ERR_INVALID_INDEX : 0u;
+  }
+  __syncthreads();
+  // slots that were not dispatched leave the tail of perm / row_experts unused
+  for (int64_t r = (int64_t)s_total_valid + threadIdx.x; r < N; r += blockDim.x) {
+    perm[r] = kInvalid;
+    if (row_experts) row_experts[r] = kInvalid;
+  }
+}
+
+__global__ void __launch_bounds__(256)
+scatter_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
+               const uint32_t* __restrict__ chunk_base, uint32_t* __restrict__ perm,
+               uint32_t* __restrict__ row_experts) {
+  extern __shared__ uint32_t smem[];
+  uint32_t* wcnt = smem;  // [kWarps][E]: per-warp counters / running bases
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const int64_t tw = (int64_t)blockIdx.x * kDispatchChunk + w * 32;
+  uint32_t* my = wcnt + w * E;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+
+  // pass 1: per-warp counts
+  for (int i = 0; i < 32; ++i) {
+    const int64_t t = tw + i;
+    if (t >= T) break;
+    for (int j0 = 0; j0 < k; j0 += 32) {
+      const int j = j0 + lane;
+      const uint32_t e = j < k ? __ldg(idx + t * k + j) : kInvalid;
+      const bool ok = e < (uint32_t)E;
+      const uint32_t key = ok ? e : kInvalid;
+      const uint32_t grp = __match_any_sync(0xffffffffu, key);
+      if (ok && (grp & lt_mask) == 0) my[e] += __popc(grp);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // per-expert exclusive prefix over the warps, starting at the chunk's base
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    uint32_t run = chunk_base[(size_t)blockIdx.x * E + e];
+    for (int ww = 0; ww < kWarps; ++ww) {
+      const uint32_t c = wcnt[ww * E + e];
+      wcnt[ww * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // pass 2: the same walk, now writing rows
+  for (int i = 0; i < 32; ++i) {
+    const int64_t t = tw + i;
+    if (t >= T) break;
+    for (int j0 = 0; j0 < k; j0 += 32) {
+      const int j = j0 + lane;
+      const uint32_t e = j < k ? __ldg(idx + t * k + j) : kInvalid;
+      const bool ok = e < (uint32_t)E;
+      const uint32_t key = ok ? e : kInvalid;
+      const uint32_t grp = __match_any_sync(0xffffffffu, key);
+      uint32_t base = ok ? my[e] : 0u;
+      __syncwarp();
+      if (ok) {
+        const uint32_t r = base + __popc(grp & lt_mask);
+        perm[r] = (uint32_t)(t * k + j);
+        if (row_experts) row_experts[r] = e;
+        if ((grp & lt_mask) == 0) my[e] = base + __popc(grp);
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// x_disp[r,:] = x[perm[r] / k, :] for r < offsets[E]; one warp per row.
+template <int VEC_BYTES>
+__global__ void __launch_bounds__(256)
+gather_kernel(const char* __restrict__ x, int64_t row_bytes, int k, const uint32_t* __restrict__ perm,
+              const uint32_t* __restrict__ offsets, int E, int64_t N, char* __restrict__ x_disp) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= N) return;
+  const uint32_t valid_rows = __ldg(offsets + E);
+  if (r >= (int64_t)valid_rows) return;
+  const int64_t t = __ldg(perm + r) / (uint32_t)k;
+  const char* src = x + t * row_bytes;
+  char* dst = x_disp + r * row_bytes;
+  if constexpr (VEC_BYTES == 16) {
+    const int64_t nv = row_bytes / 16;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    int64_t v = lane;
+    for (; v + 3 * 32 < nv; v += 4 * 32) {
+      uint4 a = __ldg(s4 + v), b = __ldg(s4 + v + 32), c = __ldg(s4 + v + 64), d = __ldg(s4 + v + 96);
+      d4[v] = a;
+      d4[v + 32] = b;
+      d4[v + 64] = c;
+      d4[v + 96] = d;
+    }
+    for (; v < nv; v += 32) d4[v] = __ldg(s4 + v);
+  } else {
+    const int64_t nv = row_bytes / 2;
+    const uint16_t* s2 = reinterpret_cast<const uint16_t*>(src);
+    uint16_t* d2 = reinterpret_cast<uint16_t*>(dst);
+    for (int64_t v = lane; v < nv; v += 32) d2[v] = s2[v];
+  }
+}
+
+}  // namespace
+
+size_t dispatch_scratch_bytes(int64_t T, int E) {
+  const int64_t nc = dispatch_chunks(T);
+  return align_up((size_t)nc * (E + 1) * 4, 256) + align_up((size_t)nc * E * 4, 256);
+}
+
+cudaError_t launch_dispatch(const uint32_t* idx, int64_t T, int E, int k, uint32_t* offsets,
+                            uint32_t* row_experts, uint32_t* perm, void* scratch,
+                            uint32_t* status, cudaStream_t s) {
+  const int64_t nc = dispatch_chunks(T);
+  uint32_t* counts = static_cast<uint32_t*>(scratch);
+  uint32_t* bases = reinterpret_cast<uint32_t*>(static_cast<char*>(scratch) +
+                                                align_up((size_t)nc * (E + 1) * 4, 256));
+  count_kernel<<<(unsigned)nc, 256, (E + 1) * sizeof(uint32_t), s>>>(idx, T, E, k, counts);
+  scan_kernel<<<1, 1024, 0, s>>>(counts, (int)nc, E, T * k, offsets, bases, perm, row_experts, status);
+  const size_t smem = (size_t)kWarps * E * sizeof(uint32_t);
+  scatter_kernel<<<(unsigned)nc, 256, smem, s>>>(idx, T, E, k, bases, perm, row_experts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const void* x, moe_dtype dt, int64_t H, int k, const uint32_t* perm,
+                          const uint32_t* offsets, int E, int64_t N, void* x_disp, cudaStream_t s) {
+  const int64_t row_bytes = H * (int64_t)dtype_size(dt);
+  const unsigned grid = (unsigned)((N + 7) / 8);
+  const bool vec = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(x_disp) % 16 == 0;
+  if (vec)
+    gather_kernel<16><<<grid, 256, 0, s>>>(static_cast<const char*>(x), row_bytes, k, perm, offsets,
+                                           E, N, static_cast<char*>(x_disp));
+  else
+    gather_kernel<2><<<grid, 256, 0, s>>>(static_cast<const char*>(x), row_bytes, k, perm, offsets,
+                                          E, N, static_cast<char*>(x_disp));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,618 @@
+// gemm_tc.cu -- persistent segmented grouped GEMM on Blackwell tensor cores.
+//
+// Computes the three expert products of SwiGluExperts::forward_dispatched_with_
+// strategy in src/moe/experts.rs (ruDNN 0.1.25 source view): for every
+// dispatched row r of expert e, A[r,:] . W[e]^T, with
+//   gate/up : both products in one accumulator tile, epilogue h = silu(g) * u
+//             (silu(z) = z * sigmoid(z), MindSpeed-Ops PR 163, rms_norm_gated
+//             notes), stored as the 16-bit operand of the down product;
+//   down    : o = h . W_down[e]^T, stored either in dispatch order
+//             (moe_experts_forward) or multiplied by the routing weight of
+//             its slot and stored at that token slot (fused forward: the
+//             weight scale and the un-permute of the user guide's combine,
+//             section 6, move into this epilogue).
+// The pages' own grouped product is a scalar or "cooperative matrix" loop
+// (prior art); this is an sm_103a design:
+//
+//   * one CTA per SM, persistent over a tile list: tiles are 128 rows x 256
+//     FP32 accumulator columns of one expert; the list is built on the device
+//     from offsets[] (segment lengths are never read by the host);
+//   * warp 0: TMA producer (cp.async.bulk.tensor, 128-byte swizzle) filling a
+//     4-stage ring of {A 128x64, B 256x64} 16-bit tiles; the B tile is two
+//     128-row boxes (gate rows + up rows, or two halves of the down rows);
+//   * warp 1: allocates 512 TMEM columns and issues tcgen05.mma (kind::f16,
+//     M=128, N=256, K=16, FP32 accumulate) from one thread; tcgen05.commit
+//     frees a ring stage and signals a finished accumulator;
+//   * warps 2-5: epilogue; each reads its 32 TMEM lanes (= 32 tile rows) with
+//     tcgen05.ld while the MMA warp fills the other accumulator;
+//   * rows past the end of a segment are computed (the A box may run into the
+//     next expert's rows or past the buffer, where TMA fills zeros) and never
+//     stored, so segments of any length are handled without padding;
+//   * tiles are visited expert by expert; inside an expert, column panels of
+//     `panel` n-blocks are swept over all its m-tiles so that CTAs running at
+//     the same time share weight tiles in L2.
+//
+// Every wait on an mbarrier is bounded: after ~2 s the CTA records
+// MOE_ERR_DEVICE_TIMEOUT in the workspace status word, stops issuing work,
+// waits (bounded) for its own copies and MMAs in flight, frees its TMEM and
+// returns.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;        // FP32 accumulator columns per tile
+constexpr int BK = 64;         // 64 16-bit elements = one 128-byte swizzle row
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;        // 16 KiB
+constexpr uint32_t B_HALF_BYTES = 128 * BK * 2;  // 16 KiB
+constexpr uint32_t STAGE_BYTES = A_BYTES + 2 * B_HALF_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int MAX_E = 1024;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+struct Params {
+  const uint32_t* offsets;
+  int E;
+  int nb;             // n-blocks per m-tile
+  int panel;          // n-blocks per raster panel
+  int k_blocks;
+  int mode;
+  int cols_per_tile;  // output columns per tile: 128 (gate/up) or 256 (down)
+  int b1_row_off;     // row offset of the second B box inside the n-block
+  int64_t n_out;
+  void* out;
+  const uint32_t* perm;
+  const void* weights;
+  int wdt;
+  uint32_t* status;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+// Bounded wait for phase `parity` of `bar`.  Returns false if the CTA is
+// aborting or the time limit passed (then the abort flag and status are set).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                       uint32_t* status) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_test(bar, parity)) return true;
+    if ((n & 127u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer() - t0 > kWaitLimitNs) {
+        *abort_flag = 1u;
+        set_status(status, (uint32_t)MOE_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+               "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+               : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, both K-major, one 128x256x16 step.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+// 32 consecutive FP32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4)      // start address
+         | ((uint64_t)1 << 16)                     // leading offset (unused here)
+         | ((uint64_t)(1024 >> 4) << 32)           // stride offset between 8-row groups
+         | ((uint64_t)1 << 46)                     // descriptor version
+         | ((uint64_t)2 << 61);                    // 128-byte swizzle
+}
+// Instruction descriptor: FP32 accumulator, 16-bit A/B (bf16 or f16), both
+// K-major, M = 128, N = 256.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- tile list
+struct Tile {
+  int e;
+  int nb;
+  int64_t m0;
+  int rows;
+};
+
+__device__ __forceinline__ Tile decode_tile(uint32_t tile, const Params& p, const uint32_t* s_pref,
+                                            const uint32_t* s_off) {
+  const uint32_t q = tile / (uint32_t)p.nb;
+  int lo = 0, hi = p.E;  // s_pref[lo] <= q < s_pref[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_pref[mid] <= q) lo = mid; else hi = mid;
+  }
+  const uint32_t mte = s_pref[lo + 1] - s_pref[lo];
+  const uint32_t L = tile - s_pref[lo] * (uint32_t)p.nb;
+  const uint32_t w = (uint32_t)p.panel;
+  const uint32_t pid = L / (mte * w);
+  const uint32_t rem = L - pid * mte * w;
+  const uint32_t width = min(w, (uint32_t)p.nb - pid * w);
+  Tile t;
+  t.e = lo;
+  t.nb = (int)(pid * w + rem % width);
+  t.m0 = (int64_t)s_off[lo] + (int64_t)(rem / width) * BM;
+  const int64_t left = (int64_t)s_off[lo + 1] - t.m0;
+  t.rows = (int)(left < BM ? left : BM);
+  return t;
+}
+
+// ---------------------------------------------------------------- the kernel
+template <typename T>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
+                const __grid_constant__ CUtensorMap mapB1, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  const uint32_t ring = (raw_s + 1023u) & ~1023u;  // 1024-byte aligned for the swizzle
+  uint8_t* ring_ptr = smem_raw + (ring - raw_s);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  uint32_t* s_off = reinterpret_cast<uint32_t*>(ring_ptr + STAGES * STAGE_BYTES + 256);
+  uint32_t* s_pref = s_off + (p.E + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_map(&mapA);
+    prefetch_map(&mapB0);
+    prefetch_map(&mapB1);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  for (int i = threadIdx.x; i <= E; i += THREADS) s_off[i] = p.offsets[i];
+  __syncthreads();
+  if (warp == 2) {  // s_pref[e] = number of 128-row tiles of experts < e
+    const int per = (E + 31) / 32;
+    uint32_t loc = 0;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) loc += (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+    }
+    uint32_t incl = loc;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    uint32_t run = incl - loc;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        s_pref[e] = run;
+        run += (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+      }
+    }
+    if (lane == 31) s_pref[E] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t total_tiles = s_pref[E] * (uint32_t)p.nb;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t last_fill[STAGES];
+      bool filled[STAGES];
+      for (int s = 0; s < STAGES; ++s) filled[s] = false, last_fill[s] = 0;
+      bool ok = true;
+      for (uint32_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile(tile, p, s_pref, s_off);
+        const int b0row = t.nb * p.cols_per_tile;
+        const int b1row = b0row + p.b1_row_off;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = ring + stage * STAGE_BYTES;
+          mbar_expect_tx(full_bar(stage), STAGE_BYTES);
+          tma_load_2d(sa, &mapA, kb * BK, (int)t.m0, full_bar(stage));
+          tma_load_3d(sa + A_BYTES, &mapB0, kb * BK, b0row, t.e, full_bar(stage));
+          tma_load_3d(sa + A_BYTES + B_HALF_BYTES, &mapB1, kb * BK, b1row, t.e, full_bar(stage));
+          filled[stage] = true;
+          last_fill[stage] = phase;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // aborting: let this CTA's copies in flight land before exit
+        for (int s = 0; s < STAGES; ++s) {
+          if (!filled[s]) continue;
+          const uint64_t t0 = global_timer();
+          while (!mbar_test(full_bar(s), last_fill[s]) && global_timer() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(sizeof(T) == 2 && !std::is_same<T, __half>::value);
+      int stage = 0;
+      uint32_t phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (uint32_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = ring + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            umma_f16(d_tmem, sw128_desc(sa + kk * UMMA_K * 2), sw128_desc(sb + kk * UMMA_K * 2),
+                     idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(stage));  // ring stage free once these MMAs finish
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));  // accumulator ready for the epilogue
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // every MMA this thread issued must be complete before TMEM is freed
+      umma_commit(drain_bar);
+      const uint64_t t0 = global_timer();
+      while (!mbar_test(drain_bar, 0) && global_timer() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // this warp may access TMEM lanes 32*quarter .. +31
+    const int row = quarter * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    T* out = static_cast<T*>(p.out);
+    for (uint32_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile(tile, p, s_pref, s_off);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      const bool row_ok = row < t.rows;
+      const int64_t grow = t.m0 + row;
+      if (p.mode == kGateUpSwiglu) {
+        const int64_t col0 = (int64_t)t.nb * 128;
+        T* dst = out + grow * p.n_out + col0;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c, g);
+          tmem_ld32(taddr + 128 + c, u);
+          tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (col0 + c + v * 8 + 8 <= p.n_out) {
+                float f[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float gg = __uint_as_float(g[v * 8 + i]);
+                  const float uu = __uint_as_float(u[v * 8 + i]);
+                  f[i] = gg / (1.f + __expf(-gg)) * uu;
+                }
+                *reinterpret_cast<uint4*>(dst + c + v * 8) = pack8<T>(f);
+              }
+            }
+          }
+        }
+      } else {
+        int64_t orow = grow;
+        float scale = 1.f;
+        if (p.mode == kDownWeighted && row_ok) {
+          const uint32_t s = __ldg(p.perm + grow);
+          orow = s;
+          scale = load_dyn(p.weights, p.wdt, s);
+        }
+        const int64_t col0 = (int64_t)t.nb * 256;
+        T* dst = out + orow * p.n_out + col0;
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(taddr + c, o);
+          tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (col0 + c + v * 8 + 8 <= p.n_out) {
+                float f[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[v * 8 + i]) * scale;
+                *reinterpret_cast<uint4*>(dst + c + v * 8) = pack8<T>(f);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+CUtensorMapDataType tmap_type(moe_dtype dt) {
+  return dt == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+// rows x cols (cols contiguous), box 128 rows x 64 columns
+bool encode_2d(CUtensorMap* m, const void* base, moe_dtype dt, uint64_t rows, uint64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, 128u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, tmap_type(dt), 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// experts x rows x cols (cols contiguous), box 1 x 128 x 64
+bool encode_3d(CUtensorMap* m, const void* base, moe_dtype dt, uint64_t E, uint64_t rows,
+               uint64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cols, rows, E};
+  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint32_t box[3] = {(cuuint32_t)BK, 128u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(m, tmap_type(dt), 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t smem_bytes(int E) { return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + 8 * (size_t)(E + 1); }
+
+template <typename T>
+cudaError_t launch_t(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB0,
+                     const CUtensorMap& mB1, const Params& p, int grid, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(grouped_gemm_tc<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem_bytes(MAX_E));
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  grouped_gemm_tc<T><<<grid, THREADS, smem_bytes(a.E), s>>>(mA, mB0, mB1, p);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+struct TcWeights {
+  CUtensorMap gate;  // CUtensorMap carries its own 64-byte alignment
+  CUtensorMap up;
+  CUtensorMap down;
+  int64_t E, I, H;
+};
+
+bool tc_supported(moe_dtype dt, int64_t I, int64_t H) {
+  return (dt == MOE_BF16 || dt == MOE_F16) && I % 8 == 0 && H % 8 == 0;
+}
+
+TcWeights* tc_weights_create(const void* gate, const void* up, const void* down, moe_dtype dt,
+                             int64_t E, int64_t I, int64_t H, const char** err) {
+  if (!tc::encode_fn()) {
+    *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return nullptr;
+  }
+  TcWeights* w = new TcWeights();
+  w->E = E;
+  w->I = I;
+  w->H = H;
+  if (!tc::encode_3d(&w->gate, gate, dt, E, I, H) || !tc::encode_3d(&w->up, up, dt, E, I, H) ||
+      !tc::encode_3d(&w->down, down, dt, E, H, I)) {
+    *err = "cuTensorMapEncodeTiled rejected an expert weight tensor";
+    delete w;
+    return nullptr;
+  }
+  return w;
+}
+
+void tc_weights_destroy(TcWeights* w) { delete w; }
+
+cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, cudaStream_t s) {
+  CUtensorMap mA;
+  if (!tc::encode_2d(&mA, a.A, a.dt, (uint64_t)a.N, (uint64_t)a.K)) return cudaErrorInvalidValue;
+  tc::Params p{};
+  p.offsets = a.offsets;
+  p.E = a.E;
+  p.mode = a.mode;
+  p.n_out = a.n_out;
+  p.out = a.out;
+  p.perm = a.perm;
+  p.weights = a.weights;
+  p.wdt = (int)a.wdt;
+  p.status = a.status;
+  p.k_blocks = (int)((a.K + tc::BK - 1) / tc::BK);
+  const CUtensorMap* b0;
+  const CUtensorMap* b1;
+  if (a.mode == kGateUpSwiglu) {
+    p.cols_per_tile = 128;
+    p.b1_row_off = 0;
+    b0 = &w->gate;
+    b1 = &w->up;
+  } else {
+    p.cols_per_tile = 256;
+    p.b1_row_off = 128;
+    b0 = &w->down;
+    b1 = &w->down;
+  }
+  p.nb = (int)((a.n_out + p.cols_per_tile - 1) / p.cols_per_tile);
+  const int64_t mt_max = (a.N + tc::BM - 1) / tc::BM + std::min<int64_t>(a.E, a.N);
+  const int64_t tiles_max = mt_max * p.nb;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, tiles_max));
+  // panel width: about one wave of CTAs spread over an expert's expected m-tiles
+  const int64_t mt_per_expert = std::max<int64_t>(1, (a.N + (int64_t)tc::BM * a.E - 1) / ((int64_t)tc::BM * a.E));
+  p.panel = (int)std::max<int64_t>(1, std::min<int64_t>(p.nb, (grid + mt_per_expert - 1) / mt_per_expert));
+  if (a.dt == MOE_BF16) return tc::launch_t<__nv_bfloat16>(a, mA, *b0, *b1, p, grid, s);
+  return tc::launch_t<__half>(a, mA, *b0, *b1, p, grid, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,70 @@
+// internal.h -- launchers shared between the translation units of the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---- routing (route.cu) ----------------------------------------------------
+cudaError_t launch_route(const void* logits, moe_dtype ldt, int64_t T, int E, int k, int renorm,
+                         uint32_t* idx, void* weights, float* w32, uint32_t* status_reset,
+                         cudaStream_t s);
+
+// ---- dispatch (dispatch.cu) ------------------------------------------------
+constexpr int kDispatchChunk = 256;  // tokens per block of the dispatch kernels
+inline int64_t dispatch_chunks(int64_t T) { return (T + kDispatchChunk - 1) / kDispatchChunk; }
+// bytes of scratch the dispatch kernels need (chunk counts and chunk bases)
+size_t dispatch_scratch_bytes(int64_t T, int E);
+cudaError_t launch_dispatch(const uint32_t* idx, int64_t T, int E, int k, uint32_t* offsets,
+                            uint32_t* row_experts, uint32_t* perm, void* scratch,
+                            uint32_t* status, cudaStream_t s);
+cudaError_t launch_gather(const void* x, moe_dtype dt, int64_t H, int k, const uint32_t* perm,
+                          const uint32_t* offsets, int E, int64_t N, void* x_disp, cudaStream_t s);
+
+// ---- combine (combine.cu) --------------------------------------------------
+cudaError_t launch_invert_perm(const uint32_t* perm, int64_t N, uint32_t* slot_row, cudaStream_t s);
+cudaError_t launch_combine(const void* expert_out, moe_dtype dt, const uint32_t* slot_row,
+                           const void* weights, moe_dtype wdt, int64_t T, int k, int64_t H,
+                           void* y, cudaStream_t s);
+// y[t] = sum_j slots[t*k+j] (weights already applied), ascending j
+cudaError_t launch_slot_sum(const void* slots, moe_dtype dt, int64_t T, int k, int64_t H, void* y,
+                            cudaStream_t s);
+
+// ---- grouped GEMMs ---------------------------------------------------------
+enum GemmMode { kGateUpSwiglu = 0, kDownPlain = 1, kDownWeighted = 2 };
+
+struct GemmArgs {
+  int mode;
+  moe_dtype dt;
+  int E;
+  int64_t N;          // rows of the A operand (dispatched rows)
+  int64_t K;          // reduction length
+  int64_t n_out;      // output columns (I for gate/up, H for down)
+  const void* A;      // [N, K]
+  const void* B0;     // gate (gate/up) or down weights
+  const void* B1;     // up (gate/up) or nullptr
+  const uint32_t* offsets;
+  void* out;          // [N, n_out] (or [T*k, n_out] slots for weighted mode)
+  const uint32_t* perm;
+  const void* weights;
+  moe_dtype wdt;
+  uint32_t* status;
+};
+
+// SIMT FP32-accumulate path (gemm_simt.cu): any dtype and shape
+cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
+
+// tcgen05 path (gemm_tc.cu): F16/BF16, K and n_out multiples of 8, 16-byte aligned
+struct TcWeights;  // prebuilt tensor maps of one expert-weight set
+TcWeights* tc_weights_create(const void* gate, const void* up, const void* down, moe_dtype dt,
+                             int64_t E, int64_t I, int64_t H, const char** err);
+void tc_weights_destroy(TcWeights* w);
+cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, cudaStream_t s);
+bool tc_supported(moe_dtype dt, int64_t I, int64_t H);
+
+}  // namespace moe

@@ -1,0 +1,198 @@
+// route.cu -- softmax / top-k routing, one warp per token row.
+//
+// Implements the routing contract of the ruDNN user guide ("ruDNN
+// Benutzerhandbuch"), section 4 "Routing-Vertrag": softmax over all experts in
+// FP32 before the top-k selection, ties to the lower expert id, optional
+// renormalisation of the selected weights followed by a cast to the logits
+// dtype, NaN weights for rows holding NaN, +inf or only -inf.
+//
+// Readings of the contract used here:
+//  * the selection key is the logit itself (softmax is strictly monotone, so
+//    the k largest logits are the k largest probabilities, and the key is
+//    exact in every logits dtype); equal logits go to the lower id, +0 == -0;
+//  * slot j of a row holds the j-th selection (descending weight);
+//  * a poisoned row is all-tied: idx = 0..k-1, weights NaN;
+//  * renormalisation divides by the FP32 sum of the k selected values added
+//    in slot order; weights are always stored in the logits dtype.
+//
+// Design: a row of E <= 1024 logits is held in registers, VPL = E/32 values
+// per lane in a blocked layout (lane l owns experts l*VPL .. l*VPL+VPL-1) so
+// that each lane reads its share with one or a few vector loads.  Max, sum and
+// each of the k arg-max rounds are warp butterflies; a butterfly leaves the
+// bit-identical value in every lane, so every lane agrees on each winner.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kRowsPerBlock = 8;  // 8 warps of 32 threads
+
+// (va, ia) beats (vb, ib): larger logit, then lower id.
+__device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+template <typename T, int VPL>
+__device__ __forceinline__ void load_row(const T* row, int E, int lane, float (&v)[VPL]) {
+  const int e0 = lane * VPL;
+  constexpr int kBytes = VPL * (int)sizeof(T);
+  const T* p = row + e0;
+  bool full = e0 + VPL <= E;
+  if (kBytes >= 4 && full && (reinterpret_cast<uintptr_t>(p) % (kBytes >= 16 ? 16 : kBytes)) == 0) {
+    if constexpr (kBytes >= 16) {
+      alignas(16) T buf[VPL];
+#pragma unroll
+      for (int c = 0; c < kBytes / 16; ++c)
+        reinterpret_cast<uint4*>(buf)[c] = __ldg(reinterpret_cast<const uint4*>(p) + c);
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) v[i] = to_f32<T>(buf[i]);
+    } else if constexpr (kBytes == 8) {
+      alignas(16) T buf[VPL];
+      *reinterpret_cast<uint2*>(buf) = __ldg(reinterpret_cast<const uint2*>(p));
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) v[i] = to_f32<T>(buf[i]);
+    } else {
+      alignas(16) T buf[VPL];
+      *reinterpret_cast<uint32_t*>(buf) = __ldg(reinterpret_cast<const uint32_t*>(p));
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) v[i] = to_f32<T>(buf[i]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) v[i] = (e0 + i < E) ? to_f32<T>(p[i]) : -INFINITY;
+  }
+}
+
+template <typename T, int VPL>
+__global__ void __launch_bounds__(32 * kRowsPerBlock)
+route_kernel(const T* __restrict__ logits, int64_t T_rows, int E, int k, int renorm,
+             uint32_t* __restrict__ idx, T* __restrict__ w_out, float* __restrict__ w32,
+             uint32_t* status_reset) {
+  if (status_reset && blockIdx.x == 0 && threadIdx.x == 0) *status_reset = 0u;
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+  if (t >= T_rows) return;
+
+  float v[VPL];
+  load_row<T, VPL>(logits + t * E, E, lane, v);
+  const int e0 = lane * VPL;
+
+  // poisoned-row detection and the row maximum (padding entries excluded)
+  float m = -INFINITY;
+  bool nan_or_pinf = false;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    if (e0 + i < E) {
+      nan_or_pinf |= isnan(v[i]) || v[i] == INFINITY;
+      m = fmaxf(m, v[i]);
+    }
+  }
+  const bool poisoned = __any_sync(0xffffffffu, nan_or_pinf);
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+
+  if (poisoned || m == -INFINITY) {
+    for (int j = lane; j < k; j += 32) {
+      idx[t * k + j] = (uint32_t)j;
+      w_out[t * k + j] = from_f32<T>(NAN);
+      if (w32) w32[t * k + j] = NAN;
+    }
+    return;
+  }
+
+  // FP32 softmax denominator: per-lane sum, then a butterfly
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (e0 + i < E) s += expf(v[i] - m);
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d);
+
+  // k rounds of arg-max over the not-yet-selected experts
+  uint32_t taken = 0;  // bit i: expert e0+i already selected
+  uint32_t my_idx[2] = {0, 0};
+  float my_p[2] = {0.f, 0.f};
+  float sel_sum = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      if (e0 + i < E && !(taken >> i & 1u) && beats(v[i], e0 + i, bv, bi)) {
+        bv = v[i];
+        bi = e0 + i;
+      }
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+      int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+      if (beats(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (bi / VPL == lane) taken |= 1u << (bi % VPL);
+    const float p = expf(bv - m) / s;
+    sel_sum += p;  // every lane adds in slot order
+    if ((j & 31) == lane) {
+      my_idx[j >> 5] = (uint32_t)bi;
+      my_p[j >> 5] = p;
+    }
+  }
+
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = h * 32 + lane;
+    if (j < k) {
+      const float w = renorm ? my_p[h] / sel_sum : my_p[h];
+      idx[t * k + j] = my_idx[h];
+      w_out[t * k + j] = from_f32<T>(w);
+      if (w32) w32[t * k + j] = w;
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_typed(const void* logits, int64_t T_rows, int E, int k, int renorm,
+                         uint32_t* idx, void* weights, float* w32, uint32_t* status_reset,
+                         cudaStream_t s) {
+  dim3 grid((unsigned)((T_rows + kRowsPerBlock - 1) / kRowsPerBlock));
+  dim3 block(32 * kRowsPerBlock);
+  const T* l = static_cast<const T*>(logits);
+  T* w = static_cast<T*>(weights);
+#define MOE_ROUTE_CASE(V)                                                                     \
+  route_kernel<T, V><<<grid, block, 0, s>>>(l, T_rows, E, k, renorm, idx, w, w32, status_reset); \
+  break;
+  switch ((E + 31) / 32 <= 1 ? 1 : (E + 31) / 32 <= 2 ? 2 : (E + 31) / 32 <= 4 ? 4
+          : (E + 31) / 32 <= 8 ? 8 : (E + 31) / 32 <= 16 ? 16 : 32) {
+    case 1: MOE_ROUTE_CASE(1)
+    case 2: MOE_ROUTE_CASE(2)
+    case 4: MOE_ROUTE_CASE(4)
+    case 8: MOE_ROUTE_CASE(8)
+    case 16: MOE_ROUTE_CASE(16)
+    default: MOE_ROUTE_CASE(32)
+  }
+#undef MOE_ROUTE_CASE
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_route(const void* logits, moe_dtype ldt, int64_t T, int E, int k, int renorm,
+                         uint32_t* idx, void* weights, float* w32, uint32_t* status_reset,
+                         cudaStream_t s) {
+  switch (ldt) {
+    case MOE_F32:
+      return launch_typed<float>(logits, T, E, k, renorm, idx, weights, w32, status_reset, s);
+    case MOE_F16:
+      return launch_typed<__half>(logits, T, E, k, renorm, idx, weights, w32, status_reset, s);
+    default:
+      return launch_typed<__nv_bfloat16>(logits, T, E, k, renorm, idx, weights, w32, status_reset, s);
+  }
+}
+
+}  // namespace moe
