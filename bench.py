@@ -1,0 +1,382 @@
+"""Benchmark of the fused local MoE forward on the fine-grained headline workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+One step = one moe_forward (route -> dispatch -> grouped gate/up + SwiGLU ->
+grouped down with weighted un-permute -> combine) over T tokens whose inputs
+are already resident in HBM.  Prints ONE JSON line (rank 0).  Under torchrun
+each rank runs the same workload on its own GPU (tokens are independent, so
+ranks need no data exchange: weak scaling); the time is the max over ranks.
+
+``--impl reference`` times the FP64 CPU oracle (the only reference this
+method has) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE fwd tokens/s; grouped-GEMM TFLOP/s as % of GB300 BF16 peak (1 GPU)"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "finegrained_bf16"
+LAUNCHES_PER_STEP = 8  # route, count, scan, scatter, gather, gate/up GEMM, down GEMM, combine
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch of the gate/up GEMM on the headline workload, from one
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
+# of the kernel source it was taken on; reported as null once the source changes.
+GATEUP_TRAFFIC = {"bytes": None, "source_sha256": None}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=600)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="target wall time of the oracle sample")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a host float over all ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha256(rel: str) -> str:
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            text, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            text, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in text.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# CPU baseline / reference arm: the FP64 oracle on the host cores
+# --------------------------------------------------------------------------
+
+def _host_inputs(wl):
+    """The workload's inputs as stored bits on the host (drawn on the GPU when
+    one is present, so they are the same bits the native arm uses)."""
+    import torch
+    from top_routing_grouped_fp32_gb300.inputs import make_inputs, to_stored_numpy
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = make_inputs(wl, device=dev)
+    out = {k: to_stored_numpy(inp[k]) for k in ("x", "logits", "gate", "up", "down")}
+    del inp
+    if dev == "cuda":
+        torch.cuda.empty_cache()
+    return out
+
+
+def oracle_sample_rate(wl, host, target_s: float, tokens_offset: int = 0):
+    """Times oracle.forward_tokens (route + k experts + weighted sum per token,
+    FP64, OpenMP over tokens) on a token sample sized to about target_s
+    seconds.  Returns (tokens/s, tokens, seconds, threads)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    threads = oracle.num_threads()
+
+    def run(n):
+        toks = (np.arange(n) * 7919 + tokens_offset) % wl.T
+        t0 = time.perf_counter()
+        oracle.forward_tokens(host["x"], host["logits"], host["gate"], host["up"], host["down"],
+                              wl.dtype, wl.dtype, wl.top_k, wl.renormalize, toks)
+        return time.perf_counter() - t0
+
+    n = max(threads, 8)
+    dt = run(n)
+    n = int(min(wl.T, max(n, n * target_s / max(dt, 1e-3))))
+    dt = run(n)
+    return n / dt, n, dt, threads
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the oracle as it stands, timed per step on a bounded
+    sample of the workload's tokens."""
+    import numpy as np
+    import oracle
+    from top_routing_grouped_fp32_gb300.inputs import WORKLOADS
+    if rank != 0:
+        return 0
+    wl = WORKLOADS[args.workload]
+    host = _host_inputs(wl)
+    oracle.build()
+    threads = oracle.num_threads()
+    # size one step's sample so that warm-up + steps take about three minutes
+    rate, _, _, _ = oracle_sample_rate(wl, host, target_s=2.0)
+    budget = 180.0 / max(1, args.steps + args.warmup)
+    per_step = int(max(threads, min(wl.T, rate * budget)))
+
+    def step(i):
+        toks = (np.arange(per_step) * 7919 + i * per_step) % wl.T
+        oracle.forward_tokens(host["x"], host["logits"], host["gate"], host["up"], host["down"],
+                              wl.dtype, wl.dtype, wl.top_k, wl.renormalize, toks)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    el = time.perf_counter() - t0
+    value = per_step * args.steps / el
+    sample = (f"{per_step} tokens per step of {wl.name} through the FP64 oracle "
+              f"(route + {wl.top_k} SwiGLU experts + weighted sum per token)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "T": wl.T, "E": wl.E, "top_k": wl.top_k, "H": wl.H, "I": wl.I,
+            "renormalize": wl.renormalize, "seed": wl.seed, "weights_dtype": wl.dtype,
+            "l2": ("no flush: every step streams all expert weights "
+                   f"({3 * wl.E * wl.H * wl.I * 2 / 1e9:.2f} GB) and the dispatched rows, "
+                   "far above the 129 MB L2")}
+
+
+# --------------------------------------------------------------------------
+# native arm
+# --------------------------------------------------------------------------
+
+def run_native(args, rank, world, local):
+    import torch
+    import top_routing_grouped_fp32_gb300 as moe
+    from top_routing_grouped_fp32_gb300.inputs import WORKLOADS, make_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the native arm has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    moe.load()
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl, device=dev)
+    experts = moe.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    ws = experts.forward_workspace(wl.T, wl.top_k, inp["logits"].dtype)
+    y = torch.empty((wl.T, wl.H), dtype=inp["x"].dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        experts.forward(inp["x"], inp["logits"], wl.top_k, wl.renormalize, y=y, workspace=ws,
+                        stream=stream, events=events)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    assert moe.moe_get_device_status(ws) == 0
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for e in [x for row in ev for x in row]:
+        e.record(stream)  # torch creates the CUDA event on its first record
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler take its first readings
+    start.record(stream)
+    for i in range(K):
+        step(ev[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    barrier(world, dev)
+    ms_local = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_local, world, dev)
+    status = moe.moe_get_device_status(ws)
+
+    # per-stage device time inside the timed region (events on the launching stream)
+    names = ["route", "dispatch", "gate_up_gemm", "down_gemm", "combine"]
+    stage = {n: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
+             for j, n in enumerate(names)}
+
+    # end to end through the host-buffer entry point: copies inside the timed region
+    xh = inp["x"].cpu().pin_memory()
+    lh = inp["logits"].cpu().pin_memory()
+    yh = torch.empty((wl.T, wl.H), dtype=inp["x"].dtype).pin_memory()
+    wsh = experts.forward_host_workspace(wl.T, wl.top_k, inp["logits"].dtype)
+    for _ in range(3):
+        experts.forward_host(xh, lh, wl.top_k, wl.renormalize, yh, wsh, stream=stream)
+    torch.cuda.synchronize(dev)
+    Ke = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(Ke):
+        experts.forward_host(xh, lh, wl.top_k, wl.renormalize, yh, wsh, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    h2d = xh.numel() * xh.element_size() + lh.numel() * lh.element_size()
+    d2h = yh.numel() * yh.element_size()
+
+    line = None
+    if rank == 0:
+        peaks, peaks_src = load_peaks()
+        N = wl.T * wl.top_k
+        gemm_flops = 6.0 * N * wl.H * wl.I
+        gateup_flops = 4.0 * N * wl.H * wl.I
+        gemm_ms = stage["gate_up_gemm"] + stage["down_gemm"]
+        tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
+        gateup_tflops = gateup_flops / (stage["gate_up_gemm"] * 1e-3) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        src = "top_routing_grouped_fp32_gb300/csrc/gemm_tc.cu"
+        traffic = GATEUP_TRAFFIC["bytes"] if GATEUP_TRAFFIC["source_sha256"] == source_sha256(src) else None
+        line = {
+            "metric": METRIC,
+            "value": wl.T * world * K / (ms_total * 1e-3),
+            "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else wl.dtype,
+            "data": "synthetic (seeded randn, BF16 weights ~N(0,1/fan_in)); no dataset, random-init weights",
+            "config": workload_config(wl),
+            "gemm_tflops": tflops,
+            "gemm_frac_of_peak": tflops / peak,
+            "stages_ms": stage,
+            "roofline": {"bound": "tensor", "kernel": "grouped_gemm_tc (gate/up + SwiGLU)",
+                         "achieved": gateup_tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": gateup_tflops / peak, "traffic": traffic,
+                         "peak_source": f"{peaks_src} bf16_tflops (burst)",
+                         "algorithmic_per_launch": f"4*N*H*I = {gateup_flops:.4e} FLOP"},
+            "e2e": {"value": wl.T * world * Ke / (e2e_ms * 1e-3), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": LAUNCHES_PER_STEP * K,
+            "clocks": clock_info,
+            "device_status": status,
+        }
+    # free the GPU before the CPU leg
+    del experts, ws, wsh, inp, y
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = _host_inputs(wl)
+        rate, n, dt, threads = oracle_sample_rate(wl, host, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": (f"{n} tokens of {wl.name} through the FP64 oracle (route + {wl.top_k} SwiGLU "
+                       f"experts + weighted sum per token) in {dt:.1f} s")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_native(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

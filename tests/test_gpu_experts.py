@@ -1,0 +1,76 @@
+"""Expert parity: moe_experts_forward (grouped gate/up + SwiGLU + down) against
+the oracle on the same dispatched rows.  Sizes span several 128-row tiles,
+ragged segment ends, empty experts, K and N not multiples of the tile, both
+16-bit dtypes on the tcgen05 path and FP32 / odd shapes on the SIMT path."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import DT, assert_y_close, stored, u32, values
+from top_routing_grouped_fp32_gb300.inputs import make_inputs, small_workload
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(moe, T, E, k, H, I, dtype, seed=0, skew=0.0):
+    wl = small_workload(T, E, k, H, I, dtype=dtype, seed=seed, skew=skew)
+    inp = make_inputs(wl, device="cuda")
+    experts = moe.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    idx, _ = moe.moe_route(inp["logits"], k, True)
+    d = moe.moe_dispatch(idx, E, x=inp["x"])
+    out = experts.forward_dispatched(d.x_disp, d.offsets)
+    torch.cuda.synchronize()
+    off = u32(d.offsets)
+    ref = oracle.experts(values(d.x_disp), off, stored(inp["gate"]), stored(inp["up"]),
+                         stored(inp["down"]), dtype)
+    n = int(off[-1])
+    assert_y_close(out[:n], ref[:n], dtype, "expert_out")
+    return experts, d, out
+
+
+@pytest.mark.parametrize("T,E,k,H,I,dtype", [
+    (200, 4, 2, 512, 384, "bf16"),     # 400 rows, 3 gate/up n-blocks, 2 down n-blocks
+    (200, 4, 2, 512, 384, "f16"),
+    (333, 6, 3, 264, 200, "bf16"),     # ragged K (264, 200) and ragged n (I=200, H=264)
+    (97, 16, 2, 128, 136, "bf16"),     # many experts with few rows, some empty
+    (1024, 8, 2, 256, 1408, "bf16"),   # ~256 rows/expert, 11 n-blocks
+    (64, 1, 1, 64, 64, "bf16"),        # one expert, k=1
+    (5, 3, 2, 72, 8, "bf16"),          # a handful of rows, I=8
+])
+def test_experts_tcgen05(cuda_lib, T, E, k, H, I, dtype):
+    _run(cuda_lib, T, E, k, H, I, dtype, seed=T + H)
+
+
+def test_experts_skewed_segments(cuda_lib):
+    """The hottest expert holds several full tiles while most are empty."""
+    _, d, _ = _run(cuda_lib, 800, 32, 4, 256, 256, "bf16", seed=3, skew=2.0)
+    cnt = np.diff(u32(d.offsets).astype(np.int64))
+    assert cnt.max() > 384 and (cnt == 0).sum() > 0
+
+
+@pytest.mark.parametrize("T,E,k,H,I,dtype", [
+    (64, 4, 2, 64, 128, "f32"),        # the tiny workload's shapes
+    (150, 5, 2, 40, 70, "f32"),
+    (120, 4, 2, 60, 90, "bf16"),       # H, I not multiples of 8: SIMT path
+    (80, 3, 2, 20, 44, "f16"),
+])
+def test_experts_simt(cuda_lib, T, E, k, H, I, dtype):
+    _run(cuda_lib, T, E, k, H, I, dtype, seed=T)
+
+
+def test_experts_deterministic(cuda_lib):
+    experts, d, out = _run(cuda_lib, 500, 8, 2, 256, 384, "bf16", seed=4)
+    again = experts.forward_dispatched(d.x_disp, d.offsets)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+
+
+def test_experts_rejects_mismatched_weights(cuda_lib):
+    g = torch.zeros((2, 8, 16), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cuda_lib.MoeError, match="dimensions do not match"):
+        cuda_lib.SwiGluExperts(g, g, torch.zeros((2, 8, 16), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(cuda_lib.MoeError, match="matching dtype"):
+        cuda_lib.SwiGluExperts(g, g.half(), torch.zeros((2, 16, 8), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(cuda_lib.MoeError, match="rank-three"):
+        cuda_lib.SwiGluExperts(g[0], g[0], g[0])

@@ -1,0 +1,153 @@
+"""Fused forward parity (moe_forward, the call the benchmark times).
+
+Small cases: every token against the oracle.  The five workloads at full
+size: routing indices, offsets and perm read back from the workspace and
+compared bit-exactly with the oracle over ALL tokens; y compared on a sample
+of tokens evaluated one by one by the oracle (including poisoned rows)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import DT, assert_y_close, oracle_forward_sample, oracle_route, stored, u32
+from top_routing_grouped_fp32_gb300.inputs import WORKLOADS, make_inputs, small_workload
+
+pytestmark = pytest.mark.gpu
+
+
+def _ws_views(experts, ws, T, k, ldtype):
+    lay = experts.forward_layout(T, k, ldtype)
+    N = T * k
+    E = experts.E
+    b = ws
+    idx = b[lay["idx"]:lay["idx"] + 4 * N].view(torch.int32).view(T, k)
+    offsets = b[lay["offsets"]:lay["offsets"] + 4 * (E + 1)].view(torch.int32)
+    perm = b[lay["perm"]:lay["perm"] + 4 * N].view(torch.int32)
+    return idx, offsets, perm
+
+
+def _forward(moe, wl, inp, **kw):
+    experts = moe.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    ws = experts.forward_workspace(wl.T, wl.top_k, inp["logits"].dtype)
+    y = experts.forward(inp["x"], inp["logits"], wl.top_k, wl.renormalize, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    return experts, ws, y
+
+
+def _check_routing_and_dispatch(experts, ws, wl, logits):
+    idx, offsets, perm = _ws_views(experts, ws, wl.T, wl.top_k, logits.dtype)
+    o_idx, _, _ = oracle_route(logits, wl.top_k, wl.renormalize)
+    assert np.array_equal(u32(idx), o_idx), "routing indices differ"
+    o_off, _, o_perm, bad = oracle.dispatch(o_idx, wl.E)
+    assert bad == 0
+    assert np.array_equal(u32(offsets), o_off), "offsets differ"
+    assert np.array_equal(u32(perm), o_perm), "perm differs"
+    return o_idx, o_off
+
+
+@pytest.mark.parametrize("T,E,k,H,I,dtype,renorm", [
+    (300, 8, 2, 256, 384, "bf16", True),
+    (257, 6, 3, 264, 200, "bf16", False),
+    (200, 16, 4, 512, 128, "f16", True),
+    (150, 5, 2, 40, 70, "f32", True),
+    (100, 4, 2, 60, 90, "bf16", False),
+])
+def test_forward_small_all_tokens(cuda_lib, T, E, k, H, I, dtype, renorm):
+    wl = small_workload(T, E, k, H, I, dtype=dtype, renormalize=renorm, seed=T + E)
+    inp = make_inputs(wl, device="cuda")
+    experts, ws, y = _forward(cuda_lib, wl, inp)
+    _check_routing_and_dispatch(experts, ws, wl, inp["logits"])
+    _, _, ref = oracle_forward_sample(inp, k, renorm, np.arange(T), dtype)
+    assert_y_close(y, ref, dtype)
+    assert cuda_lib.moe_get_device_status(ws) == 0
+
+
+def test_forward_tiny_fp32_workload(cuda_lib):
+    wl = WORKLOADS["tiny_fp32"]
+    inp = make_inputs(wl, device="cuda")
+    experts, ws, y = _forward(cuda_lib, wl, inp)
+    o_idx, _ = _check_routing_and_dispatch(experts, ws, wl, inp["logits"])
+    assert o_idx[:8].tolist() == [[0, 1], [1, 2], [0, 1], [0, 1], [0, 2], [3, 1], [0, 1], [0, 3]]
+    _, _, ref = oracle_forward_sample(inp, wl.top_k, wl.renormalize, np.arange(wl.T), "f32")
+    assert_y_close(y, ref, "f32")
+
+
+def _sample_tokens(wl, inp, n=24, seed=0):
+    rng = np.random.default_rng(seed)
+    toks = set(rng.choice(wl.T, size=min(n, wl.T), replace=False).tolist()) | {0, wl.T - 1}
+    meta = inp["meta"].get("poison")
+    if meta:
+        toks |= set(meta["rows"][:6]) | {meta["control"]}
+    return np.array(sorted(toks))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mixtral_bf16", "finegrained_bf16", "skewed_bf16", "decode_bf16"])
+def test_forward_full_workloads(cuda_lib, name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, device="cuda")
+    experts, ws, y = _forward(cuda_lib, wl, inp)
+    _check_routing_and_dispatch(experts, ws, wl, inp["logits"])
+    toks = _sample_tokens(wl, inp)
+    _, _, ref = oracle_forward_sample(inp, wl.top_k, wl.renormalize, toks, wl.dtype)
+    assert_y_close(y[torch.as_tensor(toks, device="cuda")], ref, wl.dtype)
+    if wl.poison_frac:
+        rows = inp["meta"]["poison"]["rows"]
+        assert torch.isnan(y[rows]).all()
+        others = torch.ones(wl.T, dtype=torch.bool, device="cuda")
+        others[rows] = False
+        assert torch.isfinite(y[others]).all()
+    assert cuda_lib.moe_get_device_status(ws) == 0
+    del experts, ws, y, inp
+    torch.cuda.empty_cache()
+
+
+def test_forward_deterministic_and_host_variant(cuda_lib):
+    wl = small_workload(1000, 16, 4, 512, 256, dtype="bf16", renormalize=True, seed=21)
+    inp = make_inputs(wl, device="cuda")
+    experts, ws, y1 = _forward(cuda_lib, wl, inp)
+    y2 = experts.forward(inp["x"], inp["logits"], wl.top_k, wl.renormalize, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    # the host-buffer entry point: the same bits
+    xh = inp["x"].cpu().pin_memory()
+    lh = inp["logits"].cpu().pin_memory()
+    yh = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    wsh = experts.forward_host_workspace(wl.T, wl.top_k, torch.bfloat16)
+    experts.forward_host(xh, lh, wl.top_k, wl.renormalize, yh, wsh)
+    torch.cuda.synchronize()
+    assert torch.equal(yh.view(torch.int16), y1.cpu().view(torch.int16))
+
+
+def test_forward_fp32_logits_bf16_experts(cuda_lib):
+    wl = small_workload(300, 8, 2, 256, 256, dtype="bf16", renormalize=True, seed=8)
+    inp = make_inputs(wl, device="cuda", logits_dtype="f32")
+    experts, ws, y = _forward(cuda_lib, wl, inp)
+    _check_routing_and_dispatch(experts, ws, wl, inp["logits"])
+    _, _, ref = oracle.forward_tokens(stored(inp["x"]), stored(inp["logits"]), stored(inp["gate"]),
+                                      stored(inp["up"]), stored(inp["down"]), "bf16", "f32", 2, True,
+                                      np.arange(wl.T))
+    assert_y_close(y, ref, "bf16")
+
+
+def test_forward_staged_matches_fused(cuda_lib):
+    """route -> dispatch -> forward_dispatched -> combine gives the fused result
+    up to the rounding of the weighted slot values."""
+    wl = small_workload(400, 8, 2, 256, 384, dtype="bf16", renormalize=False, seed=5)
+    inp = make_inputs(wl, device="cuda")
+    experts, ws, y = _forward(cuda_lib, wl, inp)
+    idx, w = cuda_lib.moe_route(inp["logits"], 2, False)
+    d = cuda_lib.moe_dispatch(idx, wl.E, x=inp["x"])
+    out = experts.forward_dispatched(d.x_disp, d.offsets)
+    y2 = cuda_lib.moe_combine(out, d.perm, w, 2)
+    torch.cuda.synchronize()
+    scale = y.float().abs().max().item()
+    assert (y.float() - y2.float()).abs().max().item() <= 2 ** -7 * scale
+
+
+def test_forward_empty_batch(cuda_lib):
+    wl = small_workload(4, 4, 2, 64, 64, dtype="bf16", seed=1)
+    inp = make_inputs(wl, device="cuda")
+    experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    y = experts.forward(inp["x"][:0], inp["logits"][:0], 2, True)
+    assert y.shape == (0, 64)

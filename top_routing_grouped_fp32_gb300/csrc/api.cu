@@ -275,13 +275,13 @@ moe_status moe_dispatch(const uint32_t* idx, int64_t T, int64_t E, int32_t top_k
     if (!valid_dtype(x_dtype)) return fail(MOE_ERR_DTYPE, "x dtype %d is not F32/F16/BF16", (int)x_dtype);
     if ((st = check_dim(H, "H")) != MOE_OK) return st;
   }
-  if (!offsets || !perm) return fail(MOE_ERR_INVALID_ARG, "offsets and perm must be non-NULL");
+  if (!offsets) return fail(MOE_ERR_INVALID_ARG, "offsets must be non-NULL");
   if (T == 0) {
-    // no rows: offsets are all zero
+    // no rows: offsets are all zero, nothing else is written
     MOE_TRY_CUDA(cudaMemsetAsync(offsets, 0, (size_t)(E + 1) * 4, stream), "cudaMemsetAsync");
     return ok();
   }
-  if (!idx) return fail(MOE_ERR_INVALID_ARG, "idx must be non-NULL");
+  if (!idx || !perm) return fail(MOE_ERR_INVALID_ARG, "idx and perm must be non-NULL");
   if ((st = check_ws(ws, ws_bytes, moe_dispatch_workspace_size(T, E, top_k))) != MOE_OK) return st;
   MOE_TRY_CUDA(moe::launch_dispatch(idx, T, (int)E, top_k, offsets, row_experts, perm,
                                     static_cast<char*>(ws) + kWsHeader, status_word(ws), stream),
