@@ -1,0 +1,45 @@
+"""The oracle pins catch plausible mistakes (CPU only).
+
+Each case plants one mistake in a COPY of oracle/moe_oracle.c inside a
+temporary directory, runs the pin suite against that copy in a subprocess and
+expects failures.  The real oracle is never modified."""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = {
+    "tie_to_higher_id": ("return a < b; /* equal", "return a > b; /* equal"),
+    "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    "gate_reads_up": ("g += load_elem(gate, wdt, base + h) * x[h];",
+                      "g += load_elem(up, wdt, base + h) * x[h];"),
+    "down_transposed": ("int64_t base = (e * H + c) * I;", "int64_t base = (e * I + c) * H;"),
+    "unstable_dispatch": ("for (int64_t s = 0; s < n; ++s) { /* ascending s: stable */",
+                          "for (int64_t s = n - 1; s >= 0; --s) {"),
+    "plus_inf_not_poison": ("if (l[e] == INFINITY) has_pinf = 1;", ";"),
+    "renorm_dropped": ("for (int j = 0; j < k; ++j) w_pre[j] = w_pre[j] / tot;", ";"),
+    "combine_unweighted": ("w_cast[t * k + j] * expert_out[r * H + c]", "expert_out[r * H + c]"),
+    "softmax_without_max_shift": ("s += exp(l[e] - m);", "s += exp(l[e]);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(tmp_path, name):
+    old, new = MUTATIONS[name]
+    src = open(os.path.join(ROOT, "oracle", "moe_oracle.c")).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    root = tmp_path / "repo"
+    shutil.copytree(os.path.join(ROOT, "oracle"), root / "oracle",
+                    ignore=shutil.ignore_patterns("_build", "__pycache__"))
+    shutil.copytree(os.path.join(ROOT, "tests"), root / "tests",
+                    ignore=shutil.ignore_patterns("__pycache__"))
+    (root / "oracle" / "moe_oracle.c").write_text(src.replace(old, new))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider",
+                        "tests/test_oracle_pins.py"], cwd=root, capture_output=True, text=True,
+                       timeout=600)
+    tail = r.stdout.strip().splitlines()[-1] if r.stdout.strip() else r.stderr[-500:]
+    assert r.returncode != 0 and "failed" in tail, f"{name} went unnoticed: {tail}"
