@@ -111,6 +111,33 @@ moe_status moe_dispatch(const uint32_t* idx, int64_t T, int64_t E, int32_t top_k
                         void* x_disp, void* workspace, size_t workspace_bytes,
                         cudaStream_t stream);
 
+/* Dispatch for callers that can neither allocate device memory nor lend
+ * this library a workspace, for example a layer plugin inside an inference
+ * engine that only receives the layer's own tensors, or a serving loop that
+ * fixed its memory plan at start-up and must not trigger cudaMalloc later
+ * (an allocation can synchronise the whole device).  The pages have no
+ * counterpart to this call: it exists for those callers only.
+ *
+ * Same arguments, results and ordering as moe_dispatch, without the
+ * workspace.  The dispatch scratch (chunk counts and bases) lives in a fixed
+ * 2 MiB device array inside the library, which every GPU that loads the
+ * library holds until the process exits.  Problems needing more scratch than
+ * that (dispatch scratch = 4*ceil(T/256)*(2E+1) bytes, rounded up; e.g.
+ * T <= 65,280 at E = 1024, T <= ~1M at E = 64) get MOE_ERR_UNSUPPORTED with a
+ * message.  The call allocates nothing.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  All calls share the array and it keeps the last call's contents;
+ * nothing in it needs clearing because each call writes every entry it reads.
+ * Calls whose kernels overlap on the GPU (unordered streams) race on the
+ * array and give wrong results.  There is no device status word: an index
+ * >= E shows up as offsets[E] < T*top_k and 0xFFFFFFFF at the tail of perm. */
+moe_status moe_dispatch_noalloc(const uint32_t* idx, int64_t T, int64_t E, int32_t top_k,
+                                const void* x, moe_dtype x_dtype, int64_t H,
+                                uint32_t* offsets, uint32_t* row_experts, uint32_t* perm,
+                                void* x_disp, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------
  * Experts.  SwiGluExperts::new in src/moe/experts.rs and the user guide,
  * section 5: bias-free gate and up [E,I,H], down [E,H,I], one float dtype,

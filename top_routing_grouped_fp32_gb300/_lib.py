@@ -56,6 +56,7 @@ _SIGNATURES = {
     "moe_route": (ST, [P, INT, I64, I64, I32, INT, P, P, P, P]),
     "moe_dispatch_workspace_size": (SZ, [I64, I64, I32]),
     "moe_dispatch": (ST, [P, I64, I64, I32, P, INT, I64, P, P, P, P, P, SZ, P]),
+    "moe_dispatch_noalloc": (ST, [P, I64, I64, I32, P, INT, I64, P, P, P, P, P]),
     "moe_experts_create": (ST, [P, P, P, INT, I64, I64, I64, ctypes.POINTER(P)]),
     "moe_experts_destroy": (None, [P]),
     "moe_experts_workspace_size": (SZ, [P, I64]),

@@ -293,6 +293,43 @@ moe_status moe_dispatch(const uint32_t* idx, int64_t T, int64_t E, int32_t top_k
   return ok();
 }
 
+moe_status moe_dispatch_noalloc(const uint32_t* idx, int64_t T, int64_t E, int32_t top_k,
+                                const void* x, moe_dtype x_dtype, int64_t H, uint32_t* offsets,
+                                uint32_t* row_experts, uint32_t* perm, void* x_disp,
+                                cudaStream_t stream) {
+  moe_status st = check_tek(T, E, top_k);
+  if (st != MOE_OK) return st;
+  if ((x == nullptr) != (x_disp == nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "x and x_disp must both be given or both be NULL");
+  if (x) {
+    if (!valid_dtype(x_dtype)) return fail(MOE_ERR_DTYPE, "x dtype %d is not F32/F16/BF16", (int)x_dtype);
+    if ((st = check_dim(H, "H")) != MOE_OK) return st;
+  }
+  if (!offsets) return fail(MOE_ERR_INVALID_ARG, "offsets must be non-NULL");
+  const size_t need = moe::dispatch_scratch_bytes(T, (int)E);
+  const size_t limit = moe::dispatch_noalloc_scratch_limit();
+  if (need > limit)
+    return fail(MOE_ERR_UNSUPPORTED,
+                "moe_dispatch_noalloc: T=%lld, E=%lld needs %zu bytes of scratch, above its fixed "
+                "%zu bytes; use moe_dispatch with a workspace",
+                (long long)T, (long long)E, need, limit);
+  if (T == 0) {
+    MOE_TRY_CUDA(cudaMemsetAsync(offsets, 0, (size_t)(E + 1) * 4, stream), "cudaMemsetAsync");
+    return ok();
+  }
+  if (!idx || !perm) return fail(MOE_ERR_INVALID_ARG, "idx and perm must be non-NULL");
+  void* scratch = nullptr;
+  MOE_TRY_CUDA(moe::dispatch_noalloc_scratch(&scratch), "cudaGetSymbolAddress of the dispatch scratch");
+  MOE_TRY_CUDA(moe::launch_dispatch(idx, T, (int)E, top_k, offsets, row_experts, perm, scratch,
+                                    nullptr, stream),
+               "dispatch kernel launch");
+  if (x)
+    MOE_TRY_CUDA(moe::launch_gather(x, x_dtype, H, top_k, perm, offsets, (int)E, T * top_k, x_disp,
+                                    stream),
+                 "gather kernel launch");
+  return ok();
+}
+
 // ---- experts -------------------------------------------------------------
 moe_status moe_experts_create(const void* gate, const void* up, const void* down, moe_dtype dt,
                               int64_t E, int64_t I, int64_t H, moe_experts_t* out) {

@@ -20,6 +20,8 @@
 //              them, so ranks follow s exactly, duplicates included.  A first
 //              pass counts per warp, a second writes perm/row_experts.
 // A fourth kernel gathers x rows into x_disp, one warp per dispatched row.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -240,6 +242,50 @@ cudaError_t launch_gather(const void* x, moe_dtype dt, int64_t H, int k, const u
     gather_kernel<2><<<grid, 256, 0, s>>>(static_cast<const char*>(x), row_bytes, k, perm, offsets,
                                           E, N, static_cast<char*>(x_disp));
   return cudaGetLastError();
+}
+
+
+// ---------------------------------------------------------------------------
+// Dispatch without a caller workspace (moe_dispatch_noalloc).
+//
+// Some callers cannot hand this library any scratch memory and cannot let it
+// allocate: an inference engine whose plugin interface only passes the
+// tensors of the layer, or a serving loop that fixed its memory plan at
+// start-up and treats any later cudaMalloc (which may synchronise the device)
+// as a fault.  For them the chunk counts and chunk bases of the dispatch live
+// in this fixed device array.  It is part of the library image: every GPU that
+// loads the library holds these bytes until the process exits.
+//
+// The kernels read only scratch entries that the same call wrote first (the
+// count kernel writes every count of every chunk, the scan writes every
+// base), so nothing has to be cleared between calls.  All calls share the one
+// array: two such calls whose kernels overlap on the GPU (different streams
+// without ordering) race on it and give wrong results.
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;  // 2 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+size_t dispatch_noalloc_scratch_limit() { return kNoAllocScratchBytes; }
+
+// Device address of g_noalloc_scratch on the current device.  The host-side
+// name of the array is only a stand-in, so the address is looked up once per
+// device with cudaGetSymbolAddress (with that device current) and cached.
+cudaError_t dispatch_noalloc_scratch(void** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (err != cudaSuccess) return err;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace moe

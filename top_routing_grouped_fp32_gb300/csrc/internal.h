@@ -23,6 +23,9 @@ size_t dispatch_scratch_bytes(int64_t T, int E);
 cudaError_t launch_dispatch(const uint32_t* idx, int64_t T, int E, int k, uint32_t* offsets,
                             uint32_t* row_experts, uint32_t* perm, void* scratch,
                             uint32_t* status, cudaStream_t s);
+// fixed device scratch for moe_dispatch_noalloc (size limit and address)
+size_t dispatch_noalloc_scratch_limit();
+cudaError_t dispatch_noalloc_scratch(void** out);
 cudaError_t launch_gather(const void* x, moe_dtype dt, int64_t H, int k, const uint32_t* perm,
                           const uint32_t* offsets, int E, int64_t N, void* x_disp, cudaStream_t s);
 
