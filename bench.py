@@ -319,6 +319,12 @@ def run_native(args, rank, world, local):
     h2d = xh.numel() * xh.element_size() + lh.numel() * lh.element_size()
     d2h = yh.numel() * yh.element_size()
 
+    # experts that received rows (read back after the timed region): the
+    # weight bytes a weight-streaming roofline charges
+    lay = experts.forward_layout(wl.T, wl.top_k, inp["logits"].dtype)
+    off = ws[lay["offsets"]:lay["offsets"] + 4 * (wl.E + 1)].view(torch.int32).cpu()
+    touched = int(((off[1:] - off[:-1]) != 0).sum().item())
+
     line = None
     if rank == 0:
         peaks, peaks_src = load_peaks()
@@ -331,6 +337,27 @@ def run_native(args, rank, world, local):
         peak = float(peaks["bf16_tflops"])
         src = "top_routing_grouped_fp32_gb300/csrc/gemm_tc.cu"
         traffic = GATEUP_TRAFFIC["bytes"] if GATEUP_TRAFFIC["source_sha256"] == source_sha256(src) else None
+        s_el = 4 if wl.dtype == "f32" else 2
+        w_gateup = touched * 2.0 * wl.H * wl.I * s_el
+        w_all = touched * 3.0 * wl.H * wl.I * s_el
+        hbm_peak = float(peaks["hbm_gbs"])
+        weights_hbm = {"touched_experts": touched, "bytes": w_all,
+                       "achieved": w_all / (gemm_ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                       "frac": w_all / (gemm_ms * 1e-3) / 1e9 / hbm_peak}
+        if wl.name.startswith("decode"):
+            # few rows per expert: the projections stream weights, HBM is the bound
+            ach = w_gateup / (stage["gate_up_gemm"] * 1e-3) / 1e9
+            roofline = {"bound": "hbm", "kernel": "grouped_gemm_tc (gate/up + SwiGLU)",
+                        "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
+                        "traffic": None, "peak_source": f"{peaks_src} hbm_gbs",
+                        "algorithmic_per_launch": f"touched*2*H*I*2 = {w_gateup:.4e} B"}
+        else:
+            roofline = {"bound": "tensor", "kernel": "grouped_gemm_tc (gate/up + SwiGLU)",
+                        "achieved": gateup_tflops, "peak": peak, "unit": "TFLOP/s",
+                        "frac": gateup_tflops / peak,
+                        "traffic": traffic if wl.name == DEFAULT_WORKLOAD else None,
+                        "peak_source": f"{peaks_src} bf16_tflops (burst)",
+                        "algorithmic_per_launch": f"4*N*H*I = {gateup_flops:.4e} FLOP"}
         line = {
             "metric": METRIC,
             "value": wl.T * world * K / (ms_total * 1e-3),
@@ -342,11 +369,8 @@ def run_native(args, rank, world, local):
             "gemm_tflops": tflops,
             "gemm_frac_of_peak": tflops / peak,
             "stages_ms": stage,
-            "roofline": {"bound": "tensor", "kernel": "grouped_gemm_tc (gate/up + SwiGLU)",
-                         "achieved": gateup_tflops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": gateup_tflops / peak, "traffic": traffic,
-                         "peak_source": f"{peaks_src} bf16_tflops (burst)",
-                         "algorithmic_per_launch": f"4*N*H*I = {gateup_flops:.4e} FLOP"},
+            "roofline": roofline,
+            "weights_hbm": weights_hbm,
             "e2e": {"value": wl.T * world * Ke / (e2e_ms * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": LAUNCHES_PER_STEP * K,

@@ -405,14 +405,23 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     T* out = static_cast<T*>(p.out);
     for (uint32_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const Tile t = decode_tile(tile, p, s_pref, s_off);
+      const bool row_ok = row < t.rows;
+      const int64_t grow = t.m0 + row;
+      // the weighted epilogue's slot and routing weight: loaded before the
+      // accumulator wait so that their latency overlaps the MMAs
+      int64_t wslot = grow;
+      float wscale = 1.f;
+      if (p.mode == kDownWeighted && row_ok) {
+        const uint32_t s = __ldg(p.perm + grow);
+        wslot = s;
+        wscale = load_dyn(p.weights, p.wdt, s);
+      }
       int ok = 1;
       if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      const bool row_ok = row < t.rows;
-      const int64_t grow = t.m0 + row;
       if (p.mode == kGateUpSwiglu) {
         const int64_t col0 = (int64_t)t.nb * 128;
         T* dst = out + grow * p.n_out + col0;
@@ -439,13 +448,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           }
         }
       } else {
-        int64_t orow = grow;
-        float scale = 1.f;
-        if (p.mode == kDownWeighted && row_ok) {
-          const uint32_t s = __ldg(p.perm + grow);
-          orow = s;
-          scale = load_dyn(p.weights, p.wdt, s);
-        }
+        const int64_t orow = wslot;
+        const float scale = wscale;
         const int64_t col0 = (int64_t)t.nb * 256;
         T* dst = out + orow * p.n_out + col0;
 #pragma unroll 1
