@@ -37,14 +37,20 @@ def _run(moe, T, E, k, H, I, dtype, seed=0, skew=0.0):
     (1024, 8, 2, 256, 1408, "bf16"),   # ~256 rows/expert, 11 n-blocks
     (64, 1, 1, 64, 64, "bf16"),        # one expert, k=1
     (5, 3, 2, 72, 8, "bf16"),          # a handful of rows, I=8
+    # >= 128 rows per expert on average: CTA-pair (cta_group::2) tiles of 256 rows
+    (2000, 8, 2, 264, 200, "bf16"),    # ragged K and n on the pair path
+    (1500, 4, 2, 256, 384, "f16"),
+    (700, 2, 1, 512, 256, "bf16"),     # two experts, pair tiles straddling a segment end
 ])
 def test_experts_tcgen05(cuda_lib, T, E, k, H, I, dtype):
     _run(cuda_lib, T, E, k, H, I, dtype, seed=T + H)
 
 
-def test_experts_skewed_segments(cuda_lib):
-    """The hottest expert holds several full tiles while most are empty."""
-    _, d, _ = _run(cuda_lib, 800, 32, 4, 256, 256, "bf16", seed=3, skew=2.0)
+@pytest.mark.parametrize("T,E", [(800, 32), (3000, 24)])
+def test_experts_skewed_segments(cuda_lib, T, E):
+    """The hottest expert holds several full tiles while others are empty
+    (single-CTA tiles for T=800, CTA-pair tiles for T=3000)."""
+    _, d, _ = _run(cuda_lib, T, E, 4, 256, 256, "bf16", seed=3, skew=2.0 if T < 1000 else 4.0)
     cnt = np.diff(u32(d.offsets).astype(np.int64))
     assert cnt.max() > 384 and (cnt == 0).sum() > 0
 

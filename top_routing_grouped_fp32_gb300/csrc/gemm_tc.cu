@@ -14,17 +14,22 @@
 // The pages' own grouped product is a scalar or "cooperative matrix" loop
 // (prior art); this is an sm_103a design:
 //
-//   * one CTA per SM, persistent over a tile list: tiles are 128 rows x 256
-//     FP32 accumulator columns of one expert; the list is built on the device
-//     from offsets[] (segment lengths are never read by the host);
-//   * warp 0: TMA producer (cp.async.bulk.tensor, 128-byte swizzle) filling a
-//     4-stage ring of {A 128x64, B 256x64} 16-bit tiles; the B tile is two
-//     128-row boxes (gate rows + up rows, or two halves of the down rows);
-//   * warp 1: allocates 512 TMEM columns and issues tcgen05.mma (kind::f16,
-//     M=128, N=256, K=16, FP32 accumulate) from one thread; tcgen05.commit
-//     frees a ring stage and signals a finished accumulator;
+//   * persistent CTAs over a tile list built on the device from offsets[]
+//     (segment lengths are never read by the host); a tile is 128*PAIR rows
+//     x 256 FP32 accumulator columns of one expert;
+//   * PAIR = 2 (the default): a cluster of two CTAs on two SMs runs one
+//     tcgen05.mma.cta_group::2 of M=256: each CTA stages its own 128 rows of A
+//     and one 128-row half of B (gate rows / up rows, or the two halves of the
+//     down rows), so an SM moves 32 KiB per 64-deep k-block instead of 48 KiB
+//     and a 6-stage ring fits in shared memory; PAIR = 1 is the single-CTA
+//     form (M=128, both B halves staged locally, 4 stages);
+//   * warp 0: TMA producer (cp.async.bulk.tensor, 128-byte swizzle); its
+//     copies complete on the leader CTA's "full" barrier;
+//   * warp 1: allocates 512 TMEM columns; in the leader CTA one thread issues
+//     the MMAs (kind::f16, FP32 accumulate) and tcgen05.commit frees ring
+//     stages and hands finished accumulators to both CTAs' epilogues;
 //   * warps 2-5: epilogue; each reads its 32 TMEM lanes (= 32 tile rows) with
-//     tcgen05.ld while the MMA warp fills the other accumulator;
+//     tcgen05.ld while the MMA fills the other accumulator;
 //   * rows past the end of a segment are computed (the A box may run into the
 //     next expert's rows or past the buffer, where TMA fills zeros) and never
 //     stored, so segments of any length are handled without padding;
@@ -48,18 +53,24 @@
 namespace moe {
 namespace tc {
 
-constexpr int BM = 128;
+constexpr int BM = 128;        // rows per CTA
 constexpr int BN = 256;        // FP32 accumulator columns per tile
 constexpr int BK = 64;         // 64 16-bit elements = one 128-byte swizzle row
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
 constexpr uint32_t A_BYTES = BM * BK * 2;        // 16 KiB
 constexpr uint32_t B_HALF_BYTES = 128 * BK * 2;  // 16 KiB
-constexpr uint32_t STAGE_BYTES = A_BYTES + 2 * B_HALF_BYTES;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int MAX_E = 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+template <int PAIR>
+struct Cfg {
+  static constexpr int STAGES = PAIR == 1 ? 4 : 6;
+  static constexpr uint32_t B_BYTES = (PAIR == 1 ? 2u : 1u) * B_HALF_BYTES;  // B staged per CTA
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TILE_M = BM * PAIR;
+};
 
 struct Params {
   const uint32_t* offsets;
@@ -87,22 +98,52 @@ __device__ __forceinline__ uint64_t global_timer() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
+template <bool CLUSTER>
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred P;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, P;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (CLUSTER) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// arrival on a barrier of another CTA of the cluster (shared::cluster address)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
@@ -110,12 +151,13 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 // Bounded wait for phase `parity` of `bar`.  Returns false if the CTA is
 // aborting or the time limit passed (then the abort flag and status are set).
+template <bool CLUSTER>
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                        uint32_t* status) {
-  if (mbar_test(bar, parity)) return true;
+  if (mbar_test<CLUSTER>(bar, parity)) return true;
   const uint64_t t0 = global_timer();
   for (uint32_t n = 1;; ++n) {
-    if (mbar_test(bar, parity)) return true;
+    if (mbar_test<CLUSTER>(bar, parity)) return true;
     if ((n & 127u) == 0) {
       if (*abort_flag) return false;
       if (global_timer() - t0 > kWaitLimitNs) {
@@ -126,21 +168,41 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile u
     }
   }
 }
+// TMA tile loads into this CTA's shared memory.  PAIR == 2: the completion is
+// counted on `bar`, a shared::cluster address that may be the leader CTA's.
+template <int PAIR>
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
+  if constexpr (PAIR == 2) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+  } else {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+  }
 }
+template <int PAIR>
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
+  if constexpr (PAIR == 2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+  } else {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+  }
 }
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -151,30 +213,81 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
+// TMEM allocation: PAIR == 2 allocates the same columns in both CTAs of the
+// pair and is executed by one warp of each CTA.
+template <int PAIR>
 __device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
-               "r"(cols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if constexpr (PAIR == 2) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
 }
+template <int PAIR>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
-               : "memory");
+  if constexpr (PAIR == 2) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+                 : "memory");
+  } else {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+                 : "memory");
+  }
 }
-// D[tmem] (+)= A[smem] * B[smem]^T, both K-major, one 128x256x16 step.
+// D[tmem] (+)= A[smem] * B[smem]^T, both K-major, one (128*PAIR) x 256 x 16 step.
+template <int PAIR>
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if constexpr (PAIR == 2) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
 }
+// Arrive on `bar` (same offset in every CTA of the pair) once all MMAs this
+// thread issued have completed.  PAIR == 2: the arrival goes to both CTAs.
+template <int PAIR>
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
+  if constexpr (PAIR == 2) {
+    const uint16_t both = 3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(both)
+        : "memory");
+  } else {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+  }
+}
+// Arrive on the issuing CTA's own `bar` once all its MMAs have completed.
+template <int PAIR>
+__device__ __forceinline__ void umma_commit_local(uint32_t bar) {
+  if constexpr (PAIR == 2) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+  } else {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+  }
 }
 // 32 consecutive FP32 columns of this warp's 32 TMEM lanes.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -203,22 +316,21 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
          | ((uint64_t)2 << 61);                    // 128-byte swizzle
 }
 // Instruction descriptor: FP32 accumulator, 16-bit A/B (bf16 or f16), both
-// K-major, M = 128, N = 256.
-__host__ __device__ constexpr uint32_t make_idesc(bool bf16) {
+// K-major, M = 128*PAIR, N = 256.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16, int M) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ---------------------------------------------------------------- tile list
 struct Tile {
   int e;
   int nb;
-  int64_t m0;
-  int rows;
+  int64_t m0;  // first row of the (pair) tile
 };
 
 __device__ __forceinline__ Tile decode_tile(uint32_t tile, const Params& p, const uint32_t* s_pref,
-                                            const uint32_t* s_off) {
+                                            const uint32_t* s_off, int tile_m) {
   const uint32_t q = tile / (uint32_t)p.nb;
   int lo = 0, hi = p.E;  // s_pref[lo] <= q < s_pref[hi]
   while (hi - lo > 1) {
@@ -234,25 +346,26 @@ __device__ __forceinline__ Tile decode_tile(uint32_t tile, const Params& p, cons
   Tile t;
   t.e = lo;
   t.nb = (int)(pid * w + rem % width);
-  t.m0 = (int64_t)s_off[lo] + (int64_t)(rem / width) * BM;
-  const int64_t left = (int64_t)s_off[lo + 1] - t.m0;
-  t.rows = (int)(left < BM ? left : BM);
+  t.m0 = (int64_t)s_off[lo] + (int64_t)(rem / width) * tile_m;
   return t;
 }
 
 // ---------------------------------------------------------------- the kernel
-template <typename T>
+template <typename T, int PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
                 const __grid_constant__ CUtensorMap mapB1, const Params p) {
+  using C = Cfg<PAIR>;
+  constexpr int STAGES = C::STAGES;
+  constexpr bool kCluster = PAIR == 2;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t ring = (raw_s + 1023u) & ~1023u;  // 1024-byte aligned for the swizzle
   uint8_t* ring_ptr = smem_raw + (ring - raw_s);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + STAGES * STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + STAGES * C::STAGE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile uint32_t* abort_flag = tmem_slot + 1;
-  uint32_t* s_off = reinterpret_cast<uint32_t*>(ring_ptr + STAGES * STAGE_BYTES + 256);
+  uint32_t* s_off = reinterpret_cast<uint32_t*>(ring_ptr + STAGES * C::STAGE_BYTES + 256);
   uint32_t* s_pref = s_off + (p.E + 1);
 
   const uint32_t bar0 = smem_u32(bars);
@@ -264,6 +377,9 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
+  const uint32_t rank = kCluster ? cluster_rank() : 0u;  // this CTA's half of the pair tile
+  const bool leader = rank == 0;
+  const uint32_t cluster_id = blockIdx.x / PAIR, num_clusters = gridDim.x / PAIR;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -272,7 +388,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);  // one arrival per epilogue warp
+      mbar_init(tempty_bar(a), 4 * PAIR);  // one arrival per epilogue warp of every CTA
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
@@ -284,15 +400,15 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     prefetch_map(&mapB0);
     prefetch_map(&mapB1);
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), TMEM_COLS);
   for (int i = threadIdx.x; i <= E; i += THREADS) s_off[i] = p.offsets[i];
   __syncthreads();
-  if (warp == 2) {  // s_pref[e] = number of 128-row tiles of experts < e
+  if (warp == 2) {  // s_pref[e] = number of (128*PAIR)-row tiles of experts < e
     const int per = (E + 31) / 32;
     uint32_t loc = 0;
     for (int i = 0; i < per; ++i) {
       const int e = lane * per + i;
-      if (e < E) loc += (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+      if (e < E) loc += (s_off[e + 1] - s_off[e] + C::TILE_M - 1) / C::TILE_M;
     }
     uint32_t incl = loc;
 #pragma unroll
@@ -305,16 +421,20 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       const int e = lane * per + i;
       if (e < E) {
         s_pref[e] = run;
-        run += (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+        run += (s_off[e + 1] - s_off[e] + C::TILE_M - 1) / C::TILE_M;
       }
     }
     if (lane == 31) s_pref[E] = incl;
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kCluster) cluster_sync();  // the peer's barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t total_tiles = s_pref[E] * (uint32_t)p.nb;
+  // the leader CTA's barriers, as seen from this CTA
+  const uint32_t full0_leader = kCluster ? mapa(full_bar(0), 0) : full_bar(0);
+  const uint32_t tempty0_leader = kCluster ? mapa(tempty_bar(0), 0) : tempty_bar(0);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -325,20 +445,28 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       bool filled[STAGES];
       for (int s = 0; s < STAGES; ++s) filled[s] = false, last_fill[s] = 0;
       bool ok = true;
-      for (uint32_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, p, s_pref, s_off);
+      for (uint32_t tile = cluster_id; ok && tile < total_tiles; tile += num_clusters) {
+        const Tile t = decode_tile(tile, p, s_pref, s_off, C::TILE_M);
+        const int a_row = (int)(t.m0 + (int64_t)rank * BM);
         const int b0row = t.nb * p.cols_per_tile;
         const int b1row = b0row + p.b1_row_off;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
+          if (!mbar_wait<kCluster>(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          const uint32_t sa = ring + stage * STAGE_BYTES;
-          mbar_expect_tx(full_bar(stage), STAGE_BYTES);
-          tma_load_2d(sa, &mapA, kb * BK, (int)t.m0, full_bar(stage));
-          tma_load_3d(sa + A_BYTES, &mapB0, kb * BK, b0row, t.e, full_bar(stage));
-          tma_load_3d(sa + A_BYTES + B_HALF_BYTES, &mapB1, kb * BK, b1row, t.e, full_bar(stage));
+          const uint32_t sa = ring + stage * C::STAGE_BYTES;
+          const uint32_t fb = full0_leader + 8u * stage;
+          if (leader) mbar_expect_tx(full_bar(stage), C::STAGE_BYTES * PAIR);
+          tma_load_2d<PAIR>(sa, &mapA, kb * BK, a_row, fb);
+          if constexpr (PAIR == 1) {
+            tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kb * BK, b0row, t.e, fb);
+            tma_load_3d<PAIR>(sa + A_BYTES + B_HALF_BYTES, &mapB1, kb * BK, b1row, t.e, fb);
+          } else if (leader) {
+            tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kb * BK, b0row, t.e, fb);
+          } else {
+            tma_load_3d<PAIR>(sa + A_BYTES, &mapB1, kb * BK, b1row, t.e, fb);
+          }
           filled[stage] = true;
           last_fill[stage] = phase;
           if (++stage == STAGES) {
@@ -347,54 +475,56 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           }
         }
       }
-      if (!ok) {  // aborting: let this CTA's copies in flight land before exit
+      if (!ok && leader) {  // aborting: let the copies in flight land before exit
         for (int s = 0; s < STAGES; ++s) {
           if (!filled[s]) continue;
           const uint64_t t0 = global_timer();
-          while (!mbar_test(full_bar(s), last_fill[s]) && global_timer() - t0 < kWaitLimitNs) {
+          while (!mbar_test<kCluster>(full_bar(s), last_fill[s]) &&
+                 global_timer() - t0 < kWaitLimitNs) {
           }
         }
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(sizeof(T) == 2 && !std::is_same<T, __half>::value);
+    // ------------------------------------------------------------ MMA issuer (leader CTA)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc =
+          make_idesc(sizeof(T) == 2 && !std::is_same<T, __half>::value, C::TILE_M);
       int stage = 0;
       uint32_t phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (uint32_t tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) break;
+      for (uint32_t tile = cluster_id; ok && tile < total_tiles; tile += num_clusters) {
+        if (!mbar_wait<kCluster>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
+          if (!mbar_wait<kCluster>(full_bar(stage), phase, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = ring + stage * STAGE_BYTES;
+          const uint32_t sa = ring + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            umma_f16(d_tmem, sw128_desc(sa + kk * UMMA_K * 2), sw128_desc(sb + kk * UMMA_K * 2),
-                     idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_f16<PAIR>(d_tmem, sw128_desc(sa + kk * UMMA_K * 2), sw128_desc(sb + kk * UMMA_K * 2),
+                           idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(empty_bar(stage));  // ring stage free once these MMAs finish
+          umma_commit<PAIR>(empty_bar(stage));  // ring stage free (in every CTA) once done
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(tfull_bar(acc));  // accumulator ready for the epilogue
+        umma_commit<PAIR>(tfull_bar(acc));  // accumulator ready for the epilogues
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       // every MMA this thread issued must be complete before TMEM is freed
-      umma_commit(drain_bar);
+      umma_commit_local<PAIR>(drain_bar);
       const uint64_t t0 = global_timer();
-      while (!mbar_test(drain_bar, 0) && global_timer() - t0 < kWaitLimitNs) {
+      while (!mbar_test<false>(drain_bar, 0) && global_timer() - t0 < kWaitLimitNs) {
       }
     }
   } else {
@@ -403,10 +533,10 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     const int row = quarter * 32 + lane;
     uint32_t acc = 0, acc_phase = 0;
     T* out = static_cast<T*>(p.out);
-    for (uint32_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      const Tile t = decode_tile(tile, p, s_pref, s_off);
-      const bool row_ok = row < t.rows;
-      const int64_t grow = t.m0 + row;
+    for (uint32_t tile = cluster_id; tile < total_tiles; tile += num_clusters) {
+      const Tile t = decode_tile(tile, p, s_pref, s_off, C::TILE_M);
+      const int64_t grow = t.m0 + (int64_t)rank * BM + row;
+      const bool row_ok = grow < (int64_t)s_off[t.e + 1];
       // the weighted epilogue's slot and routing weight: loaded before the
       // accumulator wait so that their latency overlaps the MMAs
       int64_t wslot = grow;
@@ -417,7 +547,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         wscale = load_dyn(p.weights, p.wdt, s);
       }
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
+      if (lane == 0) ok = mbar_wait<kCluster>(tfull_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
@@ -448,10 +578,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           }
         }
       } else {
-        const int64_t orow = wslot;
-        const float scale = wscale;
         const int64_t col0 = (int64_t)t.nb * 256;
-        T* dst = out + orow * p.n_out + col0;
+        T* dst = out + wslot * p.n_out + col0;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
           uint32_t o[32];
@@ -463,7 +591,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
               if (col0 + c + v * 8 + 8 <= p.n_out) {
                 float f[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[v * 8 + i]) * scale;
+                for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[v * 8 + i]) * wscale;
                 *reinterpret_cast<uint4*>(dst + c + v * 8) = pack8<T>(f);
               }
             }
@@ -472,16 +600,22 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (lane == 0) {
+        if constexpr (kCluster) mbar_arrive_cluster(tempty0_leader + 8u * acc);
+        else mbar_arrive(tempty_bar(acc));
+      }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
 
   __syncthreads();
+  // PAIR == 2: the leader's MMAs write the peer's TMEM and the peer arrives on
+  // the leader's barriers, so neither CTA frees TMEM or exits before both are done
+  if constexpr (kCluster) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc<PAIR>(tmem_base, TMEM_COLS);
   }
 }
 
@@ -531,20 +665,69 @@ bool encode_3d(CUtensorMap* m, const void* base, moe_dtype dt, uint64_t E, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t smem_bytes(int E) { return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + 8 * (size_t)(E + 1); }
+template <int PAIR>
+size_t smem_bytes(int E) {
+  return 1024 + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES + 256 + 8 * (size_t)(E + 1);
+}
 
-template <typename T>
-cudaError_t launch_t(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB0,
-                     const CUtensorMap& mB1, const Params& p, int grid, cudaStream_t s) {
+// Clusters of PAIR CTAs that can be resident at once (one CTA per SM).
+template <typename T, int PAIR>
+cudaError_t resident_clusters(int num_sms, int* out) {
   static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(grouped_gemm_tc<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem_bytes(MAX_E));
+  static cudaError_t err = cudaSuccess;
+  static int clusters = 0;
+  std::call_once(once, [num_sms] {
+    err = cudaFuncSetAttribute(grouped_gemm_tc<T, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_bytes<PAIR>(MAX_E));
+    if (err != cudaSuccess) return;
+    if (PAIR == 1) {
+      clusters = num_sms;
+      return;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = PAIR;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(PAIR * (num_sms / PAIR));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = smem_bytes<PAIR>(MAX_E);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_tc<T, PAIR>, &cfg);
   });
-  if (attr_err != cudaSuccess) return attr_err;
-  grouped_gemm_tc<T><<<grid, THREADS, smem_bytes(a.E), s>>>(mA, mB0, mB1, p);
-  return cudaGetLastError();
+  *out = clusters;
+  return err;
+}
+
+template <typename T, int PAIR>
+cudaError_t launch_t(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB0,
+                     const CUtensorMap& mB1, Params p, int num_sms, cudaStream_t s) {
+  int clusters = 0;
+  cudaError_t err = resident_clusters<T, PAIR>(num_sms, &clusters);
+  if (err != cudaSuccess) return err;
+  if (clusters < 1) return cudaErrorLaunchOutOfResources;
+  constexpr int TM = Cfg<PAIR>::TILE_M;
+  const int64_t mt_max = (a.N + TM - 1) / TM + std::min<int64_t>(a.E, a.N);
+  const int64_t tiles_max = mt_max * p.nb;
+  const int nclu = (int)std::max<int64_t>(1, std::min<int64_t>(clusters, tiles_max));
+  // panel width: about one wave of clusters spread over an expert's expected m-tiles
+  const int64_t mt_per_expert = std::max<int64_t>(1, (a.N + (int64_t)TM * a.E - 1) / ((int64_t)TM * a.E));
+  p.panel = (int)std::max<int64_t>(1, std::min<int64_t>(p.nb, (nclu + mt_per_expert - 1) / mt_per_expert));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(nclu * PAIR);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem_bytes<PAIR>(a.E);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc<T, PAIR>, mA, mB0, mB1, p);
 }
 
 }  // namespace tc
@@ -609,14 +792,16 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, c
     b1 = &w->down;
   }
   p.nb = (int)((a.n_out + p.cols_per_tile - 1) / p.cols_per_tile);
-  const int64_t mt_max = (a.N + tc::BM - 1) / tc::BM + std::min<int64_t>(a.E, a.N);
-  const int64_t tiles_max = mt_max * p.nb;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, tiles_max));
-  // panel width: about one wave of CTAs spread over an expert's expected m-tiles
-  const int64_t mt_per_expert = std::max<int64_t>(1, (a.N + (int64_t)tc::BM * a.E - 1) / ((int64_t)tc::BM * a.E));
-  p.panel = (int)std::max<int64_t>(1, std::min<int64_t>(p.nb, (grid + mt_per_expert - 1) / mt_per_expert));
-  if (a.dt == MOE_BF16) return tc::launch_t<__nv_bfloat16>(a, mA, *b0, *b1, p, grid, s);
-  return tc::launch_t<__half>(a, mA, *b0, *b1, p, grid, s);
+  // CTA pairs halve the B bytes each SM stages per k-block; they pay off when
+  // experts hold at least a full 128-row tile on average.  With fewer rows per
+  // expert (decode-sized batches) the GEMM streams weights from HBM and single
+  // CTAs keep twice as many independent streams in flight.
+  const bool pair = a.N >= (int64_t)tc::BM * a.E;
+  if (a.dt == MOE_BF16)
+    return pair ? tc::launch_t<__nv_bfloat16, 2>(a, mA, *b0, *b1, p, num_sms, s)
+                : tc::launch_t<__nv_bfloat16, 1>(a, mA, *b0, *b1, p, num_sms, s);
+  return pair ? tc::launch_t<__half, 2>(a, mA, *b0, *b1, p, num_sms, s)
+              : tc::launch_t<__half, 1>(a, mA, *b0, *b1, p, num_sms, s);
 }
 
 }  // namespace moe
