@@ -97,13 +97,14 @@ def source_sha256(rel: str) -> str:
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    """nvidia-smi clock / power / throttle sampling; only samples whose
+    timestamps fall inside the timed window are summarised."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 100):
+    def __init__(self, gpu_index: int, period_ms: int = 50):
         self.gpu = gpu_index
         self.period = period_ms
         self.proc = None
@@ -117,7 +118,9 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0: float, t1: float):
+        """Summary of the samples taken between wall-clock times t0 and t1."""
+        import datetime
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -126,22 +129,28 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             text, _ = self.proc.communicate()
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in text.strip().splitlines():
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                v_sm, v_max, v_pw = float(parts[2]), float(parts[3]), float(parts[4])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            if not (t0 <= ts <= t1):
+                continue
+            sm.append(v_sm)
+            smax.append(v_max)
+            power.append(v_pw)
+            for n, v in zip(names, parts[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
+                "power_w_median": statistics.median(power) if power else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -281,13 +290,15 @@ def run_native(args, rank, world, local):
     barrier(world, dev)
     torch.cuda.synchronize(dev)
     clocks.start()
-    time.sleep(0.3)  # let the sampler take its first readings
+    time.sleep(0.3)  # let the sampler start before the timed region
+    w0 = time.time()
     start.record(stream)
     for i in range(K):
         step(ev[i])
     end.record(stream)
     torch.cuda.synchronize(dev)
-    clock_info = clocks.stop()
+    w1 = time.time()
+    clock_info = clocks.stop(w0, w1)
     barrier(world, dev)
     ms_local = start.elapsed_time(end)
     ms_total = max_over_ranks(ms_local, world, dev)
