@@ -15,5 +15,6 @@ from .oracle import (  # noqa: F401
     num_threads,
     round_to_dtype,
     route,
+    route_sigmoid_grouped,
     set_threads,
 )

@@ -29,6 +29,7 @@
  *          then the down product.  SwiGluExperts::new: bias-free weights.
  *   [SILU] MindSpeed-Ops PR 163 diffs, rms_norm_gated notes: silu(x) is
  *          x * sigmoid(x).
+ *   [UG10] ruDNN Benutzerhandbuch, section 10: sigmoid group-limited routing.
  *
  * Readings where the pages leave a step open (the same list is kept in the
  * design notes):
@@ -183,6 +184,105 @@ void oracle_route(const void* logits, int ldt, int64_t T, int64_t E, int k, int 
             route_row(row, E, k, renorm, ldt, idx + t * k, w_pre + t * k, w_cast + t * k);
         }
         free(row);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* sigmoid group-limited routing  [UG10]                                    */
+/* ------------------------------------------------------------------------ */
+/* ruDNN Benutzerhandbuch, section 10 "Gruppenbeschraenktes Sigmoid-MoE-
+ * Routing": scores are sigmoid(logit); an optional FP32 correction bias is
+ * added for the selection only; experts form `groups` equal contiguous
+ * groups; a group's score is the largest corrected score of its experts, or
+ * the sum of its two largest when group_top_two is set; the
+ * `selected_groups` best groups are kept and top_k experts are chosen among
+ * their experts by corrected score; ties go to the lower id (group or
+ * expert).  Weights are the original sigmoid values, optionally
+ * renormalised over the selected experts, times `scale`.
+ *
+ * Readings (also in the design notes):
+ *   S1 the selection runs in FP32 as the page states for the bias: the
+ *      sigmoid is the correctly rounded FP32 value of 1/(1+exp(-x)) (computed
+ *      in double, rounded once), the corrected score is its FP32 sum with the
+ *      bias and the top-two group score is an FP32 sum;
+ *   S2 slot order: descending corrected score, ties to the lower id;
+ *   S3 a row holding a NaN logit or NaN corrected score is all-tied: idx =
+ *      0..k-1 and NaN weights (the section 4 rule carried over);
+ *   S4 weights are stored in the logits dtype (round to nearest even). */
+static float sigmoid_f32(double x) { return (float)(1.0 / (1.0 + exp(-x))); }
+
+/* "a beats b" on FP32 keys: larger first, equal -> lower id */
+static int beats_f(float va, int64_t a, float vb, int64_t b) {
+    if (va > vb) return 1;
+    if (va < vb) return 0;
+    return a < b;
+}
+
+void oracle_route_sigmoid_grouped(const void* logits, int ldt, int64_t T, int64_t E,
+                                  const float* bias, int k, int groups, int selected_groups,
+                                  int group_top_two, int renorm, double scale,
+                                  uint32_t* idx, double* w_pre, double* w_cast) {
+    const int64_t gs = E / groups;
+#pragma omp parallel
+    {
+        float* c = (float*)malloc((size_t)E * sizeof(float));
+        double* sig = (double*)malloc((size_t)E * sizeof(double));
+        float* gscore = (float*)malloc((size_t)groups * sizeof(float));
+        char* gsel = (char*)malloc((size_t)groups);
+        char* used = (char*)malloc((size_t)E);
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < T; ++t) {
+            uint32_t* ix = idx + t * k;
+            double* wp = w_pre + t * k;
+            double* wc = w_cast + t * k;
+            int poisoned = 0;
+            for (int64_t e = 0; e < E; ++e) {
+                const double l = load_elem(logits, ldt, t * E + e);
+                sig[e] = 1.0 / (1.0 + exp(-l));          /* weight value, no rounding */
+                c[e] = sigmoid_f32(l) + (bias ? bias[e] : 0.0f); /* FP32 selection key */
+                if (isnan(l) || isnan(c[e])) poisoned = 1;
+            }
+            if (poisoned) {
+                for (int j = 0; j < k; ++j) { ix[j] = (uint32_t)j; wp[j] = NAN; wc[j] = NAN; }
+                continue;
+            }
+            /* group scores */
+            for (int g = 0; g < groups; ++g) {
+                float best = -INFINITY, second = -INFINITY;
+                int64_t bi = -1;
+                for (int64_t e = g * gs; e < (g + 1) * gs; ++e)
+                    if (bi < 0 || beats_f(c[e], e, best, bi)) { best = c[e]; bi = e; }
+                for (int64_t e = g * gs; e < (g + 1) * gs; ++e)
+                    if (e != bi && c[e] > second) second = c[e];
+                gscore[g] = group_top_two ? best + second : best;
+                gsel[g] = 0;
+            }
+            /* keep the selected_groups best groups */
+            for (int r = 0; r < selected_groups; ++r) {
+                int bg = -1;
+                for (int g = 0; g < groups; ++g)
+                    if (!gsel[g] && (bg < 0 || beats_f(gscore[g], g, gscore[bg], bg))) bg = g;
+                gsel[bg] = 1;
+            }
+            /* top_k experts of the kept groups by corrected score */
+            for (int64_t e = 0; e < E; ++e) used[e] = !gsel[e / gs];
+            double tot = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int64_t be = -1;
+                for (int64_t e = 0; e < E; ++e)
+                    if (!used[e] && (be < 0 || beats_f(c[e], e, c[be], be))) be = e;
+                used[be] = 1;
+                ix[j] = (uint32_t)be;
+                wp[j] = sig[be];
+                tot += sig[be];
+            }
+            for (int j = 0; j < k; ++j) {
+                if (renorm) wp[j] = wp[j] / tot;
+                wp[j] = wp[j] * scale;
+                wc[j] = oracle_round_to_dtype(wp[j], ldt);
+            }
+        }
+        free(c); free(sig); free(gscore); free(gsel); free(used);
     }
 }
 

@@ -50,6 +50,8 @@ def _load():
         I32 = ctypes.c_int
         lib.oracle_route.argtypes = [P, I32, I64, I64, I32, I32, P, P, P]
         lib.oracle_dispatch.argtypes = [P, I64, I64, I32, P, P, P, P]
+        lib.oracle_route_sigmoid_grouped.argtypes = [P, I32, I64, I64, P, I32, I32, I32, I32, I32,
+                                                     ctypes.c_double, P, P, P]
         lib.oracle_experts.argtypes = [P, P, I64, P, P, P, I32, I64, I64, P]
         lib.oracle_combine.argtypes = [P, P, P, I64, I32, I64, P]
         lib.oracle_forward_tokens.argtypes = [P, P, I32, I32, I64, I64, I32, I32, I64, I64,
@@ -105,6 +107,24 @@ def route(logits: np.ndarray, dtype: str, top_k: int, renormalize: bool):
     w_cast = np.empty((T, top_k), np.float64)
     _load().oracle_route(_ptr(s), DTYPE_CODES[dtype], T, E, top_k, int(bool(renormalize)),
                          _ptr(idx), _ptr(w_pre), _ptr(w_cast))
+    return idx, w_pre, w_cast
+
+
+def route_sigmoid_grouped(logits: np.ndarray, dtype: str, top_k: int, groups: int,
+                          selected_groups: int, group_top_two: bool, renormalize: bool,
+                          scale: float = 1.0, bias=None):
+    """Sigmoid group-limited routing: (idx u32 [T,k], w_pre f64 [T,k], w_cast f64 [T,k])."""
+    s = _stored(logits, dtype)
+    T, E = s.shape
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    idx = np.empty((T, top_k), np.uint32)
+    w_pre = np.empty((T, top_k), np.float64)
+    w_cast = np.empty((T, top_k), np.float64)
+    _load().oracle_route_sigmoid_grouped(_ptr(s), DTYPE_CODES[dtype], T, E,
+                                         _ptr(b) if b is not None else None, top_k, groups,
+                                         selected_groups, int(bool(group_top_two)),
+                                         int(bool(renormalize)), float(scale),
+                                         _ptr(idx), _ptr(w_pre), _ptr(w_cast))
     return idx, w_pre, w_cast
 
 

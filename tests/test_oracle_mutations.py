@@ -24,6 +24,12 @@ MUTATIONS = {
     "renorm_dropped": ("for (int j = 0; j < k; ++j) w_pre[j] = w_pre[j] / tot;", ";"),
     "combine_unweighted": ("w_cast[t * k + j] * expert_out[r * H + c]", "expert_out[r * H + c]"),
     "softmax_without_max_shift": ("s += exp(l[e] - m);", "s += exp(l[e]);"),
+    "sigmoid_bias_in_weights": ("sig[e] = 1.0 / (1.0 + exp(-l));",
+                                "sig[e] = 1.0 / (1.0 + exp(-l)) + (bias ? bias[e] : 0.0);"),
+    "sigmoid_top_two_ignored": ("gscore[g] = group_top_two ? best + second : best;",
+                                "gscore[g] = best;"),
+    "sigmoid_group_tie_to_higher": ("if (!gsel[g] && (bg < 0 || beats_f(gscore[g], g, gscore[bg], bg))) bg = g;",
+                                    "if (!gsel[g] && (bg < 0 || gscore[g] >= gscore[bg])) bg = g;"),
 }
 
 
@@ -39,7 +45,8 @@ def test_pins_catch_planted_mistake(tmp_path, name):
                     ignore=shutil.ignore_patterns("__pycache__"))
     (root / "oracle" / "moe_oracle.c").write_text(src.replace(old, new))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider",
-                        "tests/test_oracle_pins.py"], cwd=root, capture_output=True, text=True,
+                        "tests/test_oracle_pins.py", "tests/test_oracle_sigmoid_pins.py"],
+                       cwd=root, capture_output=True, text=True,
                        timeout=600)
     tail = r.stdout.strip().splitlines()[-1] if r.stdout.strip() else r.stderr[-500:]
     assert r.returncode != 0 and "failed" in tail, f"{name} went unnoticed: {tail}"
