@@ -82,6 +82,41 @@ moe_status moe_route(const void* logits, moe_dtype logits_dtype, int64_t T, int6
                      float* weights_f32, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Sigmoid group-limited routing.  ruDNN Benutzerhandbuch, section 10
+ * "Gruppenbeschraenktes Sigmoid-MoE-Routing" (GroupRoutingOptions).
+ *
+ * Per row: scores s_e = sigmoid(logit_e); corrected scores c_e = s_e +
+ * bias_e (bias: optional FP32 [E] device array; it only affects the
+ * selection); the E experts form `groups` contiguous groups of E/groups; a
+ * group scores max c over its experts, or the sum of its two largest c when
+ * group_top_two != 0; the `selected_groups` best groups are kept and top_k
+ * experts are chosen among their experts by c.  Ties go to the lower id.
+ * Selection runs in FP32 with the correctly rounded FP32 sigmoid.  Weights
+ * are s of the chosen experts, divided by their FP32 sum (slot order) when
+ * renormalize != 0, times scale, rounded to the logits dtype; idx lists the
+ * chosen experts in descending c.  A row holding a NaN logit (or NaN
+ * corrected score) gets idx = 0..top_k-1 and NaN weights.
+ * Rules (MOE_ERR_INVALID_ARG unless noted): 1 <= E <= 1024
+ * (MOE_ERR_UNSUPPORTED above), 1 <= groups <= 128, E % groups == 0,
+ * 1 <= selected_groups <= groups, 1 <= top_k <= 64 and top_k <=
+ * selected_groups * E/groups, group_top_two needs E/groups >= 2, scale
+ * finite and > 0.  Outputs as for moe_route.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    int32_t top_k;
+    int32_t groups;
+    int32_t selected_groups;
+    int32_t group_top_two;
+    int32_t renormalize;
+    float scale;
+} moe_group_routing_options;
+
+moe_status moe_route_sigmoid_grouped(const void* logits, moe_dtype logits_dtype, int64_t T,
+                                     int64_t E, const float* bias,
+                                     const moe_group_routing_options* options, uint32_t* idx,
+                                     void* weights, float* weights_f32, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Dispatch.  ruDNN Benutzerhandbuch, section 5 "Expertengewichte und
  * Verteilung" (no token dropped; a stored map restores token order) and
  * the DispatchedTokens invariant in src/moe/experts.rs ("complete, monotone
@@ -203,6 +238,15 @@ moe_status moe_forward(moe_experts_t experts, const void* x, const void* logits,
                        moe_dtype logits_dtype, int64_t T, int32_t top_k, int renormalize,
                        void* y, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* SwiGluExperts::forward_sigmoid_grouped in src/moe/experts.rs: the fused
+ * forward with moe_route_sigmoid_grouped as its routing step (user guide,
+ * section 10).  Same buffers and workspace as moe_forward with
+ * top_k = options->top_k (moe_forward_workspace_size applies). */
+moe_status moe_forward_sigmoid_grouped(moe_experts_t experts, const void* x, const void* logits,
+                                       moe_dtype logits_dtype, int64_t T, const float* bias,
+                                       const moe_group_routing_options* options, void* y,
+                                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Same as moe_forward, and records CUDA events on `stream` at the stage
  * boundaries: events[0] before routing, [1] after routing, [2] after
  * dispatch, [3] after the gate/up projection, [4] after the down projection,
@@ -244,6 +288,15 @@ moe_status moe_forward_layout(moe_experts_t experts, int64_t T, int32_t top_k,
  * the kernel returned early; its outputs are undefined).  MOE_ERR_CUDA if
  * the synchronisation itself fails. */
 moe_status moe_get_device_status(const void* workspace, cudaStream_t stream);
+
+/* Diagnostics (no counterpart on the pages): exercises the failure path of
+ * the bounded waits inside this library's kernels.  Enqueues one small kernel
+ * that waits on a barrier nothing completes; after limit_ms (1..2000) the
+ * wait gives up, the kernel writes MOE_ERR_DEVICE_TIMEOUT into the status
+ * word at the start of `workspace` (>= 256 bytes, 256-byte aligned, device)
+ * and returns normally.  moe_get_device_status(workspace, stream) then
+ * reports MOE_ERR_DEVICE_TIMEOUT and the CUDA context stays usable. */
+moe_status moe_selftest_bounded_wait(void* workspace, uint32_t limit_ms, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

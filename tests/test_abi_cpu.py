@@ -162,3 +162,30 @@ def test_product_never_imports_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
                 assert "moe_oracle" not in src, f
+
+
+def _opts(top_k=8, groups=8, sel=4, top_two=1, renorm=1, scale=2.5):
+    from top_routing_grouped_fp32_gb300 import _lib
+    return _lib.GroupRoutingOptions(top_k, groups, sel, top_two, renorm, scale)
+
+
+@pytest.mark.parametrize("E,opt,want", [
+    (256, dict(), OK),                                   # DeepSeek-style: 8 groups, keep 4, top-two
+    (256, dict(groups=0), INVALID_ARG),                  # groups in 1..=128
+    (256, dict(groups=256), INVALID_ARG),
+    (250, dict(), INVALID_ARG),                          # E divisible by groups
+    (256, dict(sel=0), INVALID_ARG),                     # selected groups valid
+    (256, dict(sel=9), INVALID_ARG),
+    (256, dict(top_k=65), INVALID_ARG),                  # top-k in 1..=64
+    (64, dict(top_k=20, groups=8, sel=2), INVALID_ARG),  # top-k <= experts of the kept groups
+    (8, dict(top_k=2, groups=8, sel=4, top_two=1), INVALID_ARG),  # top-two needs >= 2 per group
+    (256, dict(scale=0.0), INVALID_ARG),                 # scale finite and positive
+    (256, dict(scale=float("inf")), INVALID_ARG),
+    (2048, dict(), UNSUPPORTED),                         # experts in 1..=1024
+])
+def test_sigmoid_group_option_rules(lib, E, opt, want):
+    o = _opts(**opt)
+    # T = 0: only the option rules run, nothing is launched
+    st = lib.moe_route_sigmoid_grouped(None, BF16, 0, E, None, ctypes.byref(o), None, None, None, None)
+    assert st == want, _msg(lib)
+    assert lib.moe_route_sigmoid_grouped(FAKE, BF16, 4, E, None, None, FAKE, FAKE, None, None) == INVALID_ARG

@@ -28,7 +28,8 @@ from ._lib import DTYPE_CODES, MoeError  # noqa: F401
 _TORCH_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 _CODE_TORCH = {v: k for k, v in _TORCH_CODES.items()}
 
-__all__ = ["load", "moe_route", "moe_dispatch", "moe_combine", "SwiGluExperts", "Dispatched",
+__all__ = ["load", "moe_route", "moe_route_sigmoid_grouped", "moe_dispatch", "moe_combine",
+           "SwiGluExperts", "Dispatched",
            "moe_get_device_status", "MoeError", "library_path"]
 
 
@@ -79,6 +80,32 @@ def moe_route(logits: torch.Tensor, top_k: int, renormalize: bool, weights_f32: 
     w32 = torch.empty((T, top_k), dtype=torch.float32, device=logits.device) if weights_f32 else None
     _lib.check(lib.moe_route(_ptr(logits), _code(logits), T, E, top_k, int(bool(renormalize)),
                              _ptr(idx), _ptr(w), _ptr(w32), _stream(stream)))
+    return (idx, w, w32) if weights_f32 else (idx, w)
+
+
+def group_options(top_k: int, groups: int, selected_groups: int, group_top_two: bool,
+                  renormalize: bool, scale: float = 1.0):
+    return _lib.GroupRoutingOptions(top_k, groups, selected_groups, int(bool(group_top_two)),
+                                    int(bool(renormalize)), float(scale))
+
+
+def moe_route_sigmoid_grouped(logits: torch.Tensor, top_k: int, groups: int, selected_groups: int,
+                              group_top_two: bool, renormalize: bool, scale: float = 1.0,
+                              bias: torch.Tensor | None = None, weights_f32: bool = False,
+                              stream=None):
+    """Sigmoid group-limited routing (user guide, section 10).  ``bias``: optional
+    FP32 [E] correction used for the selection only."""
+    lib = load()
+    T, E = logits.shape
+    if bias is not None and (bias.dtype != torch.float32 or bias.shape != (E,)):
+        raise MoeError(1, "bias must be a float32 [E] tensor")
+    opt = group_options(top_k, groups, selected_groups, group_top_two, renormalize, scale)
+    idx = torch.empty((T, top_k), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, top_k), dtype=logits.dtype, device=logits.device)
+    w32 = torch.empty((T, top_k), dtype=torch.float32, device=logits.device) if weights_f32 else None
+    _lib.check(lib.moe_route_sigmoid_grouped(_ptr(logits), _code(logits), T, E, _ptr(bias),
+                                             ctypes.byref(opt), _ptr(idx), _ptr(w), _ptr(w32),
+                                             _stream(stream)))
     return (idx, w, w32) if weights_f32 else (idx, w)
 
 
@@ -211,6 +238,23 @@ class SwiGluExperts:
         else:
             arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
             _lib.check(self._lib.moe_forward_timed(*args, arr, len(events)))
+        return y
+
+    def forward_sigmoid_grouped(self, x: torch.Tensor, logits: torch.Tensor, top_k: int, groups: int,
+                                selected_groups: int, group_top_two: bool, renormalize: bool,
+                                scale: float = 1.0, bias: torch.Tensor | None = None, y=None,
+                                workspace=None, stream=None) -> torch.Tensor:
+        """Fused forward with sigmoid group-limited routing
+        (SwiGluExperts::forward_sigmoid_grouped)."""
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty((T, self.H), dtype=self.dtype, device=x.device)
+        if workspace is None:
+            workspace = self.forward_workspace(T, top_k, logits.dtype)
+        opt = group_options(top_k, groups, selected_groups, group_top_two, renormalize, scale)
+        _lib.check(self._lib.moe_forward_sigmoid_grouped(
+            self.handle, _ptr(x), _ptr(logits), _code(logits), T, _ptr(bias), ctypes.byref(opt),
+            _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)))
         return y
 
     def forward_host(self, x_host: torch.Tensor, logits_host: torch.Tensor, top_k: int,

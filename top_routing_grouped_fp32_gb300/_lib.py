@@ -40,6 +40,13 @@ class ForwardLayout(ctypes.Structure):
                 ("idx", "weights", "offsets", "perm", "x_disp", "h", "slots", "total")]
 
 
+class GroupRoutingOptions(ctypes.Structure):
+    """moe_group_routing_options (user guide, section 10)."""
+    _fields_ = [("top_k", ctypes.c_int32), ("groups", ctypes.c_int32),
+                ("selected_groups", ctypes.c_int32), ("group_top_two", ctypes.c_int32),
+                ("renormalize", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -54,6 +61,10 @@ _SIGNATURES = {
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_status_string": (ctypes.c_char_p, [ST]),
     "moe_route": (ST, [P, INT, I64, I64, I32, INT, P, P, P, P]),
+    "moe_route_sigmoid_grouped": (ST, [P, INT, I64, I64, P, ctypes.POINTER(GroupRoutingOptions),
+                                       P, P, P, P]),
+    "moe_forward_sigmoid_grouped": (ST, [P, P, P, INT, I64, P, ctypes.POINTER(GroupRoutingOptions),
+                                         P, P, SZ, P]),
     "moe_dispatch_workspace_size": (SZ, [I64, I64, I32]),
     "moe_dispatch": (ST, [P, I64, I64, I32, P, INT, I64, P, P, P, P, P, SZ, P]),
     "moe_dispatch_noalloc": (ST, [P, I64, I64, I32, P, INT, I64, P, P, P, P, P]),
@@ -70,6 +81,7 @@ _SIGNATURES = {
     "moe_forward_host": (ST, [P, P, P, INT, I64, I32, INT, P, P, SZ, P]),
     "moe_forward_layout": (ST, [P, I64, I32, INT, ctypes.POINTER(ForwardLayout)]),
     "moe_get_device_status": (ST, [P, P]),
+    "moe_selftest_bounded_wait": (ST, [P, ctypes.c_uint32, P]),
 }
 
 

@@ -9,9 +9,11 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <string>
 
 #include "common.cuh"
@@ -79,6 +81,34 @@ moe_status check_tek(int64_t T, int64_t E, int32_t k) {
   if (k > kMaxK) return fail(MOE_ERR_UNSUPPORTED, "top_k=%d exceeds the supported 64", k);
   if (T > kMaxRows / k)
     return fail(MOE_ERR_UNSUPPORTED, "T*top_k=%lld exceeds 2^31-1", (long long)T * k);
+  return MOE_OK;
+}
+
+// GroupRoutingOptions rules of the user guide, section 10.
+moe_status check_group_options(int64_t T, int64_t E, const moe_group_routing_options* o) {
+  if (!o) return fail(MOE_ERR_INVALID_ARG, "group routing options are NULL");
+  if (T < 0) return fail(MOE_ERR_SHAPE, "T must be >= 0 (got %lld)", (long long)T);
+  if (E < 1 || E > kMaxE)
+    return fail(E < 1 ? MOE_ERR_SHAPE : MOE_ERR_UNSUPPORTED, "expert count must be in 1..=1024 (got %lld)",
+                (long long)E);
+  if (o->groups < 1 || o->groups > 128)
+    return fail(MOE_ERR_INVALID_ARG, "group count must be in 1..=128 (got %d)", o->groups);
+  if (E % o->groups != 0)
+    return fail(MOE_ERR_INVALID_ARG, "expert count %lld is not divisible by %d groups", (long long)E, o->groups);
+  if (o->selected_groups < 1 || o->selected_groups > o->groups)
+    return fail(MOE_ERR_INVALID_ARG, "selected_groups must be in 1..=groups (got %d of %d)",
+                o->selected_groups, o->groups);
+  const int64_t per = E / o->groups;
+  if (o->top_k < 1 || o->top_k > 64)
+    return fail(MOE_ERR_INVALID_ARG, "top_k must be in 1..=64 (got %d)", o->top_k);
+  if (o->top_k > o->selected_groups * per)
+    return fail(MOE_ERR_INVALID_ARG, "top_k=%d exceeds the %lld experts of the selected groups", o->top_k,
+                (long long)(o->selected_groups * per));
+  if (o->group_top_two && per < 2)
+    return fail(MOE_ERR_INVALID_ARG, "group_top_two needs at least two experts per group");
+  if (!(o->scale > 0.f) || !std::isfinite(o->scale))
+    return fail(MOE_ERR_INVALID_ARG, "scale must be finite and positive");
+  if (T > kMaxRows / o->top_k) return fail(MOE_ERR_UNSUPPORTED, "T*top_k exceeds 2^31-1");
   return MOE_OK;
 }
 
@@ -178,6 +208,14 @@ moe_status run_experts(const moe_experts* x, const void* x_disp, int64_t N, cons
   return MOE_OK;
 }
 
+// The routing step of a fused forward: writes idx [T,k] and weights [T,k]
+// (logits dtype) on the stream.
+using RouteFn = std::function<cudaError_t(uint32_t* idx, void* w, cudaStream_t s)>;
+
+moe_status forward_core(moe_experts_t x, const void* xin, const void* logits, moe_dtype ldt,
+                        int64_t T, int32_t k, const RouteFn& route, void* y, void* ws,
+                        size_t ws_bytes, cudaStream_t s, void* const* ev);
+
 moe_status forward_impl(moe_experts_t x, const void* xin, const void* logits, moe_dtype ldt,
                         int64_t T, int32_t k, int renorm, void* y, void* ws, size_t ws_bytes,
                         cudaStream_t s, void* const* ev) {
@@ -185,6 +223,17 @@ moe_status forward_impl(moe_experts_t x, const void* xin, const void* logits, mo
   if (st != MOE_OK) return st;
   if (!valid_dtype(ldt)) return fail(MOE_ERR_DTYPE, "logits dtype %d is not F32/F16/BF16", (int)ldt);
   if ((st = check_tek(T, x->E, k)) != MOE_OK) return st;
+  const int E = (int)x->E;
+  RouteFn route = [=](uint32_t* idx, void* w, cudaStream_t st_) {
+    return moe::launch_route(logits, ldt, T, E, k, renorm, idx, w, nullptr, nullptr, st_);
+  };
+  return forward_core(x, xin, logits, ldt, T, k, route, y, ws, ws_bytes, s, ev);
+}
+
+moe_status forward_core(moe_experts_t x, const void* xin, const void* logits, moe_dtype ldt,
+                        int64_t T, int32_t k, const RouteFn& route, void* y, void* ws,
+                        size_t ws_bytes, cudaStream_t s, void* const* ev) {
+  moe_status st;
   if (T == 0) return ok();
   if (!xin || !logits || !y) return fail(MOE_ERR_INVALID_ARG, "x, logits and y must be non-NULL");
   if (!aligned16(xin) || !aligned16(y))
@@ -203,8 +252,7 @@ moe_status forward_impl(moe_experts_t x, const void* xin, const void* logits, mo
     return ev ? cudaEventRecord((cudaEvent_t)ev[i], s) : cudaSuccess;
   };
   MOE_TRY_CUDA(rec(0), "cudaEventRecord");
-  MOE_TRY_CUDA(moe::launch_route(logits, ldt, T, E, k, renorm, idx, w, nullptr, nullptr, s),
-               "routing kernel launch");
+  MOE_TRY_CUDA(route(idx, w, s), "routing kernel launch");
   MOE_TRY_CUDA(rec(1), "cudaEventRecord");
   MOE_TRY_CUDA(moe::launch_dispatch(idx, T, E, k, offsets, nullptr, perm, at<void>(ws, L.scratch),
                                     status, s),
@@ -254,6 +302,24 @@ moe_status moe_route(const void* logits, moe_dtype ldt, int64_t T, int64_t E, in
   MOE_TRY_CUDA(moe::launch_route(logits, ldt, T, (int)E, top_k, renormalize, idx, weights,
                                  weights_f32, nullptr, stream),
                "routing kernel launch");
+  return ok();
+}
+
+// ---- sigmoid group-limited routing ---------------------------------------
+moe_status moe_route_sigmoid_grouped(const void* logits, moe_dtype ldt, int64_t T, int64_t E,
+                                     const float* bias, const moe_group_routing_options* opt,
+                                     uint32_t* idx, void* weights, float* weights_f32,
+                                     cudaStream_t stream) {
+  if (!valid_dtype(ldt)) return fail(MOE_ERR_DTYPE, "logits dtype %d is not F32/F16/BF16", (int)ldt);
+  moe_status st = check_group_options(T, E, opt);
+  if (st != MOE_OK) return st;
+  if (T == 0) return ok();
+  if (!logits || !idx || !weights) return fail(MOE_ERR_INVALID_ARG, "logits, idx and weights must be non-NULL");
+  MOE_TRY_CUDA(moe::launch_route_sigmoid_grouped(logits, ldt, T, (int)E, bias, opt->top_k, opt->groups,
+                                                 opt->selected_groups, opt->group_top_two,
+                                                 opt->renormalize, opt->scale, idx, weights,
+                                                 weights_f32, stream),
+               "sigmoid routing kernel launch");
   return ok();
 }
 
@@ -458,6 +524,24 @@ moe_status moe_forward(moe_experts_t x, const void* xin, const void* logits, moe
   return forward_impl(x, xin, logits, ldt, T, top_k, renormalize, y, ws, ws_bytes, stream, nullptr);
 }
 
+moe_status moe_forward_sigmoid_grouped(moe_experts_t x, const void* xin, const void* logits,
+                                       moe_dtype ldt, int64_t T, const float* bias,
+                                       const moe_group_routing_options* opt, void* y, void* ws,
+                                       size_t ws_bytes, cudaStream_t stream) {
+  moe_status st = check_handle(x);
+  if (st != MOE_OK) return st;
+  if (!valid_dtype(ldt)) return fail(MOE_ERR_DTYPE, "logits dtype %d is not F32/F16/BF16", (int)ldt);
+  if ((st = check_group_options(T, x->E, opt)) != MOE_OK) return st;
+  const int E = (int)x->E;
+  const moe_group_routing_options o = *opt;
+  RouteFn route = [=](uint32_t* idx, void* w, cudaStream_t st_) {
+    return moe::launch_route_sigmoid_grouped(logits, ldt, T, E, bias, o.top_k, o.groups,
+                                             o.selected_groups, o.group_top_two, o.renormalize,
+                                             o.scale, idx, w, nullptr, st_);
+  };
+  return forward_core(x, xin, logits, ldt, T, o.top_k, route, y, ws, ws_bytes, stream, nullptr);
+}
+
 moe_status moe_forward_timed(moe_experts_t x, const void* xin, const void* logits, moe_dtype ldt,
                              int64_t T, int32_t top_k, int renormalize, void* y, void* ws,
                              size_t ws_bytes, cudaStream_t stream, void* const* events, int n_events) {
@@ -498,6 +582,16 @@ moe_status moe_forward_host(moe_experts_t x, const void* x_host, const void* log
   st = forward_impl(x, xs, ls, ldt, T, top_k, renormalize, ys, ws, base, stream, nullptr);
   if (st != MOE_OK) return st;
   MOE_TRY_CUDA(cudaMemcpyAsync(y_host, ys, xb, cudaMemcpyDeviceToHost, stream), "cudaMemcpyAsync y");
+  return ok();
+}
+
+moe_status moe_selftest_bounded_wait(void* ws, uint32_t limit_ms, cudaStream_t stream) {
+  if ((ws == nullptr) || !aligned256(ws))
+    return fail(MOE_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
+  if (limit_ms < 1 || limit_ms > 2000) return fail(MOE_ERR_INVALID_ARG, "limit_ms must be in [1, 2000]");
+  MOE_TRY_CUDA(cudaMemsetAsync(ws, 0, 4, stream), "cudaMemsetAsync");
+  MOE_TRY_CUDA(moe::launch_bounded_wait_selftest(status_word(ws), (uint64_t)limit_ms * 1000000ull, stream),
+               "self-test kernel launch");
   return ok();
 }
 

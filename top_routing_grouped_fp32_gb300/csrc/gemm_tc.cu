@@ -153,14 +153,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 // aborting or the time limit passed (then the abort flag and status are set).
 template <bool CLUSTER>
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                       uint32_t* status) {
+                                       uint32_t* status, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_test<CLUSTER>(bar, parity)) return true;
   const uint64_t t0 = global_timer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_test<CLUSTER>(bar, parity)) return true;
     if ((n & 127u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer() - t0 > kWaitLimitNs) {
+      if (global_timer() - t0 > limit_ns) {
         *abort_flag = 1u;
         set_status(status, (uint32_t)MOE_ERR_DEVICE_TIMEOUT);
         return false;
@@ -619,6 +619,24 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   }
 }
 
+// ---------------------------------------------------------------- self-test
+// Exercises the path every bounded wait of this file takes when it gives up:
+// one warp waits on an mbarrier that nothing will complete; after limit_ns
+// the wait records MOE_ERR_DEVICE_TIMEOUT in the status word and the kernel
+// returns normally, leaving the context usable.
+__global__ void bounded_wait_selftest(uint32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait<false>(smem_u32(&bar), 0, &abort_flag, status, limit_ns);
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -763,6 +781,11 @@ TcWeights* tc_weights_create(const void* gate, const void* up, const void* down,
 }
 
 void tc_weights_destroy(TcWeights* w) { delete w; }
+
+cudaError_t launch_bounded_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s) {
+  tc::bounded_wait_selftest<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, cudaStream_t s) {
   CUtensorMap mA;

@@ -15,6 +15,11 @@ cudaError_t launch_route(const void* logits, moe_dtype ldt, int64_t T, int E, in
                          uint32_t* idx, void* weights, float* w32, uint32_t* status_reset,
                          cudaStream_t s);
 
+cudaError_t launch_route_sigmoid_grouped(const void* logits, moe_dtype ldt, int64_t T, int E,
+                                         const float* bias, int k, int groups, int sel_groups,
+                                         int top_two, int renorm, float scale, uint32_t* idx,
+                                         void* weights, float* w32, cudaStream_t s);
+
 // ---- dispatch (dispatch.cu) ------------------------------------------------
 constexpr int kDispatchChunk = 256;  // tokens per block of the dispatch kernels
 inline int64_t dispatch_chunks(int64_t T) { return (T + kDispatchChunk - 1) / kDispatchChunk; }
@@ -69,5 +74,7 @@ TcWeights* tc_weights_create(const void* gate, const void* up, const void* down,
 void tc_weights_destroy(TcWeights* w);
 cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, cudaStream_t s);
 bool tc_supported(moe_dtype dt, int64_t I, int64_t H);
+// a kernel whose bounded wait is made to expire (failure-path self-test)
+cudaError_t launch_bounded_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace moe

@@ -180,6 +180,185 @@ cudaError_t launch_typed(const void* logits, int64_t T_rows, int E, int k, int r
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Sigmoid group-limited routing: ruDNN user guide ("ruDNN Benutzerhandbuch"),
+// section 10.  Scores are sigmoid(logit); an optional FP32 correction bias is
+// added for the selection only; the E experts form `groups` contiguous
+// groups of E/groups; a group scores the largest corrected value of its
+// experts (or the FP32 sum of its two largest with group_top_two); the
+// `sel_groups` best groups are kept and top_k experts are chosen among
+// theirs by corrected score; ties go to the lower id; weights are the
+// original sigmoid values, optionally renormalised (FP32 sum in slot order),
+// times `scale`, rounded to the logits dtype.
+//
+// The selection is an FP32 decision, so the sigmoid is the correctly rounded
+// FP32 value: computed with a double-precision exp and rounded once.  A row
+// with a NaN logit or NaN corrected score gets idx = 0..k-1 and NaN weights.
+//
+// One warp per row; the corrected scores of the row sit in the warp's slice
+// of shared memory so that any group size can be scanned; the arg-max rounds
+// run on registers as in the softmax router.
+constexpr int kSigMaxGroups = 128;
+
+template <typename T, int VPL>
+__global__ void __launch_bounds__(32 * kRowsPerBlock)
+route_sigmoid_grouped_kernel(const T* __restrict__ logits, int64_t T_rows, int E,
+                             const float* __restrict__ bias, int k, int groups, int sel_groups,
+                             int top_two, int renorm, float scale, uint32_t* __restrict__ idx,
+                             T* __restrict__ w_out, float* __restrict__ w32) {
+  extern __shared__ float sig_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * kRowsPerBlock + warp;
+  float* c_row = sig_smem + warp * (E + 2 * kSigMaxGroups);  // corrected scores [E]
+  float* gscore = c_row + E;                                  // group scores [groups]
+  float* gsel = gscore + kSigMaxGroups;                       // 1.0 when kept
+  if (t >= T_rows) return;
+
+  float v[VPL];
+  load_row<T, VPL>(logits + t * E, E, lane, v);
+  const int e0 = lane * VPL;
+  float sg[VPL], c[VPL];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = e0 + i;
+    if (e < E) {
+      sg[i] = (float)(1.0 / (1.0 + exp(-(double)v[i])));
+      c[i] = sg[i] + (bias ? __ldg(bias + e) : 0.f);
+      bad |= isnan(v[i]) || isnan(c[i]);
+      c_row[e] = c[i];
+    } else {
+      sg[i] = 0.f;
+      c[i] = -INFINITY;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad)) {
+    for (int j = lane; j < k; j += 32) {
+      idx[t * k + j] = (uint32_t)j;
+      w_out[t * k + j] = from_f32<T>(NAN);
+      if (w32) w32[t * k + j] = NAN;
+    }
+    return;
+  }
+  __syncwarp();
+  // group scores (lane g handles groups g, g+32, ...)
+  const int gs = E / groups;
+  for (int g = lane; g < groups; g += 32) {
+    float best = -INFINITY, second = -INFINITY;
+    int bi = -1;
+    for (int e = g * gs; e < (g + 1) * gs; ++e) {
+      const float x = c_row[e];
+      if (bi < 0 || beats(x, e, best, bi)) {
+        if (bi >= 0) second = fmaxf(second, best);
+        best = x;
+        bi = e;
+      } else {
+        second = fmaxf(second, x);
+      }
+    }
+    gscore[g] = top_two ? best + second : best;
+    gsel[g] = 0.f;
+  }
+  __syncwarp();
+  // keep the sel_groups best groups
+  for (int r = 0; r < sel_groups; ++r) {
+    float bv = -INFINITY;
+    int bg = 0x7fffffff;
+    for (int g = lane; g < groups; g += 32)
+      if (gsel[g] == 0.f && beats(gscore[g], g, bv, bg)) {
+        bv = gscore[g];
+        bg = g;
+      }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+      const int og = __shfl_xor_sync(0xffffffffu, bg, d);
+      if (beats(ov, og, bv, bg)) {
+        bv = ov;
+        bg = og;
+      }
+    }
+    if ((bg & 31) == lane) gsel[bg] = 1.f;
+    __syncwarp();
+  }
+  // experts outside the kept groups take no part
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (e0 + i >= E || gsel[(e0 + i) / gs] == 0.f) taken |= 1u << i;
+
+  uint32_t my_idx[2] = {0, 0};
+  float my_p[2] = {0.f, 0.f};
+  float sel_sum = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY, bs = 0.f;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      if (!(taken >> i & 1u) && beats(c[i], e0 + i, bv, bi)) {
+        bv = c[i];
+        bi = e0 + i;
+        bs = sg[i];
+      }
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+      const float os = __shfl_xor_sync(0xffffffffu, bs, d);
+      if (beats(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+        bs = os;
+      }
+    }
+    if (bi / VPL == lane) taken |= 1u << (bi % VPL);
+    sel_sum += bs;
+    if ((j & 31) == lane) {
+      my_idx[j >> 5] = (uint32_t)bi;
+      my_p[j >> 5] = bs;
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = h * 32 + lane;
+    if (j < k) {
+      const float w = (renorm ? my_p[h] / sel_sum : my_p[h]) * scale;
+      idx[t * k + j] = my_idx[h];
+      w_out[t * k + j] = from_f32<T>(w);
+      if (w32) w32[t * k + j] = w;
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_sigmoid_typed(const void* logits, int64_t T_rows, int E, const float* bias,
+                                 int k, int groups, int sel_groups, int top_two, int renorm,
+                                 float scale, uint32_t* idx, void* weights, float* w32,
+                                 cudaStream_t s) {
+  dim3 grid((unsigned)((T_rows + kRowsPerBlock - 1) / kRowsPerBlock));
+  dim3 block(32 * kRowsPerBlock);
+  const size_t smem = (size_t)kRowsPerBlock * (E + 2 * kSigMaxGroups) * sizeof(float);
+  const T* l = static_cast<const T*>(logits);
+  T* w = static_cast<T*>(weights);
+#define MOE_SIG_CASE(V)                                                                          \
+  route_sigmoid_grouped_kernel<T, V><<<grid, block, smem, s>>>(l, T_rows, E, bias, k, groups,    \
+                                                               sel_groups, top_two, renorm,       \
+                                                               scale, idx, w, w32);               \
+  break;
+  switch ((E + 31) / 32 <= 1 ? 1 : (E + 31) / 32 <= 2 ? 2 : (E + 31) / 32 <= 4 ? 4
+          : (E + 31) / 32 <= 8 ? 8 : (E + 31) / 32 <= 16 ? 16 : 32) {
+    case 1: MOE_SIG_CASE(1)
+    case 2: MOE_SIG_CASE(2)
+    case 4: MOE_SIG_CASE(4)
+    case 8: MOE_SIG_CASE(8)
+    case 16: MOE_SIG_CASE(16)
+    default: MOE_SIG_CASE(32)
+  }
+#undef MOE_SIG_CASE
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_route(const void* logits, moe_dtype ldt, int64_t T, int E, int k, int renorm,
@@ -192,6 +371,23 @@ cudaError_t launch_route(const void* logits, moe_dtype ldt, int64_t T, int E, in
       return launch_typed<__half>(logits, T, E, k, renorm, idx, weights, w32, status_reset, s);
     default:
       return launch_typed<__nv_bfloat16>(logits, T, E, k, renorm, idx, weights, w32, status_reset, s);
+  }
+}
+
+cudaError_t launch_route_sigmoid_grouped(const void* logits, moe_dtype ldt, int64_t T, int E,
+                                         const float* bias, int k, int groups, int sel_groups,
+                                         int top_two, int renorm, float scale, uint32_t* idx,
+                                         void* weights, float* w32, cudaStream_t s) {
+  switch (ldt) {
+    case MOE_F32:
+      return launch_sigmoid_typed<float>(logits, T, E, bias, k, groups, sel_groups, top_two, renorm,
+                                         scale, idx, weights, w32, s);
+    case MOE_F16:
+      return launch_sigmoid_typed<__half>(logits, T, E, bias, k, groups, sel_groups, top_two, renorm,
+                                          scale, idx, weights, w32, s);
+    default:
+      return launch_sigmoid_typed<__nv_bfloat16>(logits, T, E, bias, k, groups, sel_groups, top_two,
+                                                 renorm, scale, idx, weights, w32, s);
   }
 }
 
