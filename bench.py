@@ -36,8 +36,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch of the gate/up GEMM on the headline workload, from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel source it was taken on; reported as null once the source changes.
-GATEUP_TRAFFIC = {"bytes": 1140981000 + 261445120,
-                  "source_sha256": "d806f334b1934ac019e7e935132df59531c1246f63e40e9b3ca36844b9404061"}
+GATEUP_TRAFFIC = {"bytes": 1142896000 + 263958016,
+                  "source_sha256": "35c95b98318c33bfdea14109b49b4df6e2080f98e6e4acce39e0cb06ae83c844"}
 
 
 def parse_args(argv=None):
@@ -47,6 +47,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--dtype", choices=["bf16", "f16"], default=None,
+                   help="store the workload in this dtype instead of its own")
     p.add_argument("--e2e-steps", type=int, default=50)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -254,7 +256,7 @@ def workload_config(wl):
 def run_native(args, rank, world, local):
     import torch
     import top_routing_grouped_fp32_gb300 as moe
-    from top_routing_grouped_fp32_gb300.inputs import WORKLOADS, make_inputs
+    from top_routing_grouped_fp32_gb300.inputs import WORKLOADS, make_inputs, with_dtype
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device (the native arm has no CPU path)")
@@ -264,11 +266,12 @@ def run_native(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     moe.load()
-    wl = WORKLOADS[args.workload]
+    wl = with_dtype(WORKLOADS[args.workload], args.dtype or WORKLOADS[args.workload].dtype)
     inp = make_inputs(wl, device=dev)
     experts = moe.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
     ws = experts.forward_workspace(wl.T, wl.top_k, inp["logits"].dtype)
     y = torch.empty((wl.T, wl.H), dtype=inp["x"].dtype, device=dev)
+    assert inp["x"].dtype == {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[wl.dtype]
     stream = torch.cuda.current_stream(dev)
 
     def step(events=None):
@@ -374,7 +377,7 @@ def run_native(args, rank, world, local):
             "value": wl.T * world * K / (ms_total * 1e-3),
             "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else wl.dtype,
+            "vs_baseline": None, "dtype": wl.dtype,
             "data": "synthetic (seeded randn, BF16 weights ~N(0,1/fan_in)); no dataset, random-init weights",
             "config": workload_config(wl),
             "gemm_tflops": tflops,

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from gpu_helpers import DT, assert_y_close, oracle_forward_sample, oracle_route, stored, u32
-from top_routing_grouped_fp32_gb300.inputs import WORKLOADS, make_inputs, small_workload
+from top_routing_grouped_fp32_gb300.inputs import WORKLOADS, make_inputs, small_workload, with_dtype
 
 pytestmark = pytest.mark.gpu
 
@@ -82,9 +82,10 @@ def _sample_tokens(wl, inp, n=24, seed=0):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("name", ["mixtral_bf16", "finegrained_bf16", "skewed_bf16", "decode_bf16"])
-def test_forward_full_workloads(cuda_lib, name):
-    wl = WORKLOADS[name]
+def test_forward_full_workloads(cuda_lib, name, dtype):
+    wl = with_dtype(WORKLOADS[name], dtype)
     inp = make_inputs(wl, device="cuda")
     experts, ws, y = _forward(cuda_lib, wl, inp)
     _check_routing_and_dispatch(experts, ws, wl, inp["logits"])

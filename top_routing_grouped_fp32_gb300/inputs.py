@@ -159,6 +159,13 @@ def make_inputs(w: Workload, device="cuda", weights: bool = True, logits_dtype: 
     return out
 
 
+def with_dtype(w: Workload, dtype: str) -> Workload:
+    """The same workload stored in another dtype (same seed and draws)."""
+    if dtype == w.dtype:
+        return w
+    return dataclasses.replace(w, name=f"{w.name.rsplit('_', 1)[0]}_{dtype}", dtype=dtype)
+
+
 def small_workload(T, E, top_k, H, I, dtype="bf16", renormalize=True, seed=0, **kw) -> Workload:
     """An ad-hoc workload for parity cases (several tiles plus ragged tails)."""
     return Workload(f"T{T}_E{E}_k{top_k}_H{H}_I{I}_{dtype}", T=T, E=E, top_k=top_k, H=H, I=I,
