@@ -8,13 +8,18 @@ from .oracle import (  # noqa: F401
     DTYPE_CODES,
     build,
     combine,
+    combine_backward,
     decode,
     dispatch,
+    dispatch_backward,
     experts,
+    experts_backward,
     forward_tokens,
     num_threads,
     round_to_dtype,
     route,
     route_sigmoid_grouped,
+    router_backward,
+    selected_router_weights,
     set_threads,
 )

@@ -30,6 +30,9 @@
  *   [SILU] MindSpeed-Ops PR 163 diffs, rms_norm_gated notes: silu(x) is
  *          x * sigmoid(x).
  *   [UG10] ruDNN Benutzerhandbuch, section 10: sigmoid group-limited routing.
+ *   [UG12] same page, section 12 "MoE-Training erster Ordnung": the backward
+ *          chain (combine, experts, dispatch, router).
+ *   [EXPB] src/moe/experts.rs, ExpertTrainingCache::backward_with_strategy.
  *
  * Readings where the pages leave a step open (the same list is kept in the
  * design notes):
@@ -444,6 +447,197 @@ void oracle_forward_tokens(const void* x, const void* logits, int ldt, int xdt,
             }
         }
         free(row); free(xt); free(a); free(o); free(wc);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* first-order training backward  [UG12], [EXPB]                            */
+/* ------------------------------------------------------------------------ */
+/* ruDNN Benutzerhandbuch, section 12 "MoE-Training erster Ordnung", and the
+ * ExpertTrainingCache::backward of src/moe/experts.rs:
+ *   1. combine backward: dexpert[r] = w[t,j] * dy[t] for the row r holding
+ *      slot (t,j); dweights[t,j] = <expert_out[r], dy[t]> (FP32 on the pages);
+ *   2. expert backward: for g = x W_gate^T, u = x W_up^T, a = silu(g) u,
+ *      o = a W_down^T and upstream do:
+ *        da = do W_down,  ddown = sum_r do_r^T a_r,
+ *        dg = da u silu'(g),  du = da silu(g),
+ *        dgate = sum_r dg_r^T x_r,  dup = sum_r du_r^T x_r,
+ *        dinput = dg W_gate + du W_up     (weight gradients FP32 on the pages);
+ *   3. dispatch backward: dx[t] = sum_j dinput[r(t,j)], no routing weights;
+ *   4. router backward: gradient of the selected router weights (fixed
+ *      selection) with respect to the logits; repeated indices gather;
+ *      an index outside [0,E) makes the whole row NaN.
+ * Pinned by central finite differences of the forward functions above. */
+
+static double silu_grad(double z) {  /* d/dz z*sigmoid(z) */
+    const double s = 1.0 / (1.0 + exp(-z));
+    return s * (1.0 + z * (1.0 - s));
+}
+
+void oracle_combine_backward(const double* expert_out, const uint32_t* perm, const double* w,
+                             const double* dy, int64_t T, int k, int64_t H,
+                             double* dexpert, double* dweights) {
+    int64_t n = T * (int64_t)k;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r) {
+        const uint32_t s = perm[r];
+        if (s == 0xFFFFFFFFu) continue;
+        const int64_t t = s / (uint32_t)k;
+        double dot = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
+            dexpert[r * H + h] = w[s] * dy[t * H + h];
+            dot += expert_out[r * H + h] * dy[t * H + h];
+        }
+        dweights[s] = dot;
+    }
+}
+
+void oracle_experts_backward(const double* x_disp, const uint32_t* offsets, int64_t E,
+                             const void* gate, const void* up, const void* down, int wdt,
+                             int64_t H, int64_t I, const double* dout,
+                             double* dinput, double* dgate, double* dup, double* ddown) {
+    const int64_t nrows = offsets[E];
+    /* per-row quantities */
+    double* g = (double*)malloc((size_t)(nrows > 0 ? nrows : 1) * I * sizeof(double));
+    double* u = (double*)malloc((size_t)(nrows > 0 ? nrows : 1) * I * sizeof(double));
+    double* da = (double*)malloc((size_t)(nrows > 0 ? nrows : 1) * I * sizeof(double));
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t e = 0;
+        while (!(offsets[e] <= (uint64_t)r && (uint64_t)r < offsets[e + 1])) ++e;
+        for (int64_t i = 0; i < I; ++i) {
+            double gg = 0.0, uu = 0.0, dd = 0.0;
+            for (int64_t h = 0; h < H; ++h) {
+                gg += load_elem(gate, wdt, (e * I + i) * H + h) * x_disp[r * H + h];
+                uu += load_elem(up, wdt, (e * I + i) * H + h) * x_disp[r * H + h];
+                dd += dout[r * H + h] * load_elem(down, wdt, (e * H + h) * I + i);
+            }
+            g[r * I + i] = gg;
+            u[r * I + i] = uu;
+            da[r * I + i] = dd;
+        }
+        for (int64_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int64_t i = 0; i < I; ++i) {
+                const double gg = g[r * I + i], uu = u[r * I + i], d = da[r * I + i];
+                const double dg = d * uu * silu_grad(gg);
+                const double du = d * silu(gg);
+                acc += dg * load_elem(gate, wdt, (e * I + i) * H + h) +
+                       du * load_elem(up, wdt, (e * I + i) * H + h);
+            }
+            dinput[r * H + h] = acc;
+        }
+    }
+    /* weight gradients: sums over each expert's rows */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t e = 0; e < E; ++e) {
+        for (int64_t i = 0; i < I; ++i) {
+            for (int64_t h = 0; h < H; ++h) {
+                double sg = 0.0, su = 0.0, sd = 0.0;
+                for (int64_t r = offsets[e]; r < (int64_t)offsets[e + 1]; ++r) {
+                    const double gg = g[r * I + i], uu = u[r * I + i], d = da[r * I + i];
+                    sg += d * uu * silu_grad(gg) * x_disp[r * H + h];
+                    su += d * silu(gg) * x_disp[r * H + h];
+                    sd += dout[r * H + h] * silu(gg) * uu;
+                }
+                dgate[(e * I + i) * H + h] = sg;
+                dup[(e * I + i) * H + h] = su;
+                ddown[(e * H + h) * I + i] = sd;
+            }
+        }
+    }
+    free(g); free(u); free(da);
+}
+
+void oracle_dispatch_backward(const double* dinput, const uint32_t* perm, int64_t T, int k,
+                              int64_t H, double* dx) {
+    int64_t n = T * (int64_t)k;
+    for (int64_t i = 0; i < T * H; ++i) dx[i] = 0.0;
+    for (int64_t r = 0; r < n; ++r) { /* ascending r per token: any fixed order, exact sums */
+        if (perm[r] == 0xFFFFFFFFu) continue;
+        const int64_t t = perm[r] / (uint32_t)k;
+        for (int64_t h = 0; h < H; ++h) dx[t * H + h] += dinput[r * H + h];
+    }
+}
+
+/* Selected router weights for a fixed selection idx (section 12
+ * selected_router_weights): scoring 0 = softmax over all E, 1 = sigmoid;
+ * optional renormalisation over the selected weights; times scale. */
+void oracle_selected_router_weights(const double* logits, const int64_t* idx, int64_t T, int64_t E,
+                                    int k, int scoring, int renorm, double scale, double* w) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const double* l = logits + t * E;
+        int bad = 0;
+        for (int j = 0; j < k; ++j) if (idx[t * k + j] < 0 || idx[t * k + j] >= E) bad = 1;
+        if (bad) { for (int j = 0; j < k; ++j) w[t * k + j] = NAN; continue; }
+        double m = -INFINITY, s = 0.0;
+        if (scoring == 0) {
+            for (int64_t e = 0; e < E; ++e) if (l[e] > m) m = l[e];
+            for (int64_t e = 0; e < E; ++e) s += exp(l[e] - m);
+        }
+        double tot = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const double x = l[idx[t * k + j]];
+            w[t * k + j] = scoring == 0 ? exp(x - m) / s : 1.0 / (1.0 + exp(-x));
+            tot += w[t * k + j];
+        }
+        for (int j = 0; j < k; ++j) w[t * k + j] = (renorm ? w[t * k + j] / tot : w[t * k + j]) * scale;
+    }
+}
+
+/* Gradient of the selected router weights above with respect to the logits,
+ * given dL/dw (dweights).  Chain rule through scale, renormalisation
+ * (w_j = q_j / Q, Q = sum_m q_m) and the scoring:
+ *   softmax: dq_m/dl_e = q_m (delta(e, idx_m) - p_e)
+ *   sigmoid: dq_m/dl_e = q_m (1 - q_m) delta(e, idx_m)                    */
+void oracle_router_backward(const double* logits, const int64_t* idx, const double* dw,
+                            int64_t T, int64_t E, int k, int scoring, int renorm, double scale,
+                            double* dlogits) {
+#pragma omp parallel
+    {
+        double* p = (double*)malloc((size_t)E * sizeof(double));
+        double* q = (double*)malloc((size_t)k * sizeof(double));
+        double* c = (double*)malloc((size_t)k * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < T; ++t) {
+            const double* l = logits + t * E;
+            double* d = dlogits + t * E;
+            int bad = 0;
+            for (int j = 0; j < k; ++j) if (idx[t * k + j] < 0 || idx[t * k + j] >= E) bad = 1;
+            if (bad) { for (int64_t e = 0; e < E; ++e) d[e] = NAN; continue; }
+            if (scoring == 0) {
+                double m = -INFINITY, s = 0.0;
+                for (int64_t e = 0; e < E; ++e) if (l[e] > m) m = l[e];
+                for (int64_t e = 0; e < E; ++e) s += exp(l[e] - m);
+                for (int64_t e = 0; e < E; ++e) p[e] = exp(l[e] - m) / s;
+            }
+            double Q = 0.0;
+            for (int j = 0; j < k; ++j) {
+                const double x = l[idx[t * k + j]];
+                q[j] = scoring == 0 ? p[idx[t * k + j]] : 1.0 / (1.0 + exp(-x));
+                Q += q[j];
+            }
+            /* c_m = dL/dq_m */
+            double gq = 0.0;
+            for (int j = 0; j < k; ++j) gq += dw[t * k + j] * q[j];
+            for (int m = 0; m < k; ++m)
+                c[m] = renorm ? scale * (dw[t * k + m] / Q - gq / (Q * Q)) : scale * dw[t * k + m];
+            for (int64_t e = 0; e < E; ++e) d[e] = 0.0;
+            double cq = 0.0;
+            for (int m = 0; m < k; ++m) {
+                const int64_t e = idx[t * k + m];
+                if (scoring == 0) {
+                    d[e] += c[m] * q[m];
+                    cq += c[m] * q[m];
+                } else {
+                    d[e] += c[m] * q[m] * (1.0 - q[m]);
+                }
+            }
+            if (scoring == 0)
+                for (int64_t e = 0; e < E; ++e) d[e] -= p[e] * cq;
+        }
+        free(p); free(q); free(c);
     }
 }
 

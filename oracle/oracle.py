@@ -57,6 +57,11 @@ def _load():
         lib.oracle_forward_tokens.argtypes = [P, P, I32, I32, I64, I64, I32, I32, I64, I64,
                                               P, P, P, P, P, I64, P, P, P]
         lib.oracle_decode.argtypes = [P, I32, I64, P]
+        lib.oracle_combine_backward.argtypes = [P, P, P, P, I64, I32, I64, P, P]
+        lib.oracle_experts_backward.argtypes = [P, P, I64, P, P, P, I32, I64, I64, P, P, P, P, P]
+        lib.oracle_dispatch_backward.argtypes = [P, P, I64, I32, I64, P]
+        lib.oracle_selected_router_weights.argtypes = [P, P, I64, I64, I32, I32, I32, ctypes.c_double, P]
+        lib.oracle_router_backward.argtypes = [P, P, P, I64, I64, I32, I32, I32, ctypes.c_double, P]
         lib.oracle_round_to_dtype.argtypes = [ctypes.c_double, I32]
         lib.oracle_round_to_dtype.restype = ctypes.c_double
         lib.oracle_num_threads.restype = I32
@@ -194,3 +199,74 @@ def forward_tokens(x: np.ndarray, logits: np.ndarray, gate: np.ndarray, up: np.n
                                   _ptr(slot) if slot is not None else None, _ptr(toks), n,
                                   _ptr(idx), _ptr(w), _ptr(y))
     return idx, w, y
+
+
+# --------------------------------------------------------------------------
+# first-order training backward (user guide section 12)
+# --------------------------------------------------------------------------
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def combine_backward(expert_out, perm, w, dy):
+    """(dexpert [N,H], dweights [T,k]) for y = combine(expert_out, perm, w)."""
+    eo, w, dy = _f64(expert_out), _f64(w), _f64(dy)
+    T, k = w.shape
+    H = dy.shape[1]
+    dex = np.zeros_like(eo)
+    dw = np.full((T, k), np.nan)
+    _load().oracle_combine_backward(_ptr(eo), _ptr(np.ascontiguousarray(perm, dtype=np.uint32)),
+                                    _ptr(w), _ptr(dy), T, k, H, _ptr(dex), _ptr(dw))
+    return dex, dw
+
+
+def experts_backward(x_disp, offsets, gate, up, down, dtype, dout):
+    """(dinput [N,H], dgate [E,I,H], dup [E,I,H], ddown [E,H,I]) in float64."""
+    xd, do = _f64(x_disp), _f64(dout)
+    g, u, d = (_stored(a, dtype) for a in (gate, up, down))
+    E, I, H = g.shape
+    offsets = np.ascontiguousarray(offsets, dtype=np.uint32)
+    dinput = np.zeros_like(xd)
+    dg = np.zeros((E, I, H))
+    du = np.zeros((E, I, H))
+    dd = np.zeros((E, H, I))
+    _load().oracle_experts_backward(_ptr(xd), _ptr(offsets), E, _ptr(g), _ptr(u), _ptr(d),
+                                    DTYPE_CODES[dtype], H, I, _ptr(do), _ptr(dinput), _ptr(dg),
+                                    _ptr(du), _ptr(dd))
+    return dinput, dg, du, dd
+
+
+def dispatch_backward(dinput, perm, T, k):
+    """dx [T,H]: every dispatched row summed back into its token."""
+    di = _f64(dinput)
+    H = di.shape[1]
+    dx = np.empty((T, H))
+    _load().oracle_dispatch_backward(_ptr(di), _ptr(np.ascontiguousarray(perm, dtype=np.uint32)),
+                                     T, k, H, _ptr(dx))
+    return dx
+
+
+def selected_router_weights(logits, idx, scoring: str, renormalize: bool, scale: float = 1.0):
+    """Router weights of a fixed selection (scoring 'softmax' or 'sigmoid'), float64."""
+    l = _f64(logits)
+    ix = np.ascontiguousarray(idx, dtype=np.int64)
+    T, E = l.shape
+    k = ix.shape[1]
+    w = np.empty((T, k))
+    _load().oracle_selected_router_weights(_ptr(l), _ptr(ix), T, E, k, 0 if scoring == "softmax" else 1,
+                                           int(bool(renormalize)), float(scale), _ptr(w))
+    return w
+
+
+def router_backward(logits, idx, dweights, scoring: str, renormalize: bool, scale: float = 1.0):
+    """dL/dlogits [T,E] for the selected router weights, given dL/dweights."""
+    l = _f64(logits)
+    ix = np.ascontiguousarray(idx, dtype=np.int64)
+    T, E = l.shape
+    k = ix.shape[1]
+    dl = np.empty((T, E))
+    _load().oracle_router_backward(_ptr(l), _ptr(ix), _ptr(_f64(dweights)), T, E, k,
+                                   0 if scoring == "softmax" else 1, int(bool(renormalize)),
+                                   float(scale), _ptr(dl))
+    return dl

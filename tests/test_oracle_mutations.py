@@ -23,13 +23,19 @@ MUTATIONS = {
     "plus_inf_not_poison": ("if (l[e] == INFINITY) has_pinf = 1;", ";"),
     "renorm_dropped": ("for (int j = 0; j < k; ++j) w_pre[j] = w_pre[j] / tot;", ";"),
     "combine_unweighted": ("w_cast[t * k + j] * expert_out[r * H + c]", "expert_out[r * H + c]"),
-    "softmax_without_max_shift": ("s += exp(l[e] - m);", "s += exp(l[e]);"),
+    "softmax_without_max_shift": ("    double s = 0.0;\n    for (int64_t e = 0; e < E; ++e) s += exp(l[e] - m);",
+                                  "    double s = 0.0;\n    for (int64_t e = 0; e < E; ++e) s += exp(l[e]);"),
     "sigmoid_bias_in_weights": ("sig[e] = 1.0 / (1.0 + exp(-l));",
                                 "sig[e] = 1.0 / (1.0 + exp(-l)) + (bias ? bias[e] : 0.0);"),
     "sigmoid_top_two_ignored": ("gscore[g] = group_top_two ? best + second : best;",
                                 "gscore[g] = best;"),
     "sigmoid_group_tie_to_higher": ("if (!gsel[g] && (bg < 0 || beats_f(gscore[g], g, gscore[bg], bg))) bg = g;",
                                     "if (!gsel[g] && (bg < 0 || gscore[g] >= gscore[bg])) bg = g;"),
+    "silu_grad_wrong": ("return s * (1.0 + z * (1.0 - s));", "return s * (1.0 + z * s);"),
+    "dgate_missing_up_factor": ("const double dg = d * uu * silu_grad(gg);", "const double dg = d * silu_grad(gg);"),
+    "router_renorm_sign": ("c[m] = renorm ? scale * (dw[t * k + m] / Q - gq / (Q * Q)) : scale * dw[t * k + m];",
+                           "c[m] = renorm ? scale * (dw[t * k + m] / Q + gq / (Q * Q)) : scale * dw[t * k + m];"),
+    "combine_backward_unweighted": ("dexpert[r * H + h] = w[s] * dy[t * H + h];", "dexpert[r * H + h] = dy[t * H + h];"),
 }
 
 
@@ -45,7 +51,8 @@ def test_pins_catch_planted_mistake(tmp_path, name):
                     ignore=shutil.ignore_patterns("__pycache__"))
     (root / "oracle" / "moe_oracle.c").write_text(src.replace(old, new))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider",
-                        "tests/test_oracle_pins.py", "tests/test_oracle_sigmoid_pins.py"],
+                        "tests/test_oracle_pins.py", "tests/test_oracle_sigmoid_pins.py",
+                        "tests/test_oracle_backward_pins.py"],
                        cwd=root, capture_output=True, text=True,
                        timeout=600)
     tail = r.stdout.strip().splitlines()[-1] if r.stdout.strip() else r.stderr[-500:]
