@@ -289,6 +289,61 @@ moe_status moe_forward_layout(moe_experts_t experts, int64_t T, int32_t top_k,
  * the synchronisation itself fails. */
 moe_status moe_get_device_status(const void* workspace, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * First-order training backward.  ruDNN Benutzerhandbuch, section 12
+ * "MoE-Training erster Ordnung", and ExpertTrainingCache::backward in
+ * src/moe/experts.rs.  All calls are deterministic (fixed summation orders).
+ * ---------------------------------------------------------------------- */
+
+/* Combine backward: for the row r holding slot s = t*top_k + j (perm[r] = s),
+ *   dexpert[r,:] = weights[s] * dy[t,:]            ([T*k, H], in `dtype`)
+ *   dweights[s]  = sum_h expert_out[r,h] * dy[t,h] ([T,k], FP32)
+ * Rows holding no slot get dexpert = 0; slots held by no row get NaN. */
+moe_status moe_combine_backward(const void* expert_out, moe_dtype dtype, const uint32_t* perm,
+                                const void* weights, moe_dtype weights_dtype, const void* dy,
+                                int64_t T, int32_t top_k, int64_t H, void* dexpert,
+                                float* dweights, cudaStream_t stream);
+
+/* Dispatch backward: dx[t,:] = sum_j dinput[r(t,j),:] (ascending j, FP32
+ * accumulation, rounded once to `dtype`), without routing weights.  A slot no
+ * row holds makes dx[t,:] NaN.  workspace: moe_combine_workspace_size(T, k). */
+moe_status moe_dispatch_backward(const void* dinput, moe_dtype dtype, const uint32_t* perm,
+                                 int64_t T, int32_t top_k, int64_t H, void* dx, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
+
+/* Expert backward for dispatched rows x_disp [N,H] (as for
+ * moe_experts_forward) and the gradient of the expert outputs dout [N,H]:
+ *   g = x W_gate^T, u = x W_up^T (recomputed), a = silu(g) u,
+ *   da = dout W_down, dg = da u silu'(g), du = da silu(g),
+ *   dinput = dg W_gate + du W_up        ([N,H], weight dtype)
+ *   ddown = sum_r dout_r^T a_r, dgate = sum_r dg_r^T x_r, dup = sum_r du_r^T x_r
+ * (FP32 [E,H,I], [E,I,H], [E,I,H]; experts without rows get zeros).
+ * FP32 accumulation throughout.  workspace:
+ * moe_experts_backward_workspace_size(experts, N) bytes. */
+size_t moe_experts_backward_workspace_size(moe_experts_t experts, int64_t N);
+moe_status moe_experts_backward(moe_experts_t experts, const void* x_disp, int64_t N,
+                                const uint32_t* offsets, const void* dout, void* dinput,
+                                float* dgate, float* dup, float* ddown, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/* Router weights of a fixed selection idx [T,k] (section 12
+ * selected_router_weights), FP32 [T,k]: scoring 0 = softmax over all E,
+ * 1 = sigmoid of the selected logits; divided by their sum when renormalize
+ * != 0; times scale (finite, > 0).  Repeated indices gather; an index >= E
+ * makes the row NaN.  1 <= top_k <= min(E, 64). */
+moe_status moe_router_weights(const void* logits, moe_dtype logits_dtype, const uint32_t* idx,
+                              int64_t T, int64_t E, int32_t top_k, int scoring, int renormalize,
+                              float scale, float* weights, cudaStream_t stream);
+
+/* Gradient of those weights with respect to the logits (section 12
+ * selected_router_backward): dlogits [T,E] in the logits dtype from FP32
+ * dweights [T,k]; the selection itself is not differentiated.  An index >= E
+ * makes the row NaN. */
+moe_status moe_router_backward(const void* logits, moe_dtype logits_dtype, const uint32_t* idx,
+                               const float* dweights, int64_t T, int64_t E, int32_t top_k,
+                               int scoring, int renormalize, float scale, void* dlogits,
+                               cudaStream_t stream);
+
 /* Diagnostics (no counterpart on the pages): exercises the failure path of
  * the bounded waits inside this library's kernels.  Enqueues one small kernel
  * that waits on a barrier nothing completes; after limit_ms (1..2000) the

@@ -1,0 +1,107 @@
+"""First-order training backward (user guide section 12) against the oracle.
+
+Floating outputs follow the forward's bar (max |err| <= 1e-4 * max |ref| for
+FP32 outputs or FP32 weights, 2e-2 for BF16/FP16 outputs); the oracle's
+backward is itself pinned by finite differences (test_oracle_backward_pins)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import DT, assert_y_close, stored, u32, values
+from top_routing_grouped_fp32_gb300.inputs import TORCH_DTYPES, make_inputs, small_workload
+
+pytestmark = pytest.mark.gpu
+
+
+def _close(got, ref, tol, what):
+    g = values(got) if isinstance(got, torch.Tensor) else got
+    assert np.array_equal(np.isnan(g), np.isnan(ref)), f"{what}: NaN positions differ"
+    ok = ~np.isnan(ref)
+    scale = max(np.abs(ref[ok]).max() if ok.any() else 0.0, 1e-30)
+    err = np.abs(g[ok] - ref[ok]).max() if ok.any() else 0.0
+    assert err <= tol * scale, f"{what}: max err {err:.3e} > {tol} * {scale:.3e}"
+
+
+@pytest.mark.parametrize("T,E,k,H,I,dtype", [
+    (300, 8, 2, 256, 384, "bf16"),
+    (257, 6, 3, 72, 40, "f32"),
+    (200, 16, 4, 128, 96, "f16"),
+    (64, 1, 1, 64, 64, "bf16"),
+])
+def test_expert_backward(cuda_lib, T, E, k, H, I, dtype):
+    wl = small_workload(T, E, k, H, I, dtype=dtype, seed=T)
+    inp = make_inputs(wl, device="cuda")
+    experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    idx, _ = cuda_lib.moe_route(inp["logits"], k, True)
+    d = cuda_lib.moe_dispatch(idx, E, x=inp["x"])
+    g = torch.Generator(device="cuda").manual_seed(5)
+    dout = torch.randn((T * k, H), generator=g, device="cuda").to(TORCH_DTYPES[dtype])
+    dinput, dgate, dup, ddown = experts.backward(d.x_disp, d.offsets, dout)
+    torch.cuda.synchronize()
+    ref = oracle.experts_backward(values(d.x_disp), u32(d.offsets), stored(inp["gate"]), stored(inp["up"]),
+                                  stored(inp["down"]), dtype, values(dout))
+    assert_y_close(dinput, ref[0], dtype, "dinput")
+    for name, got, r in (("dgate", dgate, ref[1]), ("dup", dup, ref[2]), ("ddown", ddown, ref[3])):
+        _close(got, r, 1e-4, name)
+
+
+def test_expert_backward_empty_experts_get_zero(cuda_lib):
+    wl = small_workload(100, 8, 1, 64, 64, dtype="bf16", seed=3, skew=6.0)
+    inp = make_inputs(wl, device="cuda")
+    experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    idx, _ = cuda_lib.moe_route(inp["logits"], 1, True)
+    d = cuda_lib.moe_dispatch(idx, wl.E, x=inp["x"])
+    dout = torch.randn((100, 64), device="cuda").to(torch.bfloat16)
+    _, dgate, dup, ddown = experts.backward(d.x_disp, d.offsets, dout)
+    torch.cuda.synchronize()
+    cnt = np.diff(u32(d.offsets).astype(np.int64))
+    assert (cnt == 0).any()
+    for e in np.where(cnt == 0)[0]:
+        assert torch.all(dgate[e] == 0) and torch.all(dup[e] == 0) and torch.all(ddown[e] == 0)
+
+
+@pytest.mark.parametrize("dtype,wdtype", [("bf16", "bf16"), ("f32", "f32"), ("f16", "bf16")])
+def test_combine_and_dispatch_backward(cuda_lib, dtype, wdtype):
+    T, E, k, H = 333, 12, 3, 200
+    g = torch.Generator(device="cuda").manual_seed(7)
+    logits = torch.randn((T, E), generator=g, device="cuda").to(TORCH_DTYPES[wdtype])
+    idx, w = cuda_lib.moe_route(logits, k, True)
+    d = cuda_lib.moe_dispatch(idx, E)
+    eo = torch.randn((T * k, H), generator=g, device="cuda").to(TORCH_DTYPES[dtype])
+    dy = torch.randn((T, H), generator=g, device="cuda").to(TORCH_DTYPES[dtype])
+    dexpert, dweights = cuda_lib.moe_combine_backward(eo, d.perm, w, dy, k)
+    dx = cuda_lib.moe_dispatch_backward(eo, d.perm, T, k)
+    torch.cuda.synchronize()
+    r_dex, r_dw = oracle.combine_backward(values(eo), u32(d.perm), values(w), values(dy))
+    assert_y_close(dexpert, r_dex, dtype, "dexpert")
+    _close(dweights, r_dw, 1e-5, "dweights")
+    assert_y_close(dx, oracle.dispatch_backward(values(eo), u32(d.perm), T, k), dtype, "dx")
+
+
+@pytest.mark.parametrize("scoring", ["softmax", "sigmoid"])
+@pytest.mark.parametrize("renorm,scale", [(True, 1.0), (False, 2.5)])
+@pytest.mark.parametrize("dtype,E,k", [("f32", 64, 6), ("bf16", 256, 8), ("f16", 37, 5), ("f32", 1024, 64)])
+def test_router_weights_and_backward(cuda_lib, scoring, renorm, scale, dtype, E, k):
+    T = 300
+    g = torch.Generator(device="cuda").manual_seed(E + k)
+    logits = torch.randn((T, E), generator=g, device="cuda").to(TORCH_DTYPES[dtype])
+    idx = torch.stack([torch.randperm(E, generator=g, device="cuda")[:k] for _ in range(T)]).to(torch.int32)
+    idx[3, 1] = idx[3, 0]            # repeated index: gather semantics
+    idx[7, 0] = E + 3                # invalid index: NaN row
+    dw = torch.randn((T, k), generator=g, device="cuda")
+    w = cuda_lib.moe_router_weights(logits, idx, scoring, renorm, scale)
+    dl = cuda_lib.moe_router_backward(logits, idx, dw, scoring, renorm, scale)
+    torch.cuda.synchronize()
+    ix = u32(idx).astype(np.int64)
+    ix[ix >= E] = E + 3
+    lg = values(logits)
+    r_w = oracle.selected_router_weights(lg, ix, scoring, renorm, scale)
+    r_dl = oracle.router_backward(lg, ix, values(dw), scoring, renorm, scale)
+    got_w = values(w)
+    assert np.array_equal(np.isnan(got_w), np.isnan(r_w))
+    ok = ~np.isnan(r_w)
+    np.testing.assert_allclose(got_w[ok], r_w[ok], rtol=1e-5, atol=1e-7)
+    tol = 1e-4 if dtype == "f32" else 2e-2
+    _close(dl, r_dl, tol, "dlogits")
+    assert torch.isnan(dl[7]).all() and torch.isnan(w[7]).all()

@@ -29,7 +29,8 @@ _TORCH_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 _CODE_TORCH = {v: k for k, v in _TORCH_CODES.items()}
 
 __all__ = ["load", "moe_route", "moe_route_sigmoid_grouped", "moe_dispatch", "moe_combine",
-           "SwiGluExperts", "Dispatched",
+           "SwiGluExperts", "Dispatched", "moe_combine_backward", "moe_dispatch_backward",
+           "moe_router_weights", "moe_router_backward",
            "moe_get_device_status", "MoeError", "library_path"]
 
 
@@ -156,6 +157,64 @@ def moe_combine(expert_out: torch.Tensor, perm: torch.Tensor, weights: torch.Ten
     return y
 
 
+# --------------------------------------------------------------------------
+# first-order training backward (user guide, section 12)
+# --------------------------------------------------------------------------
+
+def moe_combine_backward(expert_out: torch.Tensor, perm: torch.Tensor, weights: torch.Tensor,
+                         dy: torch.Tensor, top_k: int, stream=None):
+    """(dexpert [T*k,H] in expert_out's dtype, dweights [T,k] float32)."""
+    lib = load()
+    T, H = dy.shape
+    dexpert = torch.empty_like(expert_out)
+    dweights = torch.empty((T, top_k), dtype=torch.float32, device=dy.device)
+    _lib.check(lib.moe_combine_backward(_ptr(expert_out), _code(expert_out), _ptr(perm), _ptr(weights),
+                                        _code(weights), _ptr(dy), T, top_k, H, _ptr(dexpert),
+                                        _ptr(dweights), _stream(stream)))
+    return dexpert, dweights
+
+
+def moe_dispatch_backward(dinput: torch.Tensor, perm: torch.Tensor, T: int, top_k: int,
+                          stream=None) -> torch.Tensor:
+    """dx [T,H]: every dispatched row summed back into its token."""
+    lib = load()
+    H = dinput.shape[1]
+    dx = torch.empty((T, H), dtype=dinput.dtype, device=dinput.device)
+    ws = _workspace(lib.moe_combine_workspace_size(T, top_k), dinput.device)
+    _lib.check(lib.moe_dispatch_backward(_ptr(dinput), _code(dinput), _ptr(perm), T, top_k, H, _ptr(dx),
+                                         _ptr(ws), ws.numel(), _stream(stream)))
+    return dx
+
+
+_SCORING = {"softmax": 0, "sigmoid": 1}
+
+
+def moe_router_weights(logits: torch.Tensor, idx: torch.Tensor, scoring: str = "softmax",
+                       renormalize: bool = True, scale: float = 1.0, stream=None) -> torch.Tensor:
+    """FP32 router weights [T,k] of a fixed selection idx."""
+    lib = load()
+    T, E = logits.shape
+    k = idx.shape[1]
+    w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _lib.check(lib.moe_router_weights(_ptr(logits), _code(logits), _ptr(idx), T, E, k, _SCORING[scoring],
+                                      int(bool(renormalize)), float(scale), _ptr(w), _stream(stream)))
+    return w
+
+
+def moe_router_backward(logits: torch.Tensor, idx: torch.Tensor, dweights: torch.Tensor,
+                        scoring: str = "softmax", renormalize: bool = True, scale: float = 1.0,
+                        stream=None) -> torch.Tensor:
+    """dL/dlogits [T,E] (logits dtype) from FP32 dL/dweights [T,k]."""
+    lib = load()
+    T, E = logits.shape
+    k = idx.shape[1]
+    dl = torch.empty_like(logits)
+    _lib.check(lib.moe_router_backward(_ptr(logits), _code(logits), _ptr(idx), _ptr(dweights), T, E, k,
+                                       _SCORING[scoring], int(bool(renormalize)), float(scale), _ptr(dl),
+                                       _stream(stream)))
+    return dl
+
+
 def moe_get_device_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronises the stream and returns the workspace's device status code."""
     lib = load()
@@ -239,6 +298,23 @@ class SwiGluExperts:
             arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
             _lib.check(self._lib.moe_forward_timed(*args, arr, len(events)))
         return y
+
+    def backward(self, x_disp: torch.Tensor, offsets: torch.Tensor, dout: torch.Tensor,
+                 workspace=None, stream=None):
+        """Expert backward (ExpertTrainingCache::backward): returns (dinput [N,H]
+        in the weight dtype, dgate [E,I,H], dup [E,I,H], ddown [E,H,I] in FP32)."""
+        N = x_disp.shape[0]
+        dev = x_disp.device
+        dinput = torch.empty((N, self.H), dtype=self.dtype, device=dev)
+        dgate = torch.empty((self.E, self.I, self.H), dtype=torch.float32, device=dev)
+        dup = torch.empty_like(dgate)
+        ddown = torch.empty((self.E, self.H, self.I), dtype=torch.float32, device=dev)
+        if workspace is None:
+            workspace = _workspace(self._lib.moe_experts_backward_workspace_size(self.handle, N), dev)
+        _lib.check(self._lib.moe_experts_backward(self.handle, _ptr(x_disp), N, _ptr(offsets), _ptr(dout),
+                                                  _ptr(dinput), _ptr(dgate), _ptr(dup), _ptr(ddown),
+                                                  _ptr(workspace), workspace.numel(), _stream(stream)))
+        return dinput, dgate, dup, ddown
 
     def forward_sigmoid_grouped(self, x: torch.Tensor, logits: torch.Tensor, top_k: int, groups: int,
                                 selected_groups: int, group_top_two: bool, renormalize: bool,

@@ -585,6 +585,136 @@ moe_status moe_forward_host(moe_experts_t x, const void* x_host, const void* log
   return ok();
 }
 
+// ---- first-order training backward (user guide, section 12) -------------
+moe_status moe_combine_backward(const void* expert_out, moe_dtype dt, const uint32_t* perm,
+                                const void* weights, moe_dtype wdt, const void* dy, int64_t T,
+                                int32_t top_k, int64_t H, void* dexpert, float* dweights,
+                                cudaStream_t stream) {
+  if (!valid_dtype(dt) || !valid_dtype(wdt)) return fail(MOE_ERR_DTYPE, "dtype is not F32/F16/BF16");
+  if (T < 0) return fail(MOE_ERR_SHAPE, "T must be >= 0");
+  if (top_k < 1 || top_k > kMaxK) return fail(MOE_ERR_INVALID_ARG, "top_k must be in 1..=64");
+  if (T > kMaxRows / top_k) return fail(MOE_ERR_UNSUPPORTED, "T*top_k exceeds 2^31-1");
+  moe_status st = check_dim(H, "H");
+  if (st != MOE_OK) return st;
+  if (T == 0) return ok();
+  if (!expert_out || !perm || !weights || !dy || !dexpert || !dweights)
+    return fail(MOE_ERR_INVALID_ARG, "expert_out, perm, weights, dy, dexpert and dweights must be non-NULL");
+  MOE_TRY_CUDA(moe::launch_combine_backward(expert_out, dt, perm, weights, wdt, dy, T, top_k, H, dexpert,
+                                            dweights, stream),
+               "combine backward launch");
+  return ok();
+}
+
+moe_status moe_dispatch_backward(const void* dinput, moe_dtype dt, const uint32_t* perm, int64_t T,
+                                 int32_t top_k, int64_t H, void* dx, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream) {
+  if (!valid_dtype(dt)) return fail(MOE_ERR_DTYPE, "dtype is not F32/F16/BF16");
+  if (T < 0) return fail(MOE_ERR_SHAPE, "T must be >= 0");
+  if (top_k < 1 || top_k > kMaxK) return fail(MOE_ERR_INVALID_ARG, "top_k must be in 1..=64");
+  if (T > kMaxRows / top_k) return fail(MOE_ERR_UNSUPPORTED, "T*top_k exceeds 2^31-1");
+  moe_status st = check_dim(H, "H");
+  if (st != MOE_OK) return st;
+  if (T == 0) return ok();
+  if (!dinput || !perm || !dx) return fail(MOE_ERR_INVALID_ARG, "dinput, perm and dx must be non-NULL");
+  if (!aligned16(dinput) || !aligned16(dx))
+    return fail(MOE_ERR_INVALID_ARG, "dinput and dx must be 16-byte aligned");
+  if ((st = check_ws(ws, ws_bytes, moe_combine_workspace_size(T, top_k))) != MOE_OK) return st;
+  uint32_t* slot_row = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + kWsHeader);
+  MOE_TRY_CUDA(moe::launch_invert_perm(perm, T * top_k, slot_row, stream), "perm inversion launch");
+  MOE_TRY_CUDA(moe::launch_combine(dinput, dt, slot_row, nullptr, MOE_F32, T, top_k, H, dx, stream),
+               "dispatch backward launch");
+  return ok();
+}
+
+size_t moe_experts_backward_workspace_size(moe_experts_t x, int64_t N) {
+  if (!x || N < 0) return 0;
+  return kWsHeader + 5 * align_up((size_t)N * x->I * 4, 1024);
+}
+
+moe_status moe_experts_backward(moe_experts_t x, const void* x_disp, int64_t N, const uint32_t* offsets,
+                                const void* dout, void* dinput, float* dgate, float* dup, float* ddown,
+                                void* ws, size_t ws_bytes, cudaStream_t stream) {
+  moe_status st = check_handle(x);
+  if (st != MOE_OK) return st;
+  if (N < 0 || N > kMaxRows) return fail(MOE_ERR_SHAPE, "N=%lld out of range", (long long)N);
+  if (!offsets || !dgate || !dup || !ddown)
+    return fail(MOE_ERR_INVALID_ARG, "offsets, dgate, dup and ddown must be non-NULL");
+  if (N > 0 && (!x_disp || !dout || !dinput))
+    return fail(MOE_ERR_INVALID_ARG, "x_disp, dout and dinput must be non-NULL");
+  if ((st = check_ws(ws, ws_bytes, moe_experts_backward_workspace_size(x, N))) != MOE_OK) return st;
+  const size_t part = align_up((size_t)N * x->I * 4, 1024);
+  char* base = static_cast<char*>(ws) + kWsHeader;
+  moe::ExpertsBwdArgs a{};
+  a.dt = x->dt;
+  a.E = (int)x->E;
+  a.N = N;
+  a.H = x->H;
+  a.I = x->I;
+  a.x_disp = x_disp;
+  a.dout = dout;
+  a.gate = x->gate;
+  a.up = x->up;
+  a.down = x->down;
+  a.offsets = offsets;
+  a.g = reinterpret_cast<float*>(base);
+  a.u = reinterpret_cast<float*>(base + part);
+  a.act = reinterpret_cast<float*>(base + 2 * part);
+  a.dg = reinterpret_cast<float*>(base + 3 * part);
+  a.du = reinterpret_cast<float*>(base + 4 * part);
+  a.dinput = dinput;
+  a.dgate = dgate;
+  a.dup = dup;
+  a.ddown = ddown;
+  if (N == 0) {  // no rows: every weight gradient is zero
+    const size_t wb = (size_t)x->E * x->I * x->H * 4;
+    MOE_TRY_CUDA(cudaMemsetAsync(dgate, 0, wb, stream), "cudaMemsetAsync");
+    MOE_TRY_CUDA(cudaMemsetAsync(dup, 0, wb, stream), "cudaMemsetAsync");
+    MOE_TRY_CUDA(cudaMemsetAsync(ddown, 0, wb, stream), "cudaMemsetAsync");
+    return ok();
+  }
+  MOE_TRY_CUDA(moe::launch_experts_backward(a, stream), "expert backward launch");
+  return ok();
+}
+
+static moe_status check_router_args(int64_t T, int64_t E, int32_t k, int scoring, float scale) {
+  if (T < 0) return fail(MOE_ERR_SHAPE, "T must be >= 0");
+  if (E < 1 || E > kMaxE) return fail(E < 1 ? MOE_ERR_SHAPE : MOE_ERR_UNSUPPORTED, "E must be in 1..=1024");
+  if (k < 1 || k > kMaxK || k > E) return fail(MOE_ERR_INVALID_ARG, "top_k must satisfy 1 <= top_k <= min(E, 64)");
+  if (scoring != 0 && scoring != 1) return fail(MOE_ERR_INVALID_ARG, "scoring must be 0 (softmax) or 1 (sigmoid)");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(MOE_ERR_INVALID_ARG, "scale must be finite and positive");
+  if (T > kMaxRows / k) return fail(MOE_ERR_UNSUPPORTED, "T*top_k exceeds 2^31-1");
+  return MOE_OK;
+}
+
+moe_status moe_router_weights(const void* logits, moe_dtype ldt, const uint32_t* idx, int64_t T,
+                              int64_t E, int32_t top_k, int scoring, int renormalize, float scale,
+                              float* weights, cudaStream_t stream) {
+  if (!valid_dtype(ldt)) return fail(MOE_ERR_DTYPE, "logits dtype is not F32/F16/BF16");
+  moe_status st = check_router_args(T, E, top_k, scoring, scale);
+  if (st != MOE_OK) return st;
+  if (T == 0) return ok();
+  if (!logits || !idx || !weights) return fail(MOE_ERR_INVALID_ARG, "logits, idx and weights must be non-NULL");
+  MOE_TRY_CUDA(moe::launch_router_backward(logits, ldt, T, (int)E, idx, top_k, nullptr, scoring, renormalize,
+                                           scale, nullptr, weights, stream),
+               "router weights launch");
+  return ok();
+}
+
+moe_status moe_router_backward(const void* logits, moe_dtype ldt, const uint32_t* idx,
+                               const float* dweights, int64_t T, int64_t E, int32_t top_k, int scoring,
+                               int renormalize, float scale, void* dlogits, cudaStream_t stream) {
+  if (!valid_dtype(ldt)) return fail(MOE_ERR_DTYPE, "logits dtype is not F32/F16/BF16");
+  moe_status st = check_router_args(T, E, top_k, scoring, scale);
+  if (st != MOE_OK) return st;
+  if (T == 0) return ok();
+  if (!logits || !idx || !dweights || !dlogits)
+    return fail(MOE_ERR_INVALID_ARG, "logits, idx, dweights and dlogits must be non-NULL");
+  MOE_TRY_CUDA(moe::launch_router_backward(logits, ldt, T, (int)E, idx, top_k, dweights, scoring,
+                                           renormalize, scale, dlogits, nullptr, stream),
+               "router backward launch");
+  return ok();
+}
+
 moe_status moe_selftest_bounded_wait(void* ws, uint32_t limit_ms, cudaStream_t stream) {
   if ((ws == nullptr) || !aligned256(ws))
     return fail(MOE_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");

@@ -70,7 +70,7 @@ combine_kernel(const T* __restrict__ src, const uint32_t* __restrict__ slot_row,
     float wj = 1.f;
     if constexpr (WEIGHTED) {
       const uint32_t r = __ldg(slot_row + t * k + j);
-      wj = load_dyn(w, wdt, (size_t)(t * k + j));
+      wj = w ? load_dyn(w, wdt, (size_t)(t * k + j)) : 1.f;  // no weights: dispatch backward
       if (r == kInvalid) {
 #pragma unroll
         for (int i = 0; i < C; ++i) acc[i] = NAN;
@@ -112,6 +112,41 @@ cudaError_t launch_combine_t(const void* src, const uint32_t* slot_row, const vo
   return cudaGetLastError();
 }
 
+// Combine backward (user guide, section 12: combine_backward gives dexpert and
+// FP32 dweights): one warp per dispatched row r holding slot s = t*k+j:
+//   dexpert[r,:] = w[s] * dy[t,:]      dweights[s] = sum_h expert_out[r,h] dy[t,h]
+// The dot product is summed per lane in column order, then by a butterfly
+// (a fixed order).  Rows holding no slot get dexpert = 0; slots no row holds
+// keep the NaN the caller's buffer was filled with.
+template <typename T>
+__global__ void __launch_bounds__(256)
+combine_backward_kernel(const T* __restrict__ eo, const uint32_t* __restrict__ perm,
+                        const void* __restrict__ w, int wdt, const T* __restrict__ dy, int64_t N,
+                        int k, int64_t H, T* __restrict__ dexpert, float* __restrict__ dweights) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= N) return;
+  const uint32_t s = __ldg(perm + r);
+  T* dst = dexpert + r * H;
+  if (s == kInvalid) {
+    for (int64_t c = lane; c < H; c += 32) dst[c] = from_f32<T>(0.f);
+    return;
+  }
+  const int64_t t = s / (uint32_t)k;
+  const float wv = load_dyn(w, wdt, s);
+  const T* src = eo + r * H;
+  const T* g = dy + t * H;
+  float dot = 0.f;
+  for (int64_t c = lane; c < H; c += 32) {
+    const float gv = to_f32<T>(g[c]);
+    dst[c] = from_f32<T>(wv * gv);
+    dot = fmaf(to_f32<T>(src[c]), gv, dot);
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, d);
+  if (lane == 0) dweights[s] = dot;
+}
+
 }  // namespace
 
 cudaError_t launch_invert_perm(const uint32_t* perm, int64_t N, uint32_t* slot_row, cudaStream_t s) {
@@ -138,6 +173,33 @@ cudaError_t launch_slot_sum(const void* slots, moe_dtype dt, int64_t T, int k, i
     case MOE_F16: return launch_combine_t<__half, false>(slots, nullptr, nullptr, dt, T, k, H, y, s);
     default: return launch_combine_t<__nv_bfloat16, false>(slots, nullptr, nullptr, dt, T, k, H, y, s);
   }
+}
+
+cudaError_t launch_combine_backward(const void* expert_out, moe_dtype dt, const uint32_t* perm,
+                                    const void* weights, moe_dtype wdt, const void* dy, int64_t T,
+                                    int k, int64_t H, void* dexpert, float* dweights, cudaStream_t s) {
+  const int64_t N = T * k;
+  cudaError_t err = cudaMemsetAsync(dweights, 0xFF, (size_t)N * sizeof(float), s);  // NaN
+  if (err != cudaSuccess) return err;
+  const unsigned grid = (unsigned)((N + 7) / 8);
+  switch (dt) {
+    case MOE_F32:
+      combine_backward_kernel<float><<<grid, 256, 0, s>>>(
+          static_cast<const float*>(expert_out), perm, weights, (int)wdt,
+          static_cast<const float*>(dy), N, k, H, static_cast<float*>(dexpert), dweights);
+      break;
+    case MOE_F16:
+      combine_backward_kernel<__half><<<grid, 256, 0, s>>>(
+          static_cast<const __half*>(expert_out), perm, weights, (int)wdt,
+          static_cast<const __half*>(dy), N, k, H, static_cast<__half*>(dexpert), dweights);
+      break;
+    default:
+      combine_backward_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(expert_out), perm, weights, (int)wdt,
+          static_cast<const __nv_bfloat16*>(dy), N, k, H, static_cast<__nv_bfloat16*>(dexpert),
+          dweights);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -15,6 +15,11 @@ cudaError_t launch_route(const void* logits, moe_dtype ldt, int64_t T, int E, in
                          uint32_t* idx, void* weights, float* w32, uint32_t* status_reset,
                          cudaStream_t s);
 
+// selected router weights (FP32) and, when dw != nullptr, their logit gradient
+cudaError_t launch_router_backward(const void* logits, moe_dtype ldt, int64_t T, int E,
+                                   const uint32_t* idx, int k, const float* dw, int scoring,
+                                   int renorm, float scale, void* dlogits, float* w_out,
+                                   cudaStream_t s);
 cudaError_t launch_route_sigmoid_grouped(const void* logits, moe_dtype ldt, int64_t T, int E,
                                          const float* bias, int k, int groups, int sel_groups,
                                          int top_two, int renorm, float scale, uint32_t* idx,
@@ -39,6 +44,10 @@ cudaError_t launch_invert_perm(const uint32_t* perm, int64_t N, uint32_t* slot_r
 cudaError_t launch_combine(const void* expert_out, moe_dtype dt, const uint32_t* slot_row,
                            const void* weights, moe_dtype wdt, int64_t T, int k, int64_t H,
                            void* y, cudaStream_t s);
+// dexpert[r] = w[perm[r]] * dy[t], dweights[perm[r]] = <expert_out[r], dy[t]>
+cudaError_t launch_combine_backward(const void* expert_out, moe_dtype dt, const uint32_t* perm,
+                                    const void* weights, moe_dtype wdt, const void* dy, int64_t T,
+                                    int k, int64_t H, void* dexpert, float* dweights, cudaStream_t s);
 // y[t] = sum_j slots[t*k+j] (weights already applied), ascending j
 cudaError_t launch_slot_sum(const void* slots, moe_dtype dt, int64_t T, int k, int64_t H, void* y,
                             cudaStream_t s);
@@ -63,6 +72,29 @@ struct GemmArgs {
   moe_dtype wdt;
   uint32_t* status;
 };
+
+// Backward of the SwiGLU experts (gemm_bwd.cu): FP32 accumulate, any dtype.
+struct ExpertsBwdArgs {
+  moe_dtype dt;
+  int E;
+  int64_t N, H, I;
+  const void* x_disp;   // [N, H]
+  const void* dout;     // [N, H] gradient of the expert outputs
+  const void* gate;     // [E, I, H]
+  const void* up;       // [E, I, H]
+  const void* down;     // [E, H, I]
+  const uint32_t* offsets;
+  float* g;             // [N, I] scratch: recomputed gate product
+  float* u;             // [N, I] scratch: recomputed up product
+  float* act;           // [N, I] scratch: silu(g) * u
+  float* dg;            // [N, I] scratch
+  float* du;            // [N, I] scratch
+  void* dinput;         // [N, H] in dt
+  float* dgate;         // [E, I, H]
+  float* dup;           // [E, I, H]
+  float* ddown;         // [E, H, I]
+};
+cudaError_t launch_experts_backward(const ExpertsBwdArgs& a, cudaStream_t s);
 
 // SIMT FP32-accumulate path (gemm_simt.cu): any dtype and shape
 cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s);

@@ -331,6 +331,88 @@ route_sigmoid_grouped_kernel(const T* __restrict__ logits, int64_t T_rows, int E
   }
 }
 
+// ---------------------------------------------------------------------------
+// Router weights of a fixed selection and their logit gradient (user guide,
+// section 12: selected_router_weights / selected_router_backward).  Scoring 0:
+// q_j = softmax(logits)[idx_j] over all E; scoring 1: q_j = sigmoid(logit
+// idx_j).  w_j = scale * (renorm ? q_j / Q : q_j), Q = sum_m q_m (slot order).
+// Given dw = dL/dw (FP32):  c_m = dL/dq_m = scale * (renorm ? dw_m/Q -
+// (sum_j dw_j q_j)/Q^2 : dw_m), and
+//   softmax: dL/dl_e = sum_{m: idx_m = e} c_m q_m - p_e * sum_m c_m q_m
+//   sigmoid: dL/dl_e = sum_{m: idx_m = e} c_m q_m (1 - q_m)
+// Repeated indices gather (each slot counts); an index >= E makes the row's
+// weights and gradient NaN.  One warp per row, FP32 throughout; the row's
+// logits sit in the warp's shared-memory slice.
+template <typename T>
+__global__ void __launch_bounds__(32 * kRowsPerBlock)
+router_backward_kernel(const T* __restrict__ logits, int64_t T_rows, int E,
+                       const uint32_t* __restrict__ idx, int k, const float* __restrict__ dw,
+                       int scoring, int renorm, float scale, T* __restrict__ dlogits,
+                       float* __restrict__ w_out) {
+  extern __shared__ float rb_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * kRowsPerBlock + warp;
+  float* lrow = rb_smem + warp * (E + 2 * 64);
+  float* q = lrow + E;       // [k]
+  float* cq = q + 64;        // [k]: c_m q_m (softmax) or c_m q_m (1 - q_m)
+  if (t >= T_rows) return;
+  const T* l = logits + t * E;
+  float m = -INFINITY;
+  for (int e = lane; e < E; e += 32) {
+    const float v = to_f32<T>(l[e]);
+    lrow[e] = v;
+    m = fmaxf(m, v);
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+  bool bad = false;
+  for (int j = lane; j < k; j += 32) bad |= __ldg(idx + t * k + j) >= (uint32_t)E;
+  if (__any_sync(0xffffffffu, bad)) {
+    for (int j = lane; j < k; j += 32)
+      if (w_out) w_out[t * k + j] = NAN;
+    if (dw)
+      for (int e = lane; e < E; e += 32) dlogits[t * E + e] = from_f32<T>(NAN);
+    return;
+  }
+  float ssum = 0.f;
+  if (scoring == 0) {
+    for (int e = lane; e < E; e += 32) ssum += expf(lrow[e] - m);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, d);
+  }
+  __syncwarp();
+  for (int j = lane; j < k; j += 32) {
+    const float x = lrow[__ldg(idx + t * k + j)];
+    q[j] = scoring == 0 ? expf(x - m) / ssum : 1.f / (1.f + expf(-x));
+  }
+  __syncwarp();
+  // slot-order sums, computed identically by every lane
+  float Q = 0.f, gq = 0.f;
+  for (int j = 0; j < k; ++j) {
+    Q += q[j];
+    if (dw) gq += __ldg(dw + t * k + j) * q[j];
+  }
+  for (int j = lane; j < k; j += 32) {
+    if (w_out) w_out[t * k + j] = scale * (renorm ? q[j] / Q : q[j]);
+    if (dw) {
+      const float dwj = __ldg(dw + t * k + j);
+      const float c = renorm ? scale * (dwj / Q - gq / (Q * Q)) : scale * dwj;
+      cq[j] = scoring == 0 ? c * q[j] : c * q[j] * (1.f - q[j]);
+    }
+  }
+  if (!dw) return;
+  __syncwarp();
+  float tot = 0.f;
+  for (int j = 0; j < k; ++j) tot += cq[j];
+  for (int e = lane; e < E; e += 32) {
+    float v = 0.f;
+    for (int j = 0; j < k; ++j)
+      if (__ldg(idx + t * k + j) == (uint32_t)e) v += cq[j];
+    if (scoring == 0) v -= expf(lrow[e] - m) / ssum * tot;
+    dlogits[t * E + e] = from_f32<T>(v);
+  }
+}
+
 template <typename T>
 cudaError_t launch_sigmoid_typed(const void* logits, int64_t T_rows, int E, const float* bias,
                                  int k, int groups, int sel_groups, int top_two, int renorm,
@@ -389,6 +471,32 @@ cudaError_t launch_route_sigmoid_grouped(const void* logits, moe_dtype ldt, int6
       return launch_sigmoid_typed<__nv_bfloat16>(logits, T, E, bias, k, groups, sel_groups, top_two,
                                                  renorm, scale, idx, weights, w32, s);
   }
+}
+
+cudaError_t launch_router_backward(const void* logits, moe_dtype ldt, int64_t T, int E,
+                                   const uint32_t* idx, int k, const float* dw, int scoring,
+                                   int renorm, float scale, void* dlogits, float* w_out,
+                                   cudaStream_t s) {
+  dim3 grid((unsigned)((T + kRowsPerBlock - 1) / kRowsPerBlock));
+  dim3 block(32 * kRowsPerBlock);
+  const size_t smem = (size_t)kRowsPerBlock * (E + 128) * sizeof(float);
+  switch (ldt) {
+    case MOE_F32:
+      router_backward_kernel<float><<<grid, block, smem, s>>>(
+          static_cast<const float*>(logits), T, E, idx, k, dw, scoring, renorm, scale,
+          static_cast<float*>(dlogits), w_out);
+      break;
+    case MOE_F16:
+      router_backward_kernel<__half><<<grid, block, smem, s>>>(
+          static_cast<const __half*>(logits), T, E, idx, k, dw, scoring, renorm, scale,
+          static_cast<__half*>(dlogits), w_out);
+      break;
+    default:
+      router_backward_kernel<__nv_bfloat16><<<grid, block, smem, s>>>(
+          static_cast<const __nv_bfloat16*>(logits), T, E, idx, k, dw, scoring, renorm, scale,
+          static_cast<__nv_bfloat16*>(dlogits), w_out);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace moe
