@@ -46,6 +46,10 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=600)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--mode", choices=["forward", "backward"], default="forward",
+                   help="backward: time the first-order training backward chain instead")
+    p.add_argument("--bwd-strategy", choices=["scalar", "auto", "tensor_core"], default="auto",
+                   help="expert backward strategy of --mode backward")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--dtype", choices=["bf16", "f16"], default=None,
                    help="store the workload in this dtype instead of its own")
@@ -409,11 +413,84 @@ def run_native(args, rank, world, local):
     return 0
 
 
+def run_backward(args, rank, world, local):
+    """Times the first-order backward chain (user guide section 12) after a
+    staged forward: combine backward -> expert backward -> dispatch backward
+    -> router backward.  The expert backward's roofline is the tensor pipe
+    (measured bf16 peak) for the tensor-core strategy, else the FP32 FMA pipe:
+    152 SMs x 128 lanes x 2 FLOP x the max SM clock."""
+    import torch
+    import top_routing_grouped_fp32_gb300 as moe
+    from top_routing_grouped_fp32_gb300.inputs import WORKLOADS, make_inputs, with_dtype
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = with_dtype(WORKLOADS[args.workload], args.dtype or WORKLOADS[args.workload].dtype)
+    inp = make_inputs(wl, device=dev)
+    ex = moe.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    idx, w = moe.moe_route(inp["logits"], wl.top_k, wl.renormalize)
+    d = moe.moe_dispatch(idx, wl.E, x=inp["x"])
+    eo = ex.forward_dispatched(d.x_disp, d.offsets)
+    g = torch.Generator(device=dev).manual_seed(99)
+    dy = torch.randn((wl.T, wl.H), generator=g, device=dev).to(inp["x"].dtype)
+    N = wl.T * wl.top_k
+    bws = moe._workspace(ex._lib.moe_experts_backward_workspace_size(ex.handle, N), dev)
+
+    def step(ev):
+        ev[0].record()
+        dex, dwt = moe.moe_combine_backward(eo, d.perm, w, dy, wl.top_k)
+        ev[1].record()
+        dinput, dgate, dup, ddown = ex.backward(d.x_disp, d.offsets, dex, workspace=bws,
+                                                strategy=args.bwd_strategy)
+        ev[2].record()
+        moe.moe_dispatch_backward(dinput, d.perm, wl.T, wl.top_k)
+        ev[3].record()
+        moe.moe_router_backward(inp["logits"], idx, dwt, "softmax", wl.renormalize, 1.0)
+        ev[4].record()
+
+    K = max(1, args.steps)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K + 2)]
+    for _ in range(2):
+        step(evs[-1])
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    names = ["combine_backward", "experts_backward", "dispatch_backward", "router_backward"]
+    st = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+          for j, n in enumerate(names)}
+    total = sum(st.values())
+    flops = 16.0 * N * wl.H * wl.I  # recompute g,u (4) + da (2) + dinput (4) + 3 weight grads (6)
+    ach = flops / (st["experts_backward"] * 1e-3) / 1e12
+    tensor = args.bwd_strategy == "tensor_core" or (args.bwd_strategy == "auto" and wl.dtype != "f32")
+    if tensor:
+        peaks, peaks_src = load_peaks()
+        roof = {"bound": "tensor", "kernel": "experts backward (tcgen05 chain)", "achieved": ach,
+                "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
+                "frac": ach / float(peaks["bf16_tflops"]),
+                "peak_source": f"{peaks_src} bf16_tflops (burst)"}
+    else:
+        peak = 152 * 128 * 2 * 2.07e9 / 1e12
+        roof = {"bound": "alu", "kernel": "experts backward (FP32 FMA)", "achieved": ach,
+                "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                "peak_source": "152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz"}
+    roof["algorithmic_per_launch"] = f"16*N*H*I = {flops:.4e} FLOP"
+    line = {"metric": "MoE first-order backward tokens/s", "value": wl.T / (total * 1e-3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": K, "mode": "backward",
+            "bwd_strategy": "tensor_core" if tensor else "scalar",
+            "ms_per_step": total, "higher_is_better": True, "dtype": wl.dtype, "data": "synthetic",
+            "config": workload_config(wl), "stages_ms": st, "roofline": roof}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.mode == "backward":
+        return run_backward(args, rank, world, local)
     return run_native(args, rank, world, local)
 
 

@@ -319,12 +319,34 @@ moe_status moe_dispatch_backward(const void* dinput, moe_dtype dtype, const uint
  *   ddown = sum_r dout_r^T a_r, dgate = sum_r dg_r^T x_r, dup = sum_r du_r^T x_r
  * (FP32 [E,H,I], [E,I,H], [E,I,H]; experts without rows get zeros).
  * FP32 accumulation throughout.  workspace:
- * moe_experts_backward_workspace_size(experts, N) bytes. */
+ * moe_experts_backward_workspace_size(experts, N) bytes (enough for every
+ * strategy of moe_experts_backward_with_strategy). */
 size_t moe_experts_backward_workspace_size(moe_experts_t experts, int64_t N);
 moe_status moe_experts_backward(moe_experts_t experts, const void* x_disp, int64_t N,
                                 const uint32_t* offsets, const void* dout, void* dinput,
                                 float* dgate, float* dup, float* ddown, void* workspace,
                                 size_t workspace_bytes, cudaStream_t stream);
+
+/* The same backward with an explicit strategy (section 12: the expert backward
+ * takes Scalar, Auto or TensorCore, independently of the forward's strategy;
+ * moe_experts_backward above is Scalar, the pages' default).
+ *   MOE_BWD_SCALAR      FP32 CUDA-core kernels; g, u, a, dg, du kept in FP32.
+ *   MOE_BWD_TENSOR_CORE tcgen05 kernels, F16/BF16 experts only (otherwise
+ *                       MOE_ERR_UNSUPPORTED, nothing enqueued).  As in the
+ *                       pages' training cache, a, dg and du are held in the
+ *                       weight dtype and are the 16-bit operands of dinput and
+ *                       of the weight gradients; g and u stay FP32.  FP32
+ *                       accumulation; weight gradients FP32.
+ *   MOE_BWD_AUTO        TENSOR_CORE where the experts support it, else SCALAR
+ *                       (a capability choice only: errors are returned).
+ * The tensor-core path's waits are bounded; a timeout sets the device status
+ * word to MOE_ERR_DEVICE_TIMEOUT (moe_get_device_status on the workspace). */
+enum { MOE_BWD_SCALAR = 0, MOE_BWD_AUTO = 1, MOE_BWD_TENSOR_CORE = 2 };
+moe_status moe_experts_backward_with_strategy(moe_experts_t experts, const void* x_disp, int64_t N,
+                                              const uint32_t* offsets, const void* dout,
+                                              void* dinput, float* dgate, float* dup, float* ddown,
+                                              int strategy, void* workspace,
+                                              size_t workspace_bytes, cudaStream_t stream);
 
 /* Router weights of a fixed selection idx [T,k] (section 12
  * selected_router_weights), FP32 [T,k]: scoring 0 = softmax over all E,

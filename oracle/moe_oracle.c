@@ -528,24 +528,39 @@ void oracle_experts_backward(const double* x_disp, const uint32_t* offsets, int6
             dinput[r * H + h] = acc;
         }
     }
-    /* weight gradients: sums over each expert's rows */
-#pragma omp parallel for schedule(dynamic, 1)
+    /* weight gradients: sums over each expert's rows, taken in ascending row
+     * order for every weight (rows outermost so that the row data is read
+     * contiguously; the order of the additions is the same as a per-weight loop) */
+    double* sl = (double*)malloc((size_t)(nrows > 0 ? nrows : 1) * I * sizeof(double));
+#pragma omp parallel for
+    for (int64_t j = 0; j < nrows * I; ++j) sl[j] = silu(g[j]);
     for (int64_t e = 0; e < E; ++e) {
+        const int64_t r0 = offsets[e], r1 = offsets[e + 1];
+#pragma omp parallel for schedule(dynamic, 4)
         for (int64_t i = 0; i < I; ++i) {
-            for (int64_t h = 0; h < H; ++h) {
-                double sg = 0.0, su = 0.0, sd = 0.0;
-                for (int64_t r = offsets[e]; r < (int64_t)offsets[e + 1]; ++r) {
-                    const double gg = g[r * I + i], uu = u[r * I + i], d = da[r * I + i];
-                    sg += d * uu * silu_grad(gg) * x_disp[r * H + h];
-                    su += d * silu(gg) * x_disp[r * H + h];
-                    sd += dout[r * H + h] * silu(gg) * uu;
+            double* sg = dgate + (e * I + i) * H;
+            double* su = dup + (e * I + i) * H;
+            for (int64_t h = 0; h < H; ++h) sg[h] = su[h] = 0.0;
+            for (int64_t r = r0; r < r1; ++r) {
+                const double gg = g[r * I + i], uu = u[r * I + i], d = da[r * I + i];
+                const double cg = d * uu * silu_grad(gg), cu = d * silu(gg);
+                for (int64_t h = 0; h < H; ++h) {
+                    sg[h] += cg * x_disp[r * H + h];
+                    su[h] += cu * x_disp[r * H + h];
                 }
-                dgate[(e * I + i) * H + h] = sg;
-                dup[(e * I + i) * H + h] = su;
-                ddown[(e * H + h) * I + i] = sd;
+            }
+        }
+#pragma omp parallel for schedule(dynamic, 4)
+        for (int64_t h = 0; h < H; ++h) {
+            double* sd = ddown + (e * H + h) * I;
+            for (int64_t i = 0; i < I; ++i) sd[i] = 0.0;
+            for (int64_t r = r0; r < r1; ++r) {
+                const double dd = dout[r * H + h];
+                for (int64_t i = 0; i < I; ++i) sd[i] += dd * sl[r * I + i] * u[r * I + i];
             }
         }
     }
+    free(sl);
     free(g); free(u); free(da);
 }
 

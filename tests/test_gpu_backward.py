@@ -2,14 +2,18 @@
 
 Floating outputs follow the forward's bar (max |err| <= 1e-4 * max |ref| for
 FP32 outputs or FP32 weights, 2e-2 for BF16/FP16 outputs); the oracle's
-backward is itself pinned by finite differences (test_oracle_backward_pins)."""
+backward is itself pinned by finite differences (test_oracle_backward_pins).
+The tensor-core strategy holds a, dg and du in the 16-bit weight dtype, as
+the pages' training cache does, and these are the operands of its weight
+gradients: each operand carries a relative rounding error of at most 2^-8
+(BF16), so its FP32 weight gradients are held to 2e-2 * max |ref| too."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from gpu_helpers import DT, assert_y_close, stored, u32, values
-from top_routing_grouped_fp32_gb300.inputs import TORCH_DTYPES, make_inputs, small_workload
+from top_routing_grouped_fp32_gb300.inputs import TORCH_DTYPES, WORKLOADS, make_inputs, small_workload
 
 pytestmark = pytest.mark.gpu
 
@@ -23,13 +27,25 @@ def _close(got, ref, tol, what):
     assert err <= tol * scale, f"{what}: max err {err:.3e} > {tol} * {scale:.3e}"
 
 
-@pytest.mark.parametrize("T,E,k,H,I,dtype", [
+def _wgrad_tol(dtype, strategy):
+    return 1e-4 if strategy == "scalar" else 2e-2
+
+
+BWD_CASES = [
     (300, 8, 2, 256, 384, "bf16"),
     (257, 6, 3, 72, 40, "f32"),
+    (257, 6, 3, 72, 40, "bf16"),     # H, I not multiples of 64: ragged k-blocks and columns
     (200, 16, 4, 128, 96, "f16"),
     (64, 1, 1, 64, 64, "bf16"),
-])
-def test_expert_backward(cuda_lib, T, E, k, H, I, dtype):
+    (1500, 4, 2, 320, 704, "bf16"),  # 750 rows per expert: CTA-pair tiles, several m-tiles
+]
+
+
+@pytest.mark.parametrize("strategy", ["scalar", "tensor_core"])
+@pytest.mark.parametrize("T,E,k,H,I,dtype", BWD_CASES)
+def test_expert_backward(cuda_lib, T, E, k, H, I, dtype, strategy):
+    if strategy == "tensor_core" and dtype == "f32":
+        pytest.skip("the tensor-core strategy takes F16/BF16 experts (rejection tested below)")
     wl = small_workload(T, E, k, H, I, dtype=dtype, seed=T)
     inp = make_inputs(wl, device="cuda")
     experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
@@ -37,28 +53,57 @@ def test_expert_backward(cuda_lib, T, E, k, H, I, dtype):
     d = cuda_lib.moe_dispatch(idx, E, x=inp["x"])
     g = torch.Generator(device="cuda").manual_seed(5)
     dout = torch.randn((T * k, H), generator=g, device="cuda").to(TORCH_DTYPES[dtype])
-    dinput, dgate, dup, ddown = experts.backward(d.x_disp, d.offsets, dout)
+    dinput, dgate, dup, ddown = experts.backward(d.x_disp, d.offsets, dout, strategy=strategy)
     torch.cuda.synchronize()
     ref = oracle.experts_backward(values(d.x_disp), u32(d.offsets), stored(inp["gate"]), stored(inp["up"]),
                                   stored(inp["down"]), dtype, values(dout))
     assert_y_close(dinput, ref[0], dtype, "dinput")
     for name, got, r in (("dgate", dgate, ref[1]), ("dup", dup, ref[2]), ("ddown", ddown, ref[3])):
-        _close(got, r, 1e-4, name)
+        _close(got, r, _wgrad_tol(dtype, strategy), name)
 
 
-def test_expert_backward_empty_experts_get_zero(cuda_lib):
+@pytest.mark.parametrize("strategy", ["scalar", "tensor_core"])
+def test_expert_backward_empty_experts_get_zero(cuda_lib, strategy):
     wl = small_workload(100, 8, 1, 64, 64, dtype="bf16", seed=3, skew=6.0)
     inp = make_inputs(wl, device="cuda")
     experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
     idx, _ = cuda_lib.moe_route(inp["logits"], 1, True)
     d = cuda_lib.moe_dispatch(idx, wl.E, x=inp["x"])
     dout = torch.randn((100, 64), device="cuda").to(torch.bfloat16)
-    _, dgate, dup, ddown = experts.backward(d.x_disp, d.offsets, dout)
+    _, dgate, dup, ddown = experts.backward(d.x_disp, d.offsets, dout, strategy=strategy)
     torch.cuda.synchronize()
     cnt = np.diff(u32(d.offsets).astype(np.int64))
     assert (cnt == 0).any()
     for e in np.where(cnt == 0)[0]:
         assert torch.all(dgate[e] == 0) and torch.all(dup[e] == 0) and torch.all(ddown[e] == 0)
+
+
+def test_tensor_core_backward_rejects_fp32_and_auto_falls_back(cuda_lib):
+    wl = small_workload(50, 4, 2, 64, 64, dtype="f32", seed=9)
+    inp = make_inputs(wl, device="cuda")
+    experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    idx, _ = cuda_lib.moe_route(inp["logits"], 2, True)
+    d = cuda_lib.moe_dispatch(idx, 4, x=inp["x"])
+    dout = torch.randn((100, 64), device="cuda")
+    with pytest.raises(RuntimeError, match="UNSUPPORTED|unsupported"):
+        experts.backward(d.x_disp, d.offsets, dout, strategy="tensor_core")
+    a = experts.backward(d.x_disp, d.offsets, dout, strategy="auto")
+    s = experts.backward(d.x_disp, d.offsets, dout, strategy="scalar")
+    for x, y in zip(a, s):
+        assert torch.equal(x, y)
+
+
+def test_tensor_core_backward_is_deterministic(cuda_lib):
+    wl = small_workload(700, 8, 2, 192, 256, dtype="bf16", seed=11)
+    inp = make_inputs(wl, device="cuda")
+    experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    idx, _ = cuda_lib.moe_route(inp["logits"], 2, True)
+    d = cuda_lib.moe_dispatch(idx, 8, x=inp["x"])
+    dout = torch.randn((1400, 192), device="cuda").to(torch.bfloat16)
+    r1 = experts.backward(d.x_disp, d.offsets, dout, strategy="tensor_core")
+    r2 = experts.backward(d.x_disp, d.offsets, dout, strategy="tensor_core")
+    for x, y in zip(r1, r2):
+        assert torch.equal(x, y)
 
 
 @pytest.mark.parametrize("dtype,wdtype", [("bf16", "bf16"), ("f32", "f32"), ("f16", "bf16")])
@@ -105,3 +150,33 @@ def test_router_weights_and_backward(cuda_lib, scoring, renorm, scale, dtype, E,
     tol = 1e-4 if dtype == "f32" else 2e-2
     _close(dl, r_dl, tol, "dlogits")
     assert torch.isnan(dl[7]).all() and torch.isnan(w[7]).all()
+
+
+@pytest.mark.parametrize("name", ["finegrained_bf16", "skewed_bf16"])
+def test_tensor_core_backward_full_size(cuda_lib, name):
+    """Full-size workload through the tensor-core strategy; the oracle checks the
+    smallest non-empty expert completely (its rows' dinput and its three weight
+    gradients, as a one-expert problem) and every empty expert is all zeros."""
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, device="cuda")
+    experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    idx, _ = cuda_lib.moe_route(inp["logits"], wl.top_k, wl.renormalize)
+    d = cuda_lib.moe_dispatch(idx, wl.E, x=inp["x"])
+    off = u32(d.offsets).astype(np.int64)
+    N = int(off[-1])
+    g = torch.Generator(device="cuda").manual_seed(17)
+    dout = torch.randn((d.x_disp.shape[0], wl.H), generator=g, device="cuda").to(TORCH_DTYPES[wl.dtype])
+    dinput, dgate, dup, ddown = experts.backward(d.x_disp[:N], d.offsets, dout[:N], strategy="tensor_core")
+    torch.cuda.synchronize()
+    cnt = np.diff(off)
+    e = int(np.argmin(np.where(cnt > 0, cnt, np.iinfo(np.int64).max)))
+    r0, r1 = int(off[e]), int(off[e + 1])
+    sel = torch.as_tensor([e], device="cuda")
+    ref = oracle.experts_backward(values(d.x_disp[r0:r1]), np.array([0, r1 - r0], np.uint32),
+                                  stored(inp["gate"].index_select(0, sel)), stored(inp["up"].index_select(0, sel)),
+                                  stored(inp["down"].index_select(0, sel)), wl.dtype, values(dout[r0:r1]))
+    assert_y_close(dinput[r0:r1], ref[0], wl.dtype, "dinput")
+    for nm, got, r in (("dgate", dgate[e], ref[1][0]), ("dup", dup[e], ref[2][0]), ("ddown", ddown[e], ref[3][0])):
+        _close(got, r, 2e-2, nm)
+    for z in np.where(cnt == 0)[0]:
+        assert torch.all(dgate[z] == 0) and torch.all(dup[z] == 0) and torch.all(ddown[z] == 0)

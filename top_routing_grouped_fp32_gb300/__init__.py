@@ -159,6 +159,7 @@ def moe_combine(expert_out: torch.Tensor, perm: torch.Tensor, weights: torch.Ten
 
 # --------------------------------------------------------------------------
 # first-order training backward (user guide, section 12)
+BWD_STRATEGIES = {"scalar": 0, "auto": 1, "tensor_core": 2}
 # --------------------------------------------------------------------------
 
 def moe_combine_backward(expert_out: torch.Tensor, perm: torch.Tensor, weights: torch.Tensor,
@@ -300,9 +301,12 @@ class SwiGluExperts:
         return y
 
     def backward(self, x_disp: torch.Tensor, offsets: torch.Tensor, dout: torch.Tensor,
-                 workspace=None, stream=None):
-        """Expert backward (ExpertTrainingCache::backward): returns (dinput [N,H]
-        in the weight dtype, dgate [E,I,H], dup [E,I,H], ddown [E,H,I] in FP32)."""
+                 workspace=None, stream=None, strategy: str = "scalar"):
+        """Expert backward (ExpertTrainingCache::backward_with_strategy): returns
+        (dinput [N,H] in the weight dtype, dgate [E,I,H], dup [E,I,H], ddown
+        [E,H,I] in FP32).  ``strategy``: "scalar" (the default), "auto" or
+        "tensor_core" (F16/BF16 experts)."""
+        code = BWD_STRATEGIES[strategy]
         N = x_disp.shape[0]
         dev = x_disp.device
         dinput = torch.empty((N, self.H), dtype=self.dtype, device=dev)
@@ -311,9 +315,9 @@ class SwiGluExperts:
         ddown = torch.empty((self.E, self.H, self.I), dtype=torch.float32, device=dev)
         if workspace is None:
             workspace = _workspace(self._lib.moe_experts_backward_workspace_size(self.handle, N), dev)
-        _lib.check(self._lib.moe_experts_backward(self.handle, _ptr(x_disp), N, _ptr(offsets), _ptr(dout),
-                                                  _ptr(dinput), _ptr(dgate), _ptr(dup), _ptr(ddown),
-                                                  _ptr(workspace), workspace.numel(), _stream(stream)))
+        _lib.check(self._lib.moe_experts_backward_with_strategy(
+            self.handle, _ptr(x_disp), N, _ptr(offsets), _ptr(dout), _ptr(dinput), _ptr(dgate), _ptr(dup),
+            _ptr(ddown), code, _ptr(workspace), workspace.numel(), _stream(stream)))
         return dinput, dgate, dup, ddown
 
     def forward_sigmoid_grouped(self, x: torch.Tensor, logits: torch.Tensor, top_k: int, groups: int,

@@ -85,6 +85,7 @@ _SIGNATURES = {
     "moe_dispatch_backward": (ST, [P, INT, P, I64, I32, I64, P, P, SZ, P]),
     "moe_experts_backward_workspace_size": (SZ, [P, I64]),
     "moe_experts_backward": (ST, [P, P, I64, P, P, P, P, P, P, P, SZ, P]),
+    "moe_experts_backward_with_strategy": (ST, [P, P, I64, P, P, P, P, P, P, I32, P, SZ, P]),
     "moe_router_weights": (ST, [P, INT, P, I64, I64, I32, INT, INT, ctypes.c_float, P, P]),
     "moe_router_backward": (ST, [P, INT, P, P, I64, I64, I32, INT, INT, ctypes.c_float, P, P]),
     "moe_selftest_bounded_wait": (ST, [P, ctypes.c_uint32, P]),

@@ -9,6 +9,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -626,21 +628,42 @@ moe_status moe_dispatch_backward(const void* dinput, moe_dtype dt, const uint32_
   return ok();
 }
 
-size_t moe_experts_backward_workspace_size(moe_experts_t x, int64_t N) {
-  if (!x || N < 0) return 0;
-  return kWsHeader + 5 * align_up((size_t)N * x->I * 4, 1024);
+// The tensor-core backward applies when the experts are F16/BF16 with the
+// tcgen05 tensor maps and the transposed operands stay within the launch and
+// TMA coordinate limits.
+static bool bwd_tc_ok(const moe_experts* x, int64_t N) {
+  return x->tc && 2 * x->I <= 65535 * 32 && x->H <= 65535 * 32 &&
+         N + 63 * x->E + 63 < (int64_t)INT32_MAX;
 }
 
-moe_status moe_experts_backward(moe_experts_t x, const void* x_disp, int64_t N, const uint32_t* offsets,
-                                const void* dout, void* dinput, float* dgate, float* dup, float* ddown,
-                                void* ws, size_t ws_bytes, cudaStream_t stream) {
+size_t moe_experts_backward_workspace_size(moe_experts_t x, int64_t N) {
+  if (!x || N < 0) return 0;
+  size_t need = 5 * align_up((size_t)N * x->I * 4, 1024);
+  if (bwd_tc_ok(x, N))
+    need = std::max(need, moe::experts_backward_tc_workspace(N, (int)x->E, x->H, x->I));
+  return kWsHeader + need;
+}
+
+moe_status moe_experts_backward_with_strategy(moe_experts_t x, const void* x_disp, int64_t N,
+                                              const uint32_t* offsets, const void* dout,
+                                              void* dinput, float* dgate, float* dup, float* ddown,
+                                              int strategy, void* ws, size_t ws_bytes,
+                                              cudaStream_t stream) {
   moe_status st = check_handle(x);
   if (st != MOE_OK) return st;
+  if (strategy != MOE_BWD_SCALAR && strategy != MOE_BWD_AUTO && strategy != MOE_BWD_TENSOR_CORE)
+    return fail(MOE_ERR_INVALID_ARG, "strategy must be MOE_BWD_SCALAR, MOE_BWD_AUTO or MOE_BWD_TENSOR_CORE");
   if (N < 0 || N > kMaxRows) return fail(MOE_ERR_SHAPE, "N=%lld out of range", (long long)N);
+  if (strategy == MOE_BWD_TENSOR_CORE && !bwd_tc_ok(x, N))
+    return fail(MOE_ERR_UNSUPPORTED,
+                "tensor-core backward needs F16/BF16 experts with H, I multiples of 8");
   if (!offsets || !dgate || !dup || !ddown)
     return fail(MOE_ERR_INVALID_ARG, "offsets, dgate, dup and ddown must be non-NULL");
   if (N > 0 && (!x_disp || !dout || !dinput))
     return fail(MOE_ERR_INVALID_ARG, "x_disp, dout and dinput must be non-NULL");
+  const bool tc = strategy != MOE_BWD_SCALAR && bwd_tc_ok(x, N);
+  if (tc && N > 0 && (!aligned16(x_disp) || !aligned16(dout) || !aligned16(dinput)))
+    return fail(MOE_ERR_INVALID_ARG, "x_disp, dout and dinput must be 16-byte aligned");
   if ((st = check_ws(ws, ws_bytes, moe_experts_backward_workspace_size(x, N))) != MOE_OK) return st;
   const size_t part = align_up((size_t)N * x->I * 4, 1024);
   char* base = static_cast<char*>(ws) + kWsHeader;
@@ -665,6 +688,7 @@ moe_status moe_experts_backward(moe_experts_t x, const void* x_disp, int64_t N, 
   a.dgate = dgate;
   a.dup = dup;
   a.ddown = ddown;
+  a.status = status_word(ws);
   if (N == 0) {  // no rows: every weight gradient is zero
     const size_t wb = (size_t)x->E * x->I * x->H * 4;
     MOE_TRY_CUDA(cudaMemsetAsync(dgate, 0, wb, stream), "cudaMemsetAsync");
@@ -672,8 +696,21 @@ moe_status moe_experts_backward(moe_experts_t x, const void* x_disp, int64_t N, 
     MOE_TRY_CUDA(cudaMemsetAsync(ddown, 0, wb, stream), "cudaMemsetAsync");
     return ok();
   }
-  MOE_TRY_CUDA(moe::launch_experts_backward(a, stream), "expert backward launch");
+  if (tc) {
+    MOE_TRY_CUDA(cudaMemsetAsync(ws, 0, 4, stream), "cudaMemsetAsync");
+    MOE_TRY_CUDA(moe::launch_experts_backward_tc(a, x->tc, base, x->num_sms, stream),
+                 "tensor-core expert backward launch");
+  } else {
+    MOE_TRY_CUDA(moe::launch_experts_backward(a, stream), "expert backward launch");
+  }
   return ok();
+}
+
+moe_status moe_experts_backward(moe_experts_t x, const void* x_disp, int64_t N, const uint32_t* offsets,
+                                const void* dout, void* dinput, float* dgate, float* dup, float* ddown,
+                                void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return moe_experts_backward_with_strategy(x, x_disp, N, offsets, dout, dinput, dgate, dup, ddown,
+                                            MOE_BWD_SCALAR, ws, ws_bytes, stream);
 }
 
 static moe_status check_router_args(int64_t T, int64_t E, int32_t k, int scoring, float scale) {

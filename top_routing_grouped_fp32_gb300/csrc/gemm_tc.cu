@@ -87,6 +87,17 @@ struct Params {
   const void* weights;
   int wdt;
   uint32_t* status;
+  // backward products
+  void* out2;          // second output (kGateUpRaw: u; kSwigluBwd: a; kWgrad: rows >= split)
+  const void* gbuf;    // kSwigluBwd: recomputed g [rows, n_out]
+  const void* ubuf;    // kSwigluBwd: recomputed u [rows, n_out]
+  // kWgrad: per-expert batched product W_e = A_e^T-side x B_e over the
+  // 64-aligned column range [pad[e], pad[e+1]) of transposed operands
+  int wgrad;
+  const uint32_t* pad;
+  int mb;              // m-tiles per expert
+  int64_t m_total;     // rows of the transposed A operand (M)
+  int64_t split;       // output rows per buffer (M, or I for the [dgate; dup] pair)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -327,6 +338,8 @@ struct Tile {
   int e;
   int nb;
   int64_t m0;  // first row of the (pair) tile
+  int kx0;     // first K coordinate (0, or pad[e] for weight gradients)
+  int nk;      // k-blocks of this tile
 };
 
 __device__ __forceinline__ Tile decode_tile(uint32_t tile, const Params& p, const uint32_t* s_pref,
@@ -347,6 +360,23 @@ __device__ __forceinline__ Tile decode_tile(uint32_t tile, const Params& p, cons
   t.e = lo;
   t.nb = (int)(pid * w + rem % width);
   t.m0 = (int64_t)s_off[lo] + (int64_t)(rem / width) * tile_m;
+  t.kx0 = 0;
+  t.nk = p.k_blocks;
+  return t;
+}
+
+// Weight-gradient tiles: expert-major, then m-tile, then n-block; the K range
+// is the expert's padded column range of the transposed operands.
+__device__ __forceinline__ Tile decode_wgrad(uint32_t tile, const Params& p, int tile_m) {
+  const uint32_t per = (uint32_t)(p.mb * p.nb);
+  Tile t;
+  t.e = (int)(tile / per);
+  const uint32_t rem = tile - (uint32_t)t.e * per;
+  t.m0 = (int64_t)(rem / (uint32_t)p.nb) * tile_m;
+  t.nb = (int)(rem % (uint32_t)p.nb);
+  const uint32_t k0 = __ldg(p.pad + t.e), k1 = __ldg(p.pad + t.e + 1);
+  t.kx0 = (int)k0;
+  t.nk = (int)((k1 - k0) / BK);
   return t;
 }
 
@@ -431,7 +461,11 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   if constexpr (kCluster) cluster_sync();  // the peer's barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t total_tiles = s_pref[E] * (uint32_t)p.nb;
+  const uint32_t total_tiles =
+      p.wgrad ? (uint32_t)E * (uint32_t)(p.mb * p.nb) : s_pref[E] * (uint32_t)p.nb;
+  auto tile_at = [&](uint32_t tile) {
+    return p.wgrad ? decode_wgrad(tile, p, C::TILE_M) : decode_tile(tile, p, s_pref, s_off, C::TILE_M);
+  };
   // the leader CTA's barriers, as seen from this CTA
   const uint32_t full0_leader = kCluster ? mapa(full_bar(0), 0) : full_bar(0);
   const uint32_t tempty0_leader = kCluster ? mapa(tempty_bar(0), 0) : tempty_bar(0);
@@ -446,26 +480,31 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       for (int s = 0; s < STAGES; ++s) filled[s] = false, last_fill[s] = 0;
       bool ok = true;
       for (uint32_t tile = cluster_id; ok && tile < total_tiles; tile += num_clusters) {
-        const Tile t = decode_tile(tile, p, s_pref, s_off, C::TILE_M);
+        const Tile t = tile_at(tile);
         const int a_row = (int)(t.m0 + (int64_t)rank * BM);
         const int b0row = t.nb * p.cols_per_tile;
         const int b1row = b0row + p.b1_row_off;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = 0; kb < t.nk; ++kb) {
           if (!mbar_wait<kCluster>(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
           const uint32_t sa = ring + stage * C::STAGE_BYTES;
           const uint32_t fb = full0_leader + 8u * stage;
+          const int kx = t.kx0 + kb * BK;
           if (leader) mbar_expect_tx(full_bar(stage), C::STAGE_BYTES * PAIR);
-          tma_load_2d<PAIR>(sa, &mapA, kb * BK, a_row, fb);
-          if constexpr (PAIR == 1) {
-            tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kb * BK, b0row, t.e, fb);
-            tma_load_3d<PAIR>(sa + A_BYTES + B_HALF_BYTES, &mapB1, kb * BK, b1row, t.e, fb);
+          tma_load_2d<PAIR>(sa, &mapA, kx, a_row, fb);
+          if (p.wgrad) {  // B is the 2-D transposed operand
+            if (PAIR == 1 || leader) tma_load_2d<PAIR>(sa + A_BYTES, &mapB0, kx, b0row, fb);
+            if (PAIR == 1) tma_load_2d<PAIR>(sa + A_BYTES + B_HALF_BYTES, &mapB1, kx, b1row, fb);
+            else if (!leader) tma_load_2d<PAIR>(sa + A_BYTES, &mapB1, kx, b1row, fb);
+          } else if constexpr (PAIR == 1) {
+            tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kx, b0row, t.e, fb);
+            tma_load_3d<PAIR>(sa + A_BYTES + B_HALF_BYTES, &mapB1, kx, b1row, t.e, fb);
           } else if (leader) {
-            tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kb * BK, b0row, t.e, fb);
+            tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kx, b0row, t.e, fb);
           } else {
-            tma_load_3d<PAIR>(sa + A_BYTES, &mapB1, kb * BK, b1row, t.e, fb);
+            tma_load_3d<PAIR>(sa + A_BYTES, &mapB1, kx, b1row, t.e, fb);
           }
           filled[stage] = true;
           last_fill[stage] = phase;
@@ -494,10 +533,11 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       uint32_t phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (uint32_t tile = cluster_id; ok && tile < total_tiles; tile += num_clusters) {
+        const int nk = tile_at(tile).nk;  // 0 for an expert without rows (weight gradients)
         if (!mbar_wait<kCluster>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait<kCluster>(full_bar(stage), phase, abort_flag, p.status)) {
             ok = false;
             break;
@@ -534,9 +574,9 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     uint32_t acc = 0, acc_phase = 0;
     T* out = static_cast<T*>(p.out);
     for (uint32_t tile = cluster_id; tile < total_tiles; tile += num_clusters) {
-      const Tile t = decode_tile(tile, p, s_pref, s_off, C::TILE_M);
+      const Tile t = tile_at(tile);
       const int64_t grow = t.m0 + (int64_t)rank * BM + row;
-      const bool row_ok = grow < (int64_t)s_off[t.e + 1];
+      const bool row_ok = p.wgrad ? grow < p.m_total : grow < (int64_t)s_off[t.e + 1];
       // the weighted epilogue's slot and routing weight: loaded before the
       // accumulator wait so that their latency overlaps the MMAs
       int64_t wslot = grow;
@@ -552,16 +592,16 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      if (p.mode == kGateUpSwiglu) {
+      if (p.mode == kGateUpSwiglu || p.mode == kGateUpRaw) {
         const int64_t col0 = (int64_t)t.nb * 128;
-        T* dst = out + grow * p.n_out + col0;
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(taddr + c, g);
           tmem_ld32(taddr + 128 + c, u);
           tmem_wait_ld();
-          if (row_ok) {
+          if (row_ok && p.mode == kGateUpSwiglu) {
+            T* dst = out + grow * p.n_out + col0;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               if (col0 + c + v * 8 + 8 <= p.n_out) {
@@ -575,6 +615,79 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
                 *reinterpret_cast<uint4*>(dst + c + v * 8) = pack8<T>(f);
               }
             }
+          } else if (row_ok) {  // raw gate and up products, FP32, for the backward
+            float* dg = static_cast<float*>(p.out) + grow * p.n_out + col0 + c;
+            float* du = static_cast<float*>(p.out2) + grow * p.n_out + col0 + c;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              if (col0 + c + v * 4 + 4 <= p.n_out) {
+                *reinterpret_cast<uint4*>(dg + v * 4) = make_uint4(g[v * 4], g[v * 4 + 1], g[v * 4 + 2], g[v * 4 + 3]);
+                *reinterpret_cast<uint4*>(du + v * 4) = make_uint4(u[v * 4], u[v * 4 + 1], u[v * 4 + 2], u[v * 4 + 3]);
+              }
+            }
+          }
+        }
+      } else if (p.mode == kSwigluBwd) {
+        // accumulator = da = dout . W_down[e]; with g, u recomputed by the
+        // gate/up product: dg = da * u * silu'(g), du = da * silu(g) and the
+        // activation a = silu(g) * u, all three stored in the 16-bit dtype
+        const int64_t col0 = (int64_t)t.nb * 256;
+        const int64_t I = p.n_out;
+        const float* gsrc = static_cast<const float*>(p.gbuf) + grow * I + col0;
+        const float* usrc = static_cast<const float*>(p.ubuf) + grow * I + col0;
+        T* dgdu = out + grow * 2 * I + col0;
+        T* act = static_cast<T*>(p.out2) + grow * I + col0;
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(taddr + c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int cc = c + v * 8;
+            if (!row_ok || col0 + cc + 8 > I) continue;
+            const float4 g0 = *reinterpret_cast<const float4*>(gsrc + cc);
+            const float4 g1 = *reinterpret_cast<const float4*>(gsrc + cc + 4);
+            const float4 u0 = *reinterpret_cast<const float4*>(usrc + cc);
+            const float4 u1 = *reinterpret_cast<const float4*>(usrc + cc + 4);
+            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            float fdg[8], fdu[8], fa[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float da = __uint_as_float(o[v * 8 + i]);
+              const float sg = 1.f / (1.f + __expf(-gv[i]));
+              const float silu = gv[i] * sg;
+              fdg[i] = da * uv[i] * (sg + silu * (1.f - sg));
+              fdu[i] = da * silu;
+              fa[i] = silu * uv[i];
+            }
+            *reinterpret_cast<uint4*>(dgdu + cc) = pack8<T>(fdg);
+            *reinterpret_cast<uint4*>(dgdu + I + cc) = pack8<T>(fdu);
+            *reinterpret_cast<uint4*>(act + cc) = pack8<T>(fa);
+          }
+        }
+      } else if (p.mode == kWgrad) {
+        // FP32 weight-gradient tile; rows at or past `split` go to out2
+        const int64_t col0 = (int64_t)t.nb * 256;
+        float* dst = grow < p.split
+                         ? static_cast<float*>(p.out) + ((int64_t)t.e * p.split + grow) * p.n_out + col0
+                         : static_cast<float*>(p.out2) +
+                               ((int64_t)t.e * (p.m_total - p.split) + grow - p.split) * p.n_out + col0;
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t o[32];
+          if (t.nk > 0) {
+            tmem_ld32(taddr + c, o);
+            tmem_wait_ld();
+          } else {  // an expert without rows: its gradient is zero
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            if (row_ok && col0 + c + v * 4 + 4 <= p.n_out)
+              *reinterpret_cast<uint4*>(dst + c + v * 4) = make_uint4(o[v * 4], o[v * 4 + 1], o[v * 4 + 2], o[v * 4 + 3]);
           }
         }
       } else {
@@ -720,18 +833,23 @@ cudaError_t resident_clusters(int num_sms, int* out) {
 }
 
 template <typename T, int PAIR>
-cudaError_t launch_t(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB0,
+cudaError_t launch_t(int64_t N, int E, const CUtensorMap& mA, const CUtensorMap& mB0,
                      const CUtensorMap& mB1, Params p, int num_sms, cudaStream_t s) {
   int clusters = 0;
   cudaError_t err = resident_clusters<T, PAIR>(num_sms, &clusters);
   if (err != cudaSuccess) return err;
   if (clusters < 1) return cudaErrorLaunchOutOfResources;
   constexpr int TM = Cfg<PAIR>::TILE_M;
-  const int64_t mt_max = (a.N + TM - 1) / TM + std::min<int64_t>(a.E, a.N);
-  const int64_t tiles_max = mt_max * p.nb;
+  int64_t tiles_max;
+  if (p.wgrad) {
+    tiles_max = (int64_t)E * p.mb * p.nb;
+  } else {
+    const int64_t mt_max = (N + TM - 1) / TM + std::min<int64_t>(E, N);
+    tiles_max = mt_max * p.nb;
+  }
   const int nclu = (int)std::max<int64_t>(1, std::min<int64_t>(clusters, tiles_max));
   // panel width: about one wave of clusters spread over an expert's expected m-tiles
-  const int64_t mt_per_expert = std::max<int64_t>(1, (a.N + (int64_t)TM * a.E - 1) / ((int64_t)TM * a.E));
+  const int64_t mt_per_expert = std::max<int64_t>(1, (N + (int64_t)TM * E - 1) / ((int64_t)TM * E));
   p.panel = (int)std::max<int64_t>(1, std::min<int64_t>(p.nb, (nclu + mt_per_expert - 1) / mt_per_expert));
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -741,11 +859,162 @@ cudaError_t launch_t(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(nclu * PAIR);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = smem_bytes<PAIR>(a.E);
+  cfg.dynamicSmemBytes = smem_bytes<PAIR>(E);
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_tc<T, PAIR>, mA, mB0, mB1, p);
+}
+
+template <typename T>
+cudaError_t launch_any(bool pair, int64_t N, int E, const CUtensorMap& mA, const CUtensorMap& mB0,
+                       const CUtensorMap& mB1, const Params& p, int num_sms, cudaStream_t s) {
+  return pair ? launch_t<T, 2>(N, E, mA, mB0, mB1, p, num_sms, s)
+              : launch_t<T, 1>(N, E, mA, mB0, mB1, p, num_sms, s);
+}
+
+// ---------------------------------------------------------------- backward
+// Scratch of the tensor-core expert backward; every buffer 1024-byte aligned.
+struct BwdLayout {
+  int64_t ld;  // columns of the transposed row operands (>= sum of 64-padded segments)
+  size_t pad, g, u, dgdu, act, dgduT, xT, doutT, actT, wdT, wguT, total;
+};
+
+BwdLayout bwd_layout(int64_t N, int E, int64_t H, int64_t I) {
+  BwdLayout L{};
+  L.ld = (N + 63 * (int64_t)E + 63) / 64 * 64;
+  size_t off = 0;
+  auto take = [&off](size_t bytes) {
+    const size_t at = off;
+    off += (bytes + 1023) & ~(size_t)1023;
+    return at;
+  };
+  L.pad = take((size_t)(E + 1) * 4);
+  L.g = take((size_t)N * I * 4);
+  L.u = take((size_t)N * I * 4);
+  L.dgdu = take((size_t)N * 2 * I * 2);
+  L.act = take((size_t)N * I * 2);
+  L.dgduT = take((size_t)2 * I * L.ld * 2);
+  L.xT = take((size_t)H * L.ld * 2);
+  L.doutT = take((size_t)H * L.ld * 2);
+  L.actT = take((size_t)I * L.ld * 2);
+  L.wdT = take((size_t)E * I * H * 2);
+  L.wguT = take((size_t)E * H * 2 * I * 2);
+  L.total = off;
+  return L;
+}
+
+// Products of the backward, each one launch of grouped_gemm_tc:
+//   1. g, u   = x W_gate^T, x W_up^T                  (kGateUpRaw, FP32 out)
+//   2. da     = dout W_down = dout (W_down^T)^T; epilogue forms dg, du, a
+//   3. dinput = [dg | du] [W_gate ; W_up] = [dg | du] ([W_gate^T | W_up^T])^T
+//   4. [dgate ; dup] = [dg | du]^T x per expert       (kWgrad, K = the expert's rows)
+//   5. ddown         = dout^T a per expert
+// Every operand is K-major: the weight transposes and the row transposes
+// (each expert's rows padded with zero columns to a multiple of 64) are
+// done by transpose.cu's kernels.
+template <typename T>
+cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, int num_sms, cudaStream_t s) {
+  const int64_t N = a.N, H = a.H, I = a.I;
+  const int E = a.E;
+  const moe_dtype dt = a.dt;
+  const BwdLayout L = bwd_layout(N, E, H, I);
+  uint32_t* pad = reinterpret_cast<uint32_t*>(ws + L.pad);
+  float* g = reinterpret_cast<float*>(ws + L.g);
+  float* u = reinterpret_cast<float*>(ws + L.u);
+  void* dgdu = ws + L.dgdu;
+  void* act = ws + L.act;
+  void* dgduT = ws + L.dgduT;
+  void* xT = ws + L.xT;
+  void* doutT = ws + L.doutT;
+  void* actT = ws + L.actT;
+  void* wdT = ws + L.wdT;
+  void* wguT = ws + L.wguT;
+  cudaError_t err;
+#define MOE_TC_TRY(x) \
+  if ((err = (x)) != cudaSuccess) return err
+  MOE_TC_TRY(launch_pad_offsets(a.offsets, E, pad, s));
+  MOE_TC_TRY(launch_transpose_weights(a.down, dt, E, H, I, wdT, H, 0, s));       // [e][i][h]
+  MOE_TC_TRY(launch_transpose_weights(a.gate, dt, E, I, H, wguT, 2 * I, 0, s));  // [e][h][i]
+  MOE_TC_TRY(launch_transpose_weights(a.up, dt, E, I, H, wguT, 2 * I, I, s));    // [e][h][I + i]
+  CUtensorMap mX, mDo, mDgdu, mWd, mWgu, mDgduT, mXT, mDoT, mActT;
+  if (!encode_2d(&mX, a.x_disp, dt, N, H) || !encode_2d(&mDo, a.dout, dt, N, H) ||
+      !encode_2d(&mDgdu, dgdu, dt, N, 2 * I) || !encode_3d(&mWd, wdT, dt, E, I, H) ||
+      !encode_3d(&mWgu, wguT, dt, E, H, 2 * I) || !encode_2d(&mDgduT, dgduT, dt, 2 * I, L.ld) ||
+      !encode_2d(&mXT, xT, dt, H, L.ld) || !encode_2d(&mDoT, doutT, dt, H, L.ld) ||
+      !encode_2d(&mActT, actT, dt, I, L.ld))
+    return cudaErrorInvalidValue;
+  const bool pair = N >= (int64_t)BM * E;
+  Params base{};
+  base.offsets = a.offsets;
+  base.E = E;
+  base.status = a.status;
+  base.wdt = (int)MOE_F32;
+  // 1. g, u
+  Params p = base;
+  p.mode = kGateUpRaw;
+  p.k_blocks = (int)((H + BK - 1) / BK);
+  p.cols_per_tile = 128;
+  p.b1_row_off = 0;
+  p.n_out = I;
+  p.nb = (int)((I + 127) / 128);
+  p.out = g;
+  p.out2 = u;
+  MOE_TC_TRY(launch_any<T>(pair, N, E, mX, w->gate, w->up, p, num_sms, s));
+  // 2. da -> dg, du, a
+  p = base;
+  p.mode = kSwigluBwd;
+  p.k_blocks = (int)((H + BK - 1) / BK);
+  p.cols_per_tile = 256;
+  p.b1_row_off = 128;
+  p.n_out = I;
+  p.nb = (int)((I + 255) / 256);
+  p.out = dgdu;
+  p.out2 = act;
+  p.gbuf = g;
+  p.ubuf = u;
+  MOE_TC_TRY(launch_any<T>(pair, N, E, mDo, mWd, mWd, p, num_sms, s));
+  // 3. dinput
+  p = base;
+  p.mode = kDownPlain;
+  p.k_blocks = (int)((2 * I + BK - 1) / BK);
+  p.cols_per_tile = 256;
+  p.b1_row_off = 128;
+  p.n_out = H;
+  p.nb = (int)((H + 255) / 256);
+  p.out = a.dinput;
+  MOE_TC_TRY(launch_any<T>(pair, N, E, mDgdu, mWgu, mWgu, p, num_sms, s));
+  // 4-5. weight gradients over the transposed, segment-padded operands
+  const int64_t npad_max = N + 63 * (int64_t)E;
+  MOE_TC_TRY(launch_transpose_rows(dgdu, dt, 2 * I, a.offsets, pad, E, npad_max, dgduT, L.ld, s));
+  MOE_TC_TRY(launch_transpose_rows(a.x_disp, dt, H, a.offsets, pad, E, npad_max, xT, L.ld, s));
+  MOE_TC_TRY(launch_transpose_rows(a.dout, dt, H, a.offsets, pad, E, npad_max, doutT, L.ld, s));
+  MOE_TC_TRY(launch_transpose_rows(act, dt, I, a.offsets, pad, E, npad_max, actT, L.ld, s));
+  constexpr int TM = Cfg<2>::TILE_M;
+  p = base;
+  p.mode = kWgrad;
+  p.wgrad = 1;
+  p.pad = pad;
+  p.cols_per_tile = 256;
+  p.b1_row_off = 128;
+  p.m_total = 2 * I;
+  p.split = I;
+  p.mb = (int)((2 * I + TM - 1) / TM);
+  p.n_out = H;
+  p.nb = (int)((H + 255) / 256);
+  p.out = a.dgate;
+  p.out2 = a.dup;
+  MOE_TC_TRY((launch_t<T, 2>(N, E, mDgduT, mXT, mXT, p, num_sms, s)));
+  p.m_total = H;
+  p.split = H;
+  p.mb = (int)((H + TM - 1) / TM);
+  p.n_out = I;
+  p.nb = (int)((I + 255) / 256);
+  p.out = a.ddown;
+  p.out2 = a.ddown;
+  MOE_TC_TRY((launch_t<T, 2>(N, E, mDoT, mActT, mActT, p, num_sms, s)));
+#undef MOE_TC_TRY
+  return cudaSuccess;
 }
 
 }  // namespace tc
@@ -820,11 +1089,19 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, c
   // expert (decode-sized batches) the GEMM streams weights from HBM and single
   // CTAs keep twice as many independent streams in flight.
   const bool pair = a.N >= (int64_t)tc::BM * a.E;
-  if (a.dt == MOE_BF16)
-    return pair ? tc::launch_t<__nv_bfloat16, 2>(a, mA, *b0, *b1, p, num_sms, s)
-                : tc::launch_t<__nv_bfloat16, 1>(a, mA, *b0, *b1, p, num_sms, s);
-  return pair ? tc::launch_t<__half, 2>(a, mA, *b0, *b1, p, num_sms, s)
-              : tc::launch_t<__half, 1>(a, mA, *b0, *b1, p, num_sms, s);
+  if (a.dt == MOE_BF16) return tc::launch_any<__nv_bfloat16>(pair, a.N, a.E, mA, *b0, *b1, p, num_sms, s);
+  return tc::launch_any<__half>(pair, a.N, a.E, mA, *b0, *b1, p, num_sms, s);
+}
+
+size_t experts_backward_tc_workspace(int64_t N, int E, int64_t H, int64_t I) {
+  return tc::bwd_layout(N, E, H, I).total;
+}
+
+cudaError_t launch_experts_backward_tc(const ExpertsBwdArgs& a, const TcWeights* w, void* ws,
+                                       int num_sms, cudaStream_t s) {
+  char* base = static_cast<char*>(ws);
+  if (a.dt == MOE_BF16) return tc::backward_t<__nv_bfloat16>(a, w, base, num_sms, s);
+  return tc::backward_t<__half>(a, w, base, num_sms, s);
 }
 
 }  // namespace moe

@@ -53,7 +53,15 @@ cudaError_t launch_slot_sum(const void* slots, moe_dtype dt, int64_t T, int k, i
                             cudaStream_t s);
 
 // ---- grouped GEMMs ---------------------------------------------------------
-enum GemmMode { kGateUpSwiglu = 0, kDownPlain = 1, kDownWeighted = 2 };
+enum GemmMode {
+  kGateUpSwiglu = 0,
+  kDownPlain = 1,
+  kDownWeighted = 2,
+  // backward products (tcgen05 path only)
+  kGateUpRaw = 3,   // g and u in FP32 (out, out2)
+  kSwigluBwd = 4,   // da = dout W_down, then [dg | du] (out) and a (out2), 16-bit
+  kWgrad = 5,       // per-expert FP32 weight-gradient tiles over transposed operands
+};
 
 struct GemmArgs {
   int mode;
@@ -93,8 +101,17 @@ struct ExpertsBwdArgs {
   float* dgate;         // [E, I, H]
   float* dup;           // [E, I, H]
   float* ddown;         // [E, H, I]
+  uint32_t* status;     // device status word (bounded waits of the tensor-core path)
 };
 cudaError_t launch_experts_backward(const ExpertsBwdArgs& a, cudaStream_t s);
+
+// Layout changes for the tensor-core backward (transpose.cu)
+cudaError_t launch_pad_offsets(const uint32_t* offsets, int E, uint32_t* pad, cudaStream_t s);
+cudaError_t launch_transpose_rows(const void* src, moe_dtype dt, int64_t C, const uint32_t* offsets,
+                                  const uint32_t* pad, int E, int64_t npad_max, void* dst,
+                                  int64_t ld, cudaStream_t s);
+cudaError_t launch_transpose_weights(const void* src, moe_dtype dt, int64_t E, int64_t R, int64_t C,
+                                     void* dst, int64_t ld, int64_t col0, cudaStream_t s);
 
 // SIMT FP32-accumulate path (gemm_simt.cu): any dtype and shape
 cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
@@ -106,6 +123,12 @@ TcWeights* tc_weights_create(const void* gate, const void* up, const void* down,
 void tc_weights_destroy(TcWeights* w);
 cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, cudaStream_t s);
 bool tc_supported(moe_dtype dt, int64_t I, int64_t H);
+// Expert backward on the tcgen05 engine (F16/BF16): scratch of
+// experts_backward_tc_workspace(...) bytes at `ws` (1024-byte aligned);
+// a.g/u/act/dg/du are not used.
+size_t experts_backward_tc_workspace(int64_t N, int E, int64_t H, int64_t I);
+cudaError_t launch_experts_backward_tc(const ExpertsBwdArgs& a, const TcWeights* w, void* ws,
+                                       int num_sms, cudaStream_t s);
 // a kernel whose bounded wait is made to expire (failure-path self-test)
 cudaError_t launch_bounded_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
 
