@@ -629,11 +629,10 @@ moe_status moe_dispatch_backward(const void* dinput, moe_dtype dt, const uint32_
 }
 
 // The tensor-core backward applies when the experts are F16/BF16 with the
-// tcgen05 tensor maps and the transposed operands stay within the launch and
-// TMA coordinate limits.
+// tcgen05 tensor maps and the 64-padded row space stays within the TMA
+// coordinate range.
 static bool bwd_tc_ok(const moe_experts* x, int64_t N) {
-  return x->tc && 2 * x->I <= 65535 * 32 && x->H <= 65535 * 32 &&
-         N + 63 * x->E + 63 < (int64_t)INT32_MAX;
+  return x->tc && N + 63 * x->E < (int64_t)INT32_MAX;
 }
 
 size_t moe_experts_backward_workspace_size(moe_experts_t x, int64_t N) {

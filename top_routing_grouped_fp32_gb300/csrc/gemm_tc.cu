@@ -91,12 +91,18 @@ struct Params {
   void* out2;          // second output (kGateUpRaw: u; kSwigluBwd: a; kWgrad: rows >= split)
   const void* gbuf;    // kSwigluBwd: recomputed g [rows, n_out]
   const void* ubuf;    // kSwigluBwd: recomputed u [rows, n_out]
-  // kWgrad: per-expert batched product W_e = A_e^T-side x B_e over the
-  // 64-aligned column range [pad[e], pad[e+1]) of transposed operands
+  const uint32_t* pad; // pad[e] = sum over e' < e of roundup(rows of e', 64)
+  // operand forms: A K-major (rows x K) or MN-major (K rows x M columns);
+  // B K-major 3-D, MN-major 3-D (experts x K rows x N columns) or MN-major 2-D
+  int a_mn;
+  int b_form;
+  int a_row_pad;       // A rows live in the 64-padded row space (row - offsets[e] + pad[e])
+  int kb_split;        // > 0: k-blocks from here on read map B1 and A columns from a_k2 on
+  int a_k2;
+  // kWgrad: per-expert product over the padded row range [pad[e], pad[e+1])
   int wgrad;
-  const uint32_t* pad;
   int mb;              // m-tiles per expert
-  int64_t m_total;     // rows of the transposed A operand (M)
+  int64_t m_total;     // M of the product
   int64_t split;       // output rows per buffer (M, or I for the [dgate; dup] pair)
 };
 
@@ -326,8 +332,21 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
          | ((uint64_t)1 << 46)                     // descriptor version
          | ((uint64_t)2 << 61);                    // 128-byte swizzle
 }
+// The same for an MN-major tile: each TMA box holds 64 K rows of 64
+// consecutive M (or N) elements, 128 bytes a row, swizzled in 8-row groups
+// 1024 bytes apart (stride offset); boxes for the next 64 M/N elements follow
+// 8 KiB apart (leading offset).
+constexpr uint32_t MN_BOX_BYTES = 64 * BK * 2;  // 8 KiB
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4)
+         | ((uint64_t)(MN_BOX_BYTES >> 4) << 16)   // leading offset: next 64 M/N elements
+         | ((uint64_t)(1024 >> 4) << 32)           // stride offset: next 8 K rows
+         | ((uint64_t)1 << 46)
+         | ((uint64_t)2 << 61);
+}
+enum BForm { kBKmajor3d = 0, kBMNmajor3d = 1, kBMNmajor2d = 2 };
 // Instruction descriptor: FP32 accumulator, 16-bit A/B (bf16 or f16), both
-// K-major, M = 128*PAIR, N = 256.
+// K-major (bits 15/16 set below make A/B MN-major), M = 128*PAIR, N = 256.
 __host__ __device__ constexpr uint32_t make_idesc(bool bf16, int M) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
          ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -481,7 +500,9 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       bool ok = true;
       for (uint32_t tile = cluster_id; ok && tile < total_tiles; tile += num_clusters) {
         const Tile t = tile_at(tile);
-        const int a_row = (int)(t.m0 + (int64_t)rank * BM);
+        // A's row (K-major) or M column (MN-major) of this CTA's half
+        int a_row = (int)(t.m0 + (int64_t)rank * BM);
+        if (p.a_row_pad) a_row += (int)(__ldg(p.pad + t.e) - s_off[t.e]);
         const int b0row = t.nb * p.cols_per_tile;
         const int b1row = b0row + p.b1_row_off;
         for (int kb = 0; kb < t.nk; ++kb) {
@@ -491,20 +512,35 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           }
           const uint32_t sa = ring + stage * C::STAGE_BYTES;
           const uint32_t fb = full0_leader + 8u * stage;
-          const int kx = t.kx0 + kb * BK;
+          // K coordinates of this k-block: A's, and B's (row or column)
+          const bool second = p.kb_split > 0 && kb >= p.kb_split;  // [dg | du] . [W_gate ; W_up]: up half
+          const int kx = second ? p.a_k2 + (kb - p.kb_split) * BK : t.kx0 + kb * BK;
+          const int kb_b = second ? (kb - p.kb_split) * BK : t.kx0 + kb * BK;
+          const CUtensorMap* mb = second ? &mapB1 : &mapB0;
           if (leader) mbar_expect_tx(full_bar(stage), C::STAGE_BYTES * PAIR);
-          tma_load_2d<PAIR>(sa, &mapA, kx, a_row, fb);
-          if (p.wgrad) {  // B is the 2-D transposed operand
-            if (PAIR == 1 || leader) tma_load_2d<PAIR>(sa + A_BYTES, &mapB0, kx, b0row, fb);
-            if (PAIR == 1) tma_load_2d<PAIR>(sa + A_BYTES + B_HALF_BYTES, &mapB1, kx, b1row, fb);
-            else if (!leader) tma_load_2d<PAIR>(sa + A_BYTES, &mapB1, kx, b1row, fb);
-          } else if constexpr (PAIR == 1) {
-            tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kx, b0row, t.e, fb);
-            tma_load_3d<PAIR>(sa + A_BYTES + B_HALF_BYTES, &mapB1, kx, b1row, t.e, fb);
-          } else if (leader) {
-            tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kx, b0row, t.e, fb);
+          if (p.a_mn) {  // two 64-column boxes of this CTA's 128 M values
+            tma_load_2d<PAIR>(sa, &mapA, a_row, kx, fb);
+            tma_load_2d<PAIR>(sa + MN_BOX_BYTES, &mapA, a_row + 64, kx, fb);
           } else {
-            tma_load_3d<PAIR>(sa + A_BYTES, &mapB1, kx, b1row, t.e, fb);
+            tma_load_2d<PAIR>(sa, &mapA, kx, a_row, fb);
+          }
+          if (p.b_form == kBKmajor3d) {
+            if constexpr (PAIR == 1) {
+              tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kx, b0row, t.e, fb);
+              tma_load_3d<PAIR>(sa + A_BYTES + B_HALF_BYTES, &mapB1, kx, b1row, t.e, fb);
+            } else if (leader) {
+              tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kx, b0row, t.e, fb);
+            } else {
+              tma_load_3d<PAIR>(sa + A_BYTES, &mapB1, kx, b1row, t.e, fb);
+            }
+          } else {  // MN-major B: this CTA's N columns in boxes of 64
+            const int n0 = t.nb * 256 + (PAIR == 2 ? (int)rank * 128 : 0);
+#pragma unroll
+            for (int j = 0; j < (PAIR == 2 ? 2 : 4); ++j) {
+              const uint32_t dst = sa + A_BYTES + j * MN_BOX_BYTES;
+              if (p.b_form == kBMNmajor3d) tma_load_3d<PAIR>(dst, mb, n0 + 64 * j, kb_b, t.e, fb);
+              else tma_load_2d<PAIR>(dst, mb, n0 + 64 * j, kb_b, fb);
+            }
           }
           filled[stage] = true;
           last_fill[stage] = phase;
@@ -527,8 +563,11 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader CTA)
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc =
-          make_idesc(sizeof(T) == 2 && !std::is_same<T, __half>::value, C::TILE_M);
+      const uint32_t idesc = make_idesc(sizeof(T) == 2 && !std::is_same<T, __half>::value, C::TILE_M) |
+                             ((uint32_t)(p.a_mn != 0) << 15) | ((uint32_t)(p.b_form != kBKmajor3d) << 16);
+      // per 16-deep MMA step: 32 bytes along a K-major row, 16 rows of an MN-major box
+      const uint32_t a_step = p.a_mn ? 16u * 128u : UMMA_K * 2u;
+      const uint32_t b_step = p.b_form != kBKmajor3d ? 16u * 128u : UMMA_K * 2u;
       int stage = 0;
       uint32_t phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
@@ -547,8 +586,10 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           const uint32_t sb = sa + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            umma_f16<PAIR>(d_tmem, sw128_desc(sa + kk * UMMA_K * 2), sw128_desc(sb + kk * UMMA_K * 2),
-                           idesc, (kb | kk) != 0 ? 1u : 0u);
+            const uint32_t ak = sa + kk * a_step, bk = sb + kk * b_step;
+            umma_f16<PAIR>(d_tmem, p.a_mn ? sw128_mn_desc(ak) : sw128_desc(ak),
+                           p.b_form != kBKmajor3d ? sw128_mn_desc(bk) : sw128_desc(bk), idesc,
+                           (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit<PAIR>(empty_bar(stage));  // ring stage free (in every CTA) once done
           if (++stage == STAGES) {
@@ -630,13 +671,19 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       } else if (p.mode == kSwigluBwd) {
         // accumulator = da = dout . W_down[e]; with g, u recomputed by the
         // gate/up product: dg = da * u * silu'(g), du = da * silu(g) and the
-        // activation a = silu(g) * u, all three stored in the 16-bit dtype
+        // activation a = silu(g) * u, all three stored in the 16-bit dtype in
+        // the 64-padded row space (row - offsets[e] + pad[e]); the padding rows
+        // after an expert's last row are written as zeros
         const int64_t col0 = (int64_t)t.nb * 256;
         const int64_t I = p.n_out;
+        const int64_t local = grow - (int64_t)s_off[t.e];
+        const uint32_t pe = __ldg(p.pad + t.e);
+        const bool zero_row = !row_ok && local < (int64_t)(__ldg(p.pad + t.e + 1) - pe);
+        const int64_t prow = (int64_t)pe + local;
         const float* gsrc = static_cast<const float*>(p.gbuf) + grow * I + col0;
         const float* usrc = static_cast<const float*>(p.ubuf) + grow * I + col0;
-        T* dgdu = out + grow * 2 * I + col0;
-        T* act = static_cast<T*>(p.out2) + grow * I + col0;
+        T* dgdu = out + prow * 2 * I + col0;
+        T* act = static_cast<T*>(p.out2) + prow * I + col0;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
           uint32_t o[32];
@@ -645,7 +692,14 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int cc = c + v * 8;
-            if (!row_ok || col0 + cc + 8 > I) continue;
+            if (col0 + cc + 8 > I) continue;
+            if (zero_row) {
+              const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<uint4*>(dgdu + cc) = z;
+              *reinterpret_cast<uint4*>(dgdu + I + cc) = z;
+              *reinterpret_cast<uint4*>(act + cc) = z;
+            }
+            if (!row_ok) continue;
             const float4 g0 = *reinterpret_cast<const float4*>(gsrc + cc);
             const float4 g1 = *reinterpret_cast<const float4*>(gsrc + cc + 4);
             const float4 u0 = *reinterpret_cast<const float4*>(usrc + cc);
@@ -875,14 +929,15 @@ cudaError_t launch_any(bool pair, int64_t N, int E, const CUtensorMap& mA, const
 
 // ---------------------------------------------------------------- backward
 // Scratch of the tensor-core expert backward; every buffer 1024-byte aligned.
+// Row buffers marked P live in the 64-padded row space (npad rows).
 struct BwdLayout {
-  int64_t ld;  // columns of the transposed row operands (>= sum of 64-padded segments)
-  size_t pad, g, u, dgdu, act, dgduT, xT, doutT, actT, wdT, wguT, total;
+  int64_t npad;  // >= pad[E] for any offsets: N + 63 E
+  size_t pad, g, u, dgduP, actP, xP, doutP, total;
 };
 
 BwdLayout bwd_layout(int64_t N, int E, int64_t H, int64_t I) {
   BwdLayout L{};
-  L.ld = (N + 63 * (int64_t)E + 63) / 64 * 64;
+  L.npad = N + 63 * (int64_t)E;
   size_t off = 0;
   auto take = [&off](size_t bytes) {
     const size_t at = off;
@@ -892,27 +947,50 @@ BwdLayout bwd_layout(int64_t N, int E, int64_t H, int64_t I) {
   L.pad = take((size_t)(E + 1) * 4);
   L.g = take((size_t)N * I * 4);
   L.u = take((size_t)N * I * 4);
-  L.dgdu = take((size_t)N * 2 * I * 2);
-  L.act = take((size_t)N * I * 2);
-  L.dgduT = take((size_t)2 * I * L.ld * 2);
-  L.xT = take((size_t)H * L.ld * 2);
-  L.doutT = take((size_t)H * L.ld * 2);
-  L.actT = take((size_t)I * L.ld * 2);
-  L.wdT = take((size_t)E * I * H * 2);
-  L.wguT = take((size_t)E * H * 2 * I * 2);
+  L.dgduP = take((size_t)L.npad * 2 * I * 2);
+  L.actP = take((size_t)L.npad * I * 2);
+  L.xP = take((size_t)L.npad * H * 2);
+  L.doutP = take((size_t)L.npad * H * 2);
   L.total = off;
   return L;
 }
 
-// Products of the backward, each one launch of grouped_gemm_tc:
-//   1. g, u   = x W_gate^T, x W_up^T                  (kGateUpRaw, FP32 out)
-//   2. da     = dout W_down = dout (W_down^T)^T; epilogue forms dg, du, a
-//   3. dinput = [dg | du] [W_gate ; W_up] = [dg | du] ([W_gate^T | W_up^T])^T
-//   4. [dgate ; dup] = [dg | du]^T x per expert       (kWgrad, K = the expert's rows)
-//   5. ddown         = dout^T a per expert
-// Every operand is K-major: the weight transposes and the row transposes
-// (each expert's rows padded with zero columns to a multiple of 64) are
-// done by transpose.cu's kernels.
+// rows x cols (cols contiguous), box 64 rows x 64 columns: an MN-major operand
+bool encode_2d_mn(CUtensorMap* m, const void* base, moe_dtype dt, uint64_t rows, uint64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64u, (cuuint32_t)BK};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, tmap_type(dt), 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// experts x rows x cols (cols contiguous), box 1 x 64 x 64: an MN-major weight operand
+bool encode_3d_mn(CUtensorMap* m, const void* base, moe_dtype dt, uint64_t E, uint64_t rows,
+                  uint64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cols, rows, E};
+  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint32_t box[3] = {64u, (cuuint32_t)BK, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(m, tmap_type(dt), 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Products of the backward, each one launch of grouped_gemm_tc, every weight
+// read in its stored layout (MN-major where the product needs it transposed):
+//   1. g, u   = x W_gate^T, x W_up^T                   (kGateUpRaw, FP32 out)
+//   2. da     = dout W_down (W_down MN-major); the epilogue forms dg, du, a
+//               in the padded row space
+//   3. dinput = dg W_gate + du W_up (weights MN-major; one accumulator over
+//               the gate k-blocks, then the up k-blocks)
+//   4. [dgate ; dup] = [dg | du]^T x per expert   (both operands MN-major over
+//   5. ddown         = dout^T a per expert         the expert's padded rows)
 template <typename T>
 cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, int num_sms, cudaStream_t s) {
   const int64_t N = a.N, H = a.H, I = a.I;
@@ -922,34 +1000,28 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   uint32_t* pad = reinterpret_cast<uint32_t*>(ws + L.pad);
   float* g = reinterpret_cast<float*>(ws + L.g);
   float* u = reinterpret_cast<float*>(ws + L.u);
-  void* dgdu = ws + L.dgdu;
-  void* act = ws + L.act;
-  void* dgduT = ws + L.dgduT;
-  void* xT = ws + L.xT;
-  void* doutT = ws + L.doutT;
-  void* actT = ws + L.actT;
-  void* wdT = ws + L.wdT;
-  void* wguT = ws + L.wguT;
+  void* dgduP = ws + L.dgduP;
+  void* actP = ws + L.actP;
+  void* xP = ws + L.xP;
+  void* doutP = ws + L.doutP;
   cudaError_t err;
 #define MOE_TC_TRY(x) \
   if ((err = (x)) != cudaSuccess) return err
-  MOE_TC_TRY(launch_pad_offsets(a.offsets, E, pad, s));
-  MOE_TC_TRY(launch_transpose_weights(a.down, dt, E, H, I, wdT, H, 0, s));       // [e][i][h]
-  MOE_TC_TRY(launch_transpose_weights(a.gate, dt, E, I, H, wguT, 2 * I, 0, s));  // [e][h][i]
-  MOE_TC_TRY(launch_transpose_weights(a.up, dt, E, I, H, wguT, 2 * I, I, s));    // [e][h][I + i]
-  CUtensorMap mX, mDo, mDgdu, mWd, mWgu, mDgduT, mXT, mDoT, mActT;
+  CUtensorMap mX, mDo, mDgduP, mWdMN, mWgMN, mWuMN, mDgduMN, mXMN, mDoMN, mActMN;
   if (!encode_2d(&mX, a.x_disp, dt, N, H) || !encode_2d(&mDo, a.dout, dt, N, H) ||
-      !encode_2d(&mDgdu, dgdu, dt, N, 2 * I) || !encode_3d(&mWd, wdT, dt, E, I, H) ||
-      !encode_3d(&mWgu, wguT, dt, E, H, 2 * I) || !encode_2d(&mDgduT, dgduT, dt, 2 * I, L.ld) ||
-      !encode_2d(&mXT, xT, dt, H, L.ld) || !encode_2d(&mDoT, doutT, dt, H, L.ld) ||
-      !encode_2d(&mActT, actT, dt, I, L.ld))
+      !encode_2d(&mDgduP, dgduP, dt, L.npad, 2 * I) || !encode_3d_mn(&mWdMN, a.down, dt, E, H, I) ||
+      !encode_3d_mn(&mWgMN, a.gate, dt, E, I, H) || !encode_3d_mn(&mWuMN, a.up, dt, E, I, H) ||
+      !encode_2d_mn(&mDgduMN, dgduP, dt, L.npad, 2 * I) || !encode_2d_mn(&mXMN, xP, dt, L.npad, H) ||
+      !encode_2d_mn(&mDoMN, doutP, dt, L.npad, H) || !encode_2d_mn(&mActMN, actP, dt, L.npad, I))
     return cudaErrorInvalidValue;
+  MOE_TC_TRY(launch_pad_offsets(a.offsets, E, pad, s));
   const bool pair = N >= (int64_t)BM * E;
   Params base{};
   base.offsets = a.offsets;
   base.E = E;
   base.status = a.status;
   base.wdt = (int)MOE_F32;
+  base.pad = pad;
   // 1. g, u
   Params p = base;
   p.mode = kGateUpRaw;
@@ -961,42 +1033,43 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   p.out = g;
   p.out2 = u;
   MOE_TC_TRY(launch_any<T>(pair, N, E, mX, w->gate, w->up, p, num_sms, s));
-  // 2. da -> dg, du, a
+  // 2. da -> dg, du, a (padded rows)
   p = base;
   p.mode = kSwigluBwd;
+  p.b_form = kBMNmajor3d;
   p.k_blocks = (int)((H + BK - 1) / BK);
   p.cols_per_tile = 256;
-  p.b1_row_off = 128;
   p.n_out = I;
   p.nb = (int)((I + 255) / 256);
-  p.out = dgdu;
-  p.out2 = act;
+  p.out = dgduP;
+  p.out2 = actP;
   p.gbuf = g;
   p.ubuf = u;
-  MOE_TC_TRY(launch_any<T>(pair, N, E, mDo, mWd, mWd, p, num_sms, s));
+  MOE_TC_TRY(launch_any<T>(pair, N, E, mDo, mWdMN, mWdMN, p, num_sms, s));
   // 3. dinput
+  const int kbI = (int)((I + BK - 1) / BK);
   p = base;
   p.mode = kDownPlain;
-  p.k_blocks = (int)((2 * I + BK - 1) / BK);
+  p.b_form = kBMNmajor3d;
+  p.a_row_pad = 1;
+  p.kb_split = kbI;
+  p.a_k2 = (int)I;
+  p.k_blocks = 2 * kbI;
   p.cols_per_tile = 256;
-  p.b1_row_off = 128;
   p.n_out = H;
   p.nb = (int)((H + 255) / 256);
   p.out = a.dinput;
-  MOE_TC_TRY(launch_any<T>(pair, N, E, mDgdu, mWgu, mWgu, p, num_sms, s));
-  // 4-5. weight gradients over the transposed, segment-padded operands
-  const int64_t npad_max = N + 63 * (int64_t)E;
-  MOE_TC_TRY(launch_transpose_rows(dgdu, dt, 2 * I, a.offsets, pad, E, npad_max, dgduT, L.ld, s));
-  MOE_TC_TRY(launch_transpose_rows(a.x_disp, dt, H, a.offsets, pad, E, npad_max, xT, L.ld, s));
-  MOE_TC_TRY(launch_transpose_rows(a.dout, dt, H, a.offsets, pad, E, npad_max, doutT, L.ld, s));
-  MOE_TC_TRY(launch_transpose_rows(act, dt, I, a.offsets, pad, E, npad_max, actT, L.ld, s));
+  MOE_TC_TRY(launch_any<T>(pair, N, E, mDgduP, mWgMN, mWuMN, p, num_sms, s));
+  // 4-5. weight gradients over the padded rows
+  MOE_TC_TRY(launch_pad_rows(a.x_disp, H, a.offsets, pad, E, L.npad, xP, s));
+  MOE_TC_TRY(launch_pad_rows(a.dout, H, a.offsets, pad, E, L.npad, doutP, s));
   constexpr int TM = Cfg<2>::TILE_M;
   p = base;
   p.mode = kWgrad;
   p.wgrad = 1;
-  p.pad = pad;
+  p.a_mn = 1;
+  p.b_form = kBMNmajor2d;
   p.cols_per_tile = 256;
-  p.b1_row_off = 128;
   p.m_total = 2 * I;
   p.split = I;
   p.mb = (int)((2 * I + TM - 1) / TM);
@@ -1004,7 +1077,7 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   p.nb = (int)((H + 255) / 256);
   p.out = a.dgate;
   p.out2 = a.dup;
-  MOE_TC_TRY((launch_t<T, 2>(N, E, mDgduT, mXT, mXT, p, num_sms, s)));
+  MOE_TC_TRY((launch_t<T, 2>(N, E, mDgduMN, mXMN, mXMN, p, num_sms, s)));
   p.m_total = H;
   p.split = H;
   p.mb = (int)((H + TM - 1) / TM);
@@ -1012,7 +1085,7 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   p.nb = (int)((I + 255) / 256);
   p.out = a.ddown;
   p.out2 = a.ddown;
-  MOE_TC_TRY((launch_t<T, 2>(N, E, mDoT, mActT, mActT, p, num_sms, s)));
+  MOE_TC_TRY((launch_t<T, 2>(N, E, mDoMN, mActMN, mActMN, p, num_sms, s)));
 #undef MOE_TC_TRY
   return cudaSuccess;
 }

@@ -105,13 +105,10 @@ struct ExpertsBwdArgs {
 };
 cudaError_t launch_experts_backward(const ExpertsBwdArgs& a, cudaStream_t s);
 
-// Layout changes for the tensor-core backward (transpose.cu)
+// The 64-padded row space of the tensor-core backward (rowpad.cu)
 cudaError_t launch_pad_offsets(const uint32_t* offsets, int E, uint32_t* pad, cudaStream_t s);
-cudaError_t launch_transpose_rows(const void* src, moe_dtype dt, int64_t C, const uint32_t* offsets,
-                                  const uint32_t* pad, int E, int64_t npad_max, void* dst,
-                                  int64_t ld, cudaStream_t s);
-cudaError_t launch_transpose_weights(const void* src, moe_dtype dt, int64_t E, int64_t R, int64_t C,
-                                     void* dst, int64_t ld, int64_t col0, cudaStream_t s);
+cudaError_t launch_pad_rows(const void* src, int64_t C, const uint32_t* offsets, const uint32_t* pad,
+                            int E, int64_t npad_max, void* dst, cudaStream_t s);
 
 // SIMT FP32-accumulate path (gemm_simt.cu): any dtype and shape
 cudaError_t launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
