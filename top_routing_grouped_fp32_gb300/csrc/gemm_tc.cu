@@ -88,9 +88,8 @@ struct Params {
   int wdt;
   uint32_t* status;
   // backward products
-  void* out2;          // second output (kGateUpRaw: u; kSwigluBwd: a; kWgrad: rows >= split)
-  const void* gbuf;    // kSwigluBwd: recomputed g [rows, n_out]
-  const void* ubuf;    // kSwigluBwd: recomputed u [rows, n_out]
+  void* out2;          // second output (kSwigluBwd: a; kWgrad: rows >= split)
+  const void* da;      // kSwigluBwd: da = dout W_down, FP32 [rows, n_out]
   const uint32_t* pad; // pad[e] = sum over e' < e of roundup(rows of e', 64)
   // operand forms: A K-major (rows x K) or MN-major (K rows x M columns);
   // B K-major 3-D, MN-major 3-D (experts x K rows x N columns) or MN-major 2-D
@@ -633,16 +632,16 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      if (p.mode == kGateUpSwiglu || p.mode == kGateUpRaw) {
+      if (p.mode == kGateUpSwiglu) {
         const int64_t col0 = (int64_t)t.nb * 128;
+        T* dst = out + grow * p.n_out + col0;
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(taddr + c, g);
           tmem_ld32(taddr + 128 + c, u);
           tmem_wait_ld();
-          if (row_ok && p.mode == kGateUpSwiglu) {
-            T* dst = out + grow * p.n_out + col0;
+          if (row_ok) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               if (col0 + c + v * 8 + 8 <= p.n_out) {
@@ -656,38 +655,29 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
                 *reinterpret_cast<uint4*>(dst + c + v * 8) = pack8<T>(f);
               }
             }
-          } else if (row_ok) {  // raw gate and up products, FP32, for the backward
-            float* dg = static_cast<float*>(p.out) + grow * p.n_out + col0 + c;
-            float* du = static_cast<float*>(p.out2) + grow * p.n_out + col0 + c;
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              if (col0 + c + v * 4 + 4 <= p.n_out) {
-                *reinterpret_cast<uint4*>(dg + v * 4) = make_uint4(g[v * 4], g[v * 4 + 1], g[v * 4 + 2], g[v * 4 + 3]);
-                *reinterpret_cast<uint4*>(du + v * 4) = make_uint4(u[v * 4], u[v * 4 + 1], u[v * 4 + 2], u[v * 4 + 3]);
-              }
-            }
           }
         }
       } else if (p.mode == kSwigluBwd) {
-        // accumulator = da = dout . W_down[e]; with g, u recomputed by the
-        // gate/up product: dg = da * u * silu'(g), du = da * silu(g) and the
-        // activation a = silu(g) * u, all three stored in the 16-bit dtype in
-        // the 64-padded row space (row - offsets[e] + pad[e]); the padding rows
-        // after an expert's last row are written as zeros
-        const int64_t col0 = (int64_t)t.nb * 256;
+        // accumulators g = x . W_gate[e]^T, u = x . W_up[e]^T (recomputed); with
+        // da = dout . W_down[e] (FP32, from the previous product):
+        // dg = da * u * silu'(g), du = da * silu(g) and the activation
+        // a = silu(g) * u, stored in the 16-bit dtype in the 64-padded row
+        // space (row - offsets[e] + pad[e]); the padding rows after an
+        // expert's last row are written as zeros
+        const int64_t col0 = (int64_t)t.nb * 128;
         const int64_t I = p.n_out;
         const int64_t local = grow - (int64_t)s_off[t.e];
         const uint32_t pe = __ldg(p.pad + t.e);
         const bool zero_row = !row_ok && local < (int64_t)(__ldg(p.pad + t.e + 1) - pe);
         const int64_t prow = (int64_t)pe + local;
-        const float* gsrc = static_cast<const float*>(p.gbuf) + grow * I + col0;
-        const float* usrc = static_cast<const float*>(p.ubuf) + grow * I + col0;
+        const float* dasrc = static_cast<const float*>(p.da) + grow * I + col0;
         T* dgdu = out + prow * 2 * I + col0;
         T* act = static_cast<T*>(p.out2) + prow * I + col0;
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          uint32_t o[32];
-          tmem_ld32(taddr + c, o);
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c, g);
+          tmem_ld32(taddr + 128 + c, u);
           tmem_wait_ld();
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
@@ -700,25 +690,38 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
               *reinterpret_cast<uint4*>(act + cc) = z;
             }
             if (!row_ok) continue;
-            const float4 g0 = *reinterpret_cast<const float4*>(gsrc + cc);
-            const float4 g1 = *reinterpret_cast<const float4*>(gsrc + cc + 4);
-            const float4 u0 = *reinterpret_cast<const float4*>(usrc + cc);
-            const float4 u1 = *reinterpret_cast<const float4*>(usrc + cc + 4);
-            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-            const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            const float4 d0 = *reinterpret_cast<const float4*>(dasrc + cc);
+            const float4 d1 = *reinterpret_cast<const float4*>(dasrc + cc + 4);
+            const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
             float fdg[8], fdu[8], fa[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const float da = __uint_as_float(o[v * 8 + i]);
-              const float sg = 1.f / (1.f + __expf(-gv[i]));
-              const float silu = gv[i] * sg;
-              fdg[i] = da * uv[i] * (sg + silu * (1.f - sg));
-              fdu[i] = da * silu;
-              fa[i] = silu * uv[i];
+              const float gg = __uint_as_float(g[v * 8 + i]);
+              const float uu = __uint_as_float(u[v * 8 + i]);
+              const float sg = 1.f / (1.f + __expf(-gg));
+              const float silu = gg * sg;
+              fdg[i] = dv[i] * uu * (sg + silu * (1.f - sg));
+              fdu[i] = dv[i] * silu;
+              fa[i] = silu * uu;
             }
             *reinterpret_cast<uint4*>(dgdu + cc) = pack8<T>(fdg);
             *reinterpret_cast<uint4*>(dgdu + I + cc) = pack8<T>(fdu);
             *reinterpret_cast<uint4*>(act + cc) = pack8<T>(fa);
+          }
+        }
+      } else if (p.mode == kPlainF32) {
+        // the accumulator itself, FP32, rows in dispatch order
+        const int64_t col0 = (int64_t)t.nb * 256;
+        float* dst = static_cast<float*>(p.out) + grow * p.n_out + col0;
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(taddr + c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            if (row_ok && col0 + c + v * 4 + 4 <= p.n_out)
+              *reinterpret_cast<uint4*>(dst + c + v * 4) = make_uint4(o[v * 4], o[v * 4 + 1], o[v * 4 + 2], o[v * 4 + 3]);
           }
         }
       } else if (p.mode == kWgrad) {
@@ -932,7 +935,7 @@ cudaError_t launch_any(bool pair, int64_t N, int E, const CUtensorMap& mA, const
 // Row buffers marked P live in the 64-padded row space (npad rows).
 struct BwdLayout {
   int64_t npad;  // >= pad[E] for any offsets: N + 63 E
-  size_t pad, g, u, dgduP, actP, xP, doutP, total;
+  size_t pad, da, dgduP, actP, xP, doutP, total;
 };
 
 BwdLayout bwd_layout(int64_t N, int E, int64_t H, int64_t I) {
@@ -945,8 +948,7 @@ BwdLayout bwd_layout(int64_t N, int E, int64_t H, int64_t I) {
     return at;
   };
   L.pad = take((size_t)(E + 1) * 4);
-  L.g = take((size_t)N * I * 4);
-  L.u = take((size_t)N * I * 4);
+  L.da = take((size_t)N * I * 4);
   L.dgduP = take((size_t)L.npad * 2 * I * 2);
   L.actP = take((size_t)L.npad * I * 2);
   L.xP = take((size_t)L.npad * H * 2);
@@ -984,9 +986,9 @@ bool encode_3d_mn(CUtensorMap* m, const void* base, moe_dtype dt, uint64_t E, ui
 
 // Products of the backward, each one launch of grouped_gemm_tc, every weight
 // read in its stored layout (MN-major where the product needs it transposed):
-//   1. g, u   = x W_gate^T, x W_up^T                   (kGateUpRaw, FP32 out)
-//   2. da     = dout W_down (W_down MN-major); the epilogue forms dg, du, a
-//               in the padded row space
+//   1. da     = dout W_down (W_down MN-major), FP32
+//   2. g, u   = x W_gate^T, x W_up^T recomputed; the epilogue forms dg, du
+//               and a from them and da, in the padded row space
 //   3. dinput = dg W_gate + du W_up (weights MN-major; one accumulator over
 //               the gate k-blocks, then the up k-blocks)
 //   4. [dgate ; dup] = [dg | du]^T x per expert   (both operands MN-major over
@@ -998,8 +1000,7 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   const moe_dtype dt = a.dt;
   const BwdLayout L = bwd_layout(N, E, H, I);
   uint32_t* pad = reinterpret_cast<uint32_t*>(ws + L.pad);
-  float* g = reinterpret_cast<float*>(ws + L.g);
-  float* u = reinterpret_cast<float*>(ws + L.u);
+  float* da = reinterpret_cast<float*>(ws + L.da);
   void* dgduP = ws + L.dgduP;
   void* actP = ws + L.actP;
   void* xP = ws + L.xP;
@@ -1022,30 +1023,28 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   base.status = a.status;
   base.wdt = (int)MOE_F32;
   base.pad = pad;
-  // 1. g, u
+  // 1. da = dout W_down (FP32)
   Params p = base;
-  p.mode = kGateUpRaw;
-  p.k_blocks = (int)((H + BK - 1) / BK);
-  p.cols_per_tile = 128;
-  p.b1_row_off = 0;
-  p.n_out = I;
-  p.nb = (int)((I + 127) / 128);
-  p.out = g;
-  p.out2 = u;
-  MOE_TC_TRY(launch_any<T>(pair, N, E, mX, w->gate, w->up, p, num_sms, s));
-  // 2. da -> dg, du, a (padded rows)
-  p = base;
-  p.mode = kSwigluBwd;
+  p.mode = kPlainF32;
   p.b_form = kBMNmajor3d;
   p.k_blocks = (int)((H + BK - 1) / BK);
   p.cols_per_tile = 256;
   p.n_out = I;
   p.nb = (int)((I + 255) / 256);
+  p.out = da;
+  MOE_TC_TRY(launch_any<T>(pair, N, E, mDo, mWdMN, mWdMN, p, num_sms, s));
+  // 2. g, u recomputed; epilogue: dg, du, a (padded rows)
+  p = base;
+  p.mode = kSwigluBwd;
+  p.k_blocks = (int)((H + BK - 1) / BK);
+  p.cols_per_tile = 128;
+  p.b1_row_off = 0;
+  p.n_out = I;
+  p.nb = (int)((I + 127) / 128);
   p.out = dgduP;
   p.out2 = actP;
-  p.gbuf = g;
-  p.ubuf = u;
-  MOE_TC_TRY(launch_any<T>(pair, N, E, mDo, mWdMN, mWdMN, p, num_sms, s));
+  p.da = da;
+  MOE_TC_TRY(launch_any<T>(pair, N, E, mX, w->gate, w->up, p, num_sms, s));
   // 3. dinput
   const int kbI = (int)((I + BK - 1) / BK);
   p = base;

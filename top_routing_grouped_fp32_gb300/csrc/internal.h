@@ -58,9 +58,9 @@ enum GemmMode {
   kDownPlain = 1,
   kDownWeighted = 2,
   // backward products (tcgen05 path only)
-  kGateUpRaw = 3,   // g and u in FP32 (out, out2)
-  kSwigluBwd = 4,   // da = dout W_down, then [dg | du] (out) and a (out2), 16-bit
-  kWgrad = 5,       // per-expert FP32 weight-gradient tiles over transposed operands
+  kPlainF32 = 3,    // the accumulator in FP32 (da = dout W_down)
+  kSwigluBwd = 4,   // g, u recomputed, then [dg | du] (out) and a (out2), 16-bit
+  kWgrad = 5,       // per-expert FP32 weight-gradient tiles over the padded rows
 };
 
 struct GemmArgs {
