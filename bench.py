@@ -36,7 +36,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch of the gate/up GEMM on the headline workload, from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel source it was taken on; reported as null once the source changes.
-GATEUP_TRAFFIC = {"bytes": 1142896000 + 263958016,
+GATEUP_TRAFFIC = {"workload": "finegrained_bf16", "bytes": 1142896000 + 263958016,
                   "source_sha256": "35c95b98318c33bfdea14109b49b4df6e2080f98e6e4acce39e0cb06ae83c844"}
 
 
@@ -53,6 +53,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--dtype", choices=["bf16", "f16"], default=None,
                    help="store the workload in this dtype instead of its own")
+    p.add_argument("--tokens", type=int, default=None,
+                   help="override the workload's token count (small cases for profiler captures)")
     p.add_argument("--e2e-steps", type=int, default=50)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -85,6 +87,15 @@ def barrier(world: int, device=None):
             dist.barrier(device_ids=[device.index])
         else:
             dist.barrier()
+
+
+def bench_workload(args):
+    import dataclasses
+    from top_routing_grouped_fp32_gb300.inputs import WORKLOADS, with_dtype
+    wl = with_dtype(WORKLOADS[args.workload], args.dtype or WORKLOADS[args.workload].dtype)
+    if args.tokens is not None:
+        wl = dataclasses.replace(wl, name=f"{wl.name}_T{args.tokens}", T=args.tokens)
+    return wl
 
 
 def load_peaks():
@@ -270,7 +281,7 @@ def run_native(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     moe.load()
-    wl = with_dtype(WORKLOADS[args.workload], args.dtype or WORKLOADS[args.workload].dtype)
+    wl = bench_workload(args)
     inp = make_inputs(wl, device=dev)
     experts = moe.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
     ws = experts.forward_workspace(wl.T, wl.top_k, inp["logits"].dtype)
@@ -354,7 +365,8 @@ def run_native(args, rank, world, local):
         gateup_tflops = gateup_flops / (stage["gate_up_gemm"] * 1e-3) / 1e12
         peak = float(peaks["bf16_tflops"])
         src = "top_routing_grouped_fp32_gb300/csrc/gemm_tc.cu"
-        traffic = GATEUP_TRAFFIC["bytes"] if GATEUP_TRAFFIC["source_sha256"] == source_sha256(src) else None
+        traffic = (GATEUP_TRAFFIC["bytes"] if GATEUP_TRAFFIC["source_sha256"] == source_sha256(src)
+                   and GATEUP_TRAFFIC["workload"] == wl.name else None)
         s_el = 4 if wl.dtype == "f32" else 2
         w_gateup = touched * 2.0 * wl.H * wl.I * s_el
         w_all = touched * 3.0 * wl.H * wl.I * s_el
@@ -424,7 +436,7 @@ def run_backward(args, rank, world, local):
     from top_routing_grouped_fp32_gb300.inputs import WORKLOADS, make_inputs, with_dtype
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = with_dtype(WORKLOADS[args.workload], args.dtype or WORKLOADS[args.workload].dtype)
+    wl = bench_workload(args)
     inp = make_inputs(wl, device=dev)
     ex = moe.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
     idx, w = moe.moe_route(inp["logits"], wl.top_k, wl.renormalize)

@@ -168,9 +168,8 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 // Bounded wait for phase `parity` of `bar`.  Returns false if the CTA is
 // aborting or the time limit passed (then the abort flag and status are set).
 template <bool CLUSTER>
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                       uint32_t* status, uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_test<CLUSTER>(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                            uint32_t* status, uint64_t limit_ns) {
   const uint64_t t0 = global_timer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_test<CLUSTER>(bar, parity)) return true;
@@ -183,6 +182,12 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile u
       }
     }
   }
+}
+template <bool CLUSTER>
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                          uint32_t* status, uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_test<CLUSTER>(bar, parity)) return true;  // fast path, inline
+  return mbar_wait_slow<CLUSTER>(bar, parity, abort_flag, status, limit_ns);
 }
 // TMA tile loads into this CTA's shared memory.  PAIR == 2: the completion is
 // counted on `bar`, a shared::cluster address that may be the leader CTA's.
@@ -322,6 +327,54 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- epilogue stores
+// Each lane of an epilogue warp holds one tile row; storing straight from
+// registers would make every store instruction touch 32 rows.  Instead a
+// warp's 32 rows x WORDS 32-bit words pass through its staging buffer (rows
+// padded by 4 words against bank conflicts) and are written back CH = WORDS/4
+// lanes per row, so each store instruction covers whole row segments
+// (4 rows x 128 bytes for WORDS = 32, 8 rows x 64 bytes for WORDS = 16).
+constexpr int STG_STRIDE = 36;                         // words per staged row
+constexpr uint32_t STG_BYTES_PER_WARP = 32 * STG_STRIDE * 4;
+constexpr uint32_t STG_BYTES = 4 * STG_BYTES_PER_WARP;  // 18 KiB
+
+__device__ __forceinline__ void put4(uint32_t* w, uint4 q) {
+  w[0] = q.x;
+  w[1] = q.y;
+  w[2] = q.z;
+  w[3] = q.w;
+}
+// 32-bit words of a row segment that lie inside the output (cols_left >= 0)
+template <typename V>
+__device__ __forceinline__ int valid_words(int64_t cols_left) {
+  const int64_t w = cols_left * (int64_t)sizeof(V) / 4;
+  return w < 0 ? 0 : (int)(w < 32 ? w : 32);
+}
+// dst: this lane's row segment (nullptr: the row is not stored); the
+// segment's first `valid` words are written (a multiple of 4).
+template <int WORDS>
+__device__ __forceinline__ void staged_store(uint32_t* stg, const uint32_t* w, uint32_t* dst, int valid,
+                                             int lane) {
+  constexpr int STRIDE = WORDS + 4;
+  constexpr int CH = WORDS / 4;   // 16-byte chunks per row
+  constexpr int RPI = 32 / CH;    // rows per store instruction
+#pragma unroll
+  for (int j = 0; j < CH; ++j)
+    *reinterpret_cast<uint4*>(stg + lane * STRIDE + 4 * j) =
+        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  __syncwarp();
+  const int j = lane % CH;
+#pragma unroll
+  for (int it = 0; it < CH; ++it) {
+    const int r = lane / CH + RPI * it;
+    const uint4 v = *reinterpret_cast<const uint4*>(stg + r * STRIDE + 4 * j);
+    uint32_t* d = reinterpret_cast<uint32_t*>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dst), r));
+    if (d != nullptr && 4 * j < valid) *reinterpret_cast<uint4*>(d + 4 * j) = v;
+  }
+  __syncwarp();
+}
+
 // Shared-memory matrix descriptor of a K-major tile written by TMA with the
 // 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -410,10 +463,11 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t ring = (raw_s + 1023u) & ~1023u;  // 1024-byte aligned for the swizzle
   uint8_t* ring_ptr = smem_raw + (ring - raw_s);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + STAGES * C::STAGE_BYTES);
+  uint32_t* staging = reinterpret_cast<uint32_t*>(ring_ptr + STAGES * C::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + STAGES * C::STAGE_BYTES + STG_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile uint32_t* abort_flag = tmem_slot + 1;
-  uint32_t* s_off = reinterpret_cast<uint32_t*>(ring_ptr + STAGES * C::STAGE_BYTES + 256);
+  uint32_t* s_off = reinterpret_cast<uint32_t*>(ring_ptr + STAGES * C::STAGE_BYTES + STG_BYTES + 256);
   uint32_t* s_pref = s_off + (p.E + 1);
 
   const uint32_t bar0 = smem_u32(bars);
@@ -567,6 +621,9 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       // per 16-deep MMA step: 32 bytes along a K-major row, 16 rows of an MN-major box
       const uint32_t a_step = p.a_mn ? 16u * 128u : UMMA_K * 2u;
       const uint32_t b_step = p.b_form != kBKmajor3d ? 16u * 128u : UMMA_K * 2u;
+      // descriptor bits other than the start address
+      const uint64_t a_hi = p.a_mn ? sw128_mn_desc(0) : sw128_desc(0);
+      const uint64_t b_hi = p.b_form != kBKmajor3d ? sw128_mn_desc(0) : sw128_desc(0);
       int stage = 0;
       uint32_t phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
@@ -586,8 +643,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             const uint32_t ak = sa + kk * a_step, bk = sb + kk * b_step;
-            umma_f16<PAIR>(d_tmem, p.a_mn ? sw128_mn_desc(ak) : sw128_desc(ak),
-                           p.b_form != kBKmajor3d ? sw128_mn_desc(bk) : sw128_desc(bk), idesc,
+            umma_f16<PAIR>(d_tmem, a_hi | ((ak & 0x3FFFFu) >> 4), b_hi | ((bk & 0x3FFFFu) >> 4), idesc,
                            (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit<PAIR>(empty_bar(stage));  // ring stage free (in every CTA) once done
@@ -611,6 +667,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // this warp may access TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
+    uint32_t* stg = staging + quarter * (STG_BYTES_PER_WARP / 4);
     uint32_t acc = 0, acc_phase = 0;
     T* out = static_cast<T*>(p.out);
     for (uint32_t tile = cluster_id; tile < total_tiles; tile += num_clusters) {
@@ -633,6 +690,9 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
       if (p.mode == kGateUpSwiglu) {
+        // h = silu(g) * u: stored straight from registers (one 16-byte vector
+        // per 8 columns); this epilogue is not store-bound, and measured
+        // faster without the staging round trip
         const int64_t col0 = (int64_t)t.nb * 128;
         T* dst = out + grow * p.n_out + col0;
 #pragma unroll 1
@@ -671,101 +731,92 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         const bool zero_row = !row_ok && local < (int64_t)(__ldg(p.pad + t.e + 1) - pe);
         const int64_t prow = (int64_t)pe + local;
         const float* dasrc = static_cast<const float*>(p.da) + grow * I + col0;
-        T* dgdu = out + prow * 2 * I + col0;
-        T* act = static_cast<T*>(p.out2) + prow * I + col0;
+        const bool store = row_ok || zero_row;
+        uint32_t* dgp = store ? reinterpret_cast<uint32_t*>(out + prow * 2 * I + col0) : nullptr;
+        uint32_t* dup_p = store ? reinterpret_cast<uint32_t*>(out + prow * 2 * I + I + col0) : nullptr;
+        uint32_t* ap = store ? reinterpret_cast<uint32_t*>(static_cast<T*>(p.out2) + prow * I + col0) : nullptr;
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
-          uint32_t g[32], u[32];
+          uint32_t g[32], u[32], wdg[16], wdu[16], wa[16];
           tmem_ld32(taddr + c, g);
           tmem_ld32(taddr + 128 + c, u);
           tmem_wait_ld();
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int cc = c + v * 8;
-            if (col0 + cc + 8 > I) continue;
-            if (zero_row) {
-              const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-              *reinterpret_cast<uint4*>(dgdu + cc) = z;
-              *reinterpret_cast<uint4*>(dgdu + I + cc) = z;
-              *reinterpret_cast<uint4*>(act + cc) = z;
-            }
-            if (!row_ok) continue;
-            const float4 d0 = *reinterpret_cast<const float4*>(dasrc + cc);
-            const float4 d1 = *reinterpret_cast<const float4*>(dasrc + cc + 4);
-            const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
             float fdg[8], fdu[8], fa[8];
+            if (row_ok && col0 + cc + 8 <= I) {
+              const float4 d0 = *reinterpret_cast<const float4*>(dasrc + cc);
+              const float4 d1 = *reinterpret_cast<const float4*>(dasrc + cc + 4);
+              const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float gg = __uint_as_float(g[v * 8 + i]);
-              const float uu = __uint_as_float(u[v * 8 + i]);
-              const float sg = 1.f / (1.f + __expf(-gg));
-              const float silu = gg * sg;
-              fdg[i] = dv[i] * uu * (sg + silu * (1.f - sg));
-              fdu[i] = dv[i] * silu;
-              fa[i] = silu * uu;
+              for (int i = 0; i < 8; ++i) {
+                const float gg = __uint_as_float(g[v * 8 + i]);
+                const float uu = __uint_as_float(u[v * 8 + i]);
+                const float sg = 1.f / (1.f + __expf(-gg));
+                const float silu = gg * sg;
+                fdg[i] = dv[i] * uu * (sg + silu * (1.f - sg));
+                fdu[i] = dv[i] * silu;
+                fa[i] = silu * uu;
+              }
+            } else {  // padding row (or no row): zeros
+#pragma unroll
+              for (int i = 0; i < 8; ++i) fdg[i] = fdu[i] = fa[i] = 0.f;
             }
-            *reinterpret_cast<uint4*>(dgdu + cc) = pack8<T>(fdg);
-            *reinterpret_cast<uint4*>(dgdu + I + cc) = pack8<T>(fdu);
-            *reinterpret_cast<uint4*>(act + cc) = pack8<T>(fa);
+            put4(wdg + 4 * v, pack8<T>(fdg));
+            put4(wdu + 4 * v, pack8<T>(fdu));
+            put4(wa + 4 * v, pack8<T>(fa));
           }
+          const int vw = valid_words<T>(I - col0 - c);
+          staged_store<16>(stg, wdg, dgp ? dgp + c / 2 : nullptr, vw, lane);
+          staged_store<16>(stg, wdu, dup_p ? dup_p + c / 2 : nullptr, vw, lane);
+          staged_store<16>(stg, wa, ap ? ap + c / 2 : nullptr, vw, lane);
         }
-      } else if (p.mode == kPlainF32) {
-        // the accumulator itself, FP32, rows in dispatch order
+      } else if (p.mode == kPlainF32 || p.mode == kWgrad) {
+        // FP32 accumulator rows: da in dispatch order, or a weight-gradient
+        // tile (rows at or past `split` go to out2; an expert without rows
+        // gets zeros)
         const int64_t col0 = (int64_t)t.nb * 256;
-        float* dst = static_cast<float*>(p.out) + grow * p.n_out + col0;
+        float* rowf = nullptr;
+        if (row_ok) {
+          if (p.mode == kPlainF32)
+            rowf = static_cast<float*>(p.out) + grow * p.n_out + col0;
+          else if (grow < p.split)
+            rowf = static_cast<float*>(p.out) + ((int64_t)t.e * p.split + grow) * p.n_out + col0;
+          else
+            rowf = static_cast<float*>(p.out2) +
+                   ((int64_t)t.e * (p.m_total - p.split) + grow - p.split) * p.n_out + col0;
+        }
+        uint32_t* rowp = reinterpret_cast<uint32_t*>(rowf);
+        const bool empty = p.mode == kWgrad && t.nk == 0;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
           uint32_t o[32];
-          tmem_ld32(taddr + c, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            if (row_ok && col0 + c + v * 4 + 4 <= p.n_out)
-              *reinterpret_cast<uint4*>(dst + c + v * 4) = make_uint4(o[v * 4], o[v * 4 + 1], o[v * 4 + 2], o[v * 4 + 3]);
-          }
-        }
-      } else if (p.mode == kWgrad) {
-        // FP32 weight-gradient tile; rows at or past `split` go to out2
-        const int64_t col0 = (int64_t)t.nb * 256;
-        float* dst = grow < p.split
-                         ? static_cast<float*>(p.out) + ((int64_t)t.e * p.split + grow) * p.n_out + col0
-                         : static_cast<float*>(p.out2) +
-                               ((int64_t)t.e * (p.m_total - p.split) + grow - p.split) * p.n_out + col0;
-#pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          uint32_t o[32];
-          if (t.nk > 0) {
+          if (!empty) {
             tmem_ld32(taddr + c, o);
             tmem_wait_ld();
-          } else {  // an expert without rows: its gradient is zero
+          } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = 0u;
           }
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            if (row_ok && col0 + c + v * 4 + 4 <= p.n_out)
-              *reinterpret_cast<uint4*>(dst + c + v * 4) = make_uint4(o[v * 4], o[v * 4 + 1], o[v * 4 + 2], o[v * 4 + 3]);
-          }
+          staged_store<32>(stg, o, rowp ? rowp + c : nullptr, valid_words<float>(p.n_out - col0 - c), lane);
         }
       } else {
         const int64_t col0 = (int64_t)t.nb * 256;
-        T* dst = out + wslot * p.n_out + col0;
+        uint32_t* rowp = row_ok ? reinterpret_cast<uint32_t*>(out + wslot * p.n_out + col0) : nullptr;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
-          uint32_t o[32];
+          uint32_t o[32], w[16];
           tmem_ld32(taddr + c, o);
           tmem_wait_ld();
-          if (row_ok) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              if (col0 + c + v * 8 + 8 <= p.n_out) {
-                float f[8];
+          for (int v = 0; v < 4; ++v) {
+            float f[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[v * 8 + i]) * wscale;
-                *reinterpret_cast<uint4*>(dst + c + v * 8) = pack8<T>(f);
-              }
-            }
+            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[v * 8 + i]) * wscale;
+            put4(w + 4 * v, pack8<T>(f));
           }
+          staged_store<16>(stg, w, rowp ? rowp + c / 2 : nullptr, valid_words<T>(p.n_out - col0 - c), lane);
         }
       }
       tc_fence_before();
@@ -855,7 +906,7 @@ bool encode_3d(CUtensorMap* m, const void* base, moe_dtype dt, uint64_t E, uint6
 
 template <int PAIR>
 size_t smem_bytes(int E) {
-  return 1024 + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES + 256 + 8 * (size_t)(E + 1);
+  return 1024 + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES + STG_BYTES + 256 + 8 * (size_t)(E + 1);
 }
 
 // Clusters of PAIR CTAs that can be resident at once (one CTA per SM).
