@@ -710,7 +710,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
                 for (int i = 0; i < 8; ++i) {
                   const float gg = __uint_as_float(g[v * 8 + i]);
                   const float uu = __uint_as_float(u[v * 8 + i]);
-                  f[i] = gg / (1.f + __expf(-gg)) * uu;
+                  // 16-bit output: the fast divide's ~2 ulp are far below its rounding
+                  f[i] = __fdividef(gg * uu, 1.f + __expf(-gg));
                 }
                 *reinterpret_cast<uint4*>(dst + c + v * 8) = pack8<T>(f);
               }
@@ -735,33 +736,45 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         uint32_t* dgp = store ? reinterpret_cast<uint32_t*>(out + prow * 2 * I + col0) : nullptr;
         uint32_t* dup_p = store ? reinterpret_cast<uint32_t*>(out + prow * 2 * I + I + col0) : nullptr;
         uint32_t* ap = store ? reinterpret_cast<uint32_t*>(static_cast<T*>(p.out2) + prow * I + col0) : nullptr;
-#pragma unroll 1
+        // da of this row, 32 columns per chunk; the next chunk's loads are
+        // issued before the current chunk is computed so that their latency
+        // overlaps the TMEM reads and the arithmetic
+        auto load_da = [&](int c, float (&d)[32]) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float4 d0 = make_float4(0.f, 0.f, 0.f, 0.f), d1 = d0;
+            if (row_ok && col0 + c + v * 8 + 8 <= I) {
+              d0 = __ldg(reinterpret_cast<const float4*>(dasrc + c + v * 8));
+              d1 = __ldg(reinterpret_cast<const float4*>(dasrc + c + v * 8 + 4));
+            }
+            d[v * 8 + 0] = d0.x; d[v * 8 + 1] = d0.y; d[v * 8 + 2] = d0.z; d[v * 8 + 3] = d0.w;
+            d[v * 8 + 4] = d1.x; d[v * 8 + 5] = d1.y; d[v * 8 + 6] = d1.z; d[v * 8 + 7] = d1.w;
+          }
+        };
+        float dcur[32];
+        load_da(0, dcur);
+#pragma unroll
         for (int c = 0; c < 128; c += 32) {
+          float dnext[32];
+          if (c + 32 < 128) load_da(c + 32, dnext);
           uint32_t g[32], u[32], wdg[16], wdu[16], wa[16];
           tmem_ld32(taddr + c, g);
           tmem_ld32(taddr + 128 + c, u);
           tmem_wait_ld();
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const int cc = c + v * 8;
             float fdg[8], fdu[8], fa[8];
-            if (row_ok && col0 + cc + 8 <= I) {
-              const float4 d0 = *reinterpret_cast<const float4*>(dasrc + cc);
-              const float4 d1 = *reinterpret_cast<const float4*>(dasrc + cc + 4);
-              const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float gg = __uint_as_float(g[v * 8 + i]);
-                const float uu = __uint_as_float(u[v * 8 + i]);
-                const float sg = 1.f / (1.f + __expf(-gg));
-                const float silu = gg * sg;
-                fdg[i] = dv[i] * uu * (sg + silu * (1.f - sg));
-                fdu[i] = dv[i] * silu;
-                fa[i] = silu * uu;
-              }
-            } else {  // padding row (or no row): zeros
-#pragma unroll
-              for (int i = 0; i < 8; ++i) fdg[i] = fdu[i] = fa[i] = 0.f;
+            for (int i = 0; i < 8; ++i) {
+              // padding rows (and rows not stored) have da = 0 and store zeros
+              const float gg = row_ok ? __uint_as_float(g[v * 8 + i]) : 0.f;
+              const float uu = row_ok ? __uint_as_float(u[v * 8 + i]) : 0.f;
+              const float dv = dcur[v * 8 + i];
+              const float sg = __fdividef(1.f, 1.f + __expf(-gg));  // 16-bit outputs
+              const float silu = gg * sg;
+              fdg[i] = dv * uu * (sg + silu * (1.f - sg));
+              fdu[i] = dv * silu;
+              fa[i] = silu * uu;
             }
             put4(wdg + 4 * v, pack8<T>(fdg));
             put4(wdu + 4 * v, pack8<T>(fdu));
@@ -771,6 +784,10 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           staged_store<16>(stg, wdg, dgp ? dgp + c / 2 : nullptr, vw, lane);
           staged_store<16>(stg, wdu, dup_p ? dup_p + c / 2 : nullptr, vw, lane);
           staged_store<16>(stg, wa, ap ? ap + c / 2 : nullptr, vw, lane);
+          if (c + 32 < 128) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dcur[i] = dnext[i];
+          }
         }
       } else if (p.mode == kPlainF32 || p.mode == kWgrad) {
         // FP32 accumulator rows: da in dispatch order, or a weight-gradient
