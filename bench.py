@@ -36,8 +36,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch of the gate/up GEMM on the headline workload, from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel source it was taken on; reported as null once the source changes.
-GATEUP_TRAFFIC = {"workload": "finegrained_bf16", "bytes": 1142896000 + 263958016,
-                  "source_sha256": "35c95b98318c33bfdea14109b49b4df6e2080f98e6e4acce39e0cb06ae83c844"}
+GATEUP_TRAFFIC = {"workload": "finegrained_bf16", "bytes": 1144104448 + 264506624,
+                  "source_sha256": "263205887871ce899edf3b01805866d81d61406be4054f50a3452674ec181cb5"}
 
 
 def parse_args(argv=None):
@@ -364,6 +364,10 @@ def run_native(args, rank, world, local):
         tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
         gateup_tflops = gateup_flops / (stage["gate_up_gemm"] * 1e-3) / 1e12
         peak = float(peaks["bf16_tflops"])
+        # the GEMMs are timed inside the step loop (hundreds of steps, under the
+        # power cap: the clock record shows sw_power_cap), so their roofline is
+        # the measured sustained bf16 rate; the burst fraction is kept beside it
+        peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
         src = "top_routing_grouped_fp32_gb300/csrc/gemm_tc.cu"
         traffic = (GATEUP_TRAFFIC["bytes"] if GATEUP_TRAFFIC["source_sha256"] == source_sha256(src)
                    and GATEUP_TRAFFIC["workload"] == wl.name else None)
@@ -383,10 +387,11 @@ def run_native(args, rank, world, local):
                         "algorithmic_per_launch": f"touched*2*H*I*2 = {w_gateup:.4e} B"}
         else:
             roofline = {"bound": "tensor", "kernel": "grouped_gemm_tc (gate/up + SwiGLU)",
-                        "achieved": gateup_tflops, "peak": peak, "unit": "TFLOP/s",
-                        "frac": gateup_tflops / peak,
-                        "traffic": traffic if wl.name == DEFAULT_WORKLOAD else None,
-                        "peak_source": f"{peaks_src} bf16_tflops (burst)",
+                        "achieved": gateup_tflops, "peak": peak_sus, "unit": "TFLOP/s",
+                        "frac": gateup_tflops / peak_sus,
+                        "traffic": traffic,
+                        "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside the step loop)",
+                        "frac_of_burst": gateup_tflops / peak,
                         "algorithmic_per_launch": f"4*N*H*I = {gateup_flops:.4e} FLOP"}
         line = {
             "metric": METRIC,
@@ -398,6 +403,7 @@ def run_native(args, rank, world, local):
             "config": workload_config(wl),
             "gemm_tflops": tflops,
             "gemm_frac_of_peak": tflops / peak,
+            "gemm_frac_of_sustained_peak": tflops / peak_sus,
             "stages_ms": stage,
             "roofline": roofline,
             "weights_hbm": weights_hbm,
@@ -476,10 +482,11 @@ def run_backward(args, rank, world, local):
     tensor = args.bwd_strategy == "tensor_core" or (args.bwd_strategy == "auto" and wl.dtype != "f32")
     if tensor:
         peaks, peaks_src = load_peaks()
+        sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
         roof = {"bound": "tensor", "kernel": "experts backward (tcgen05 chain)", "achieved": ach,
-                "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
-                "frac": ach / float(peaks["bf16_tflops"]),
-                "peak_source": f"{peaks_src} bf16_tflops (burst)"}
+                "peak": sus, "unit": "TFLOP/s", "frac": ach / sus,
+                "peak_source": f"{peaks_src} bf16_tflops_sustained (timed inside the step loop)",
+                "frac_of_burst": ach / float(peaks["bf16_tflops"])}
     else:
         peak = 152 * 128 * 2 * 2.07e9 / 1e12
         roof = {"bound": "alu", "kernel": "experts backward (FP32 FMA)", "achieved": ach,
