@@ -327,24 +327,43 @@ def run_native(args, rank, world, local):
     stage = {n: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
              for j, n in enumerate(names)}
 
-    # end to end through the host-buffer entry point: copies inside the timed region
-    xh = inp["x"].cpu().pin_memory()
-    lh = inp["logits"].cpu().pin_memory()
-    yh = torch.empty((wl.T, wl.H), dtype=inp["x"].dtype).pin_memory()
-    wsh = experts.forward_host_workspace(wl.T, wl.top_k, inp["logits"].dtype)
-    for _ in range(3):
-        experts.forward_host(xh, lh, wl.top_k, wl.renormalize, yh, wsh, stream=stream)
-    torch.cuda.synchronize(dev)
+    # end to end through the host-buffer entry points: every step copies its
+    # inputs in from pinned host memory and its result out, inside the timed
+    # region.  `e2e` is the pipelined entry point (moe_host_pipeline_*, the
+    # copies of neighbouring steps overlap the forward between them; two sets
+    # of host buffers alternate); `e2e_serial` is one moe_forward_host call per
+    # step (copy in, forward, copy out on one stream).  Host wall clock between
+    # two device synchronisations.
+    xh = [inp["x"].cpu().pin_memory() for _ in range(2)]
+    lh = [inp["logits"].cpu().pin_memory() for _ in range(2)]
+    yh = [torch.empty((wl.T, wl.H), dtype=inp["x"].dtype).pin_memory() for _ in range(2)]
     Ke = max(1, args.e2e_steps)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pipe = experts.host_pipeline(wl.T, wl.top_k, wl.renormalize, logits_dtype=inp["logits"].dtype,
+                                 depth=2, stream=stream)
+    for i in range(3):
+        pipe.submit(xh[i % 2], lh[i % 2], yh[i % 2])
+    pipe.sync()
     barrier(world, dev)
     torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for _ in range(Ke):
-        experts.forward_host(xh, lh, wl.top_k, wl.renormalize, yh, wsh, stream=stream)
-    e1.record(stream)
+    t0 = time.perf_counter()
+    for i in range(Ke):
+        pipe.submit(xh[i % 2], lh[i % 2], yh[i % 2])
+    pipe.sync()
     torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev)
+    pipe.close()
+    wsh = experts.forward_host_workspace(wl.T, wl.top_k, inp["logits"].dtype)
+    for _ in range(3):
+        experts.forward_host(xh[0], lh[0], wl.top_k, wl.renormalize, yh[0], wsh, stream=stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(Ke):
+        experts.forward_host(xh[0], lh[0], wl.top_k, wl.renormalize, yh[0], wsh, stream=stream)
+    torch.cuda.synchronize(dev)
+    e2e_serial_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev)
+    xh, lh, yh = xh[0], lh[0], yh[0]
     h2d = xh.numel() * xh.element_size() + lh.numel() * lh.element_size()
     d2h = yh.numel() * yh.element_size()
 
@@ -407,7 +426,10 @@ def run_native(args, rank, world, local):
             "stages_ms": stage,
             "roofline": roofline,
             "weights_hbm": weights_hbm,
+            "e2e_serial": {"value": wl.T * world * Ke / (e2e_serial_ms * 1e-3), "unit": UNIT,
+                           "api": "moe_forward_host, one call per step"},
             "e2e": {"value": wl.T * world * Ke / (e2e_ms * 1e-3), "unit": UNIT,
+                    "api": "moe_host_pipeline_submit (depth 2), one call per step",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": LAUNCHES_PER_STEP * K,
             "clocks": clock_info,

@@ -270,6 +270,38 @@ moe_status moe_forward_host(moe_experts_t experts, const void* x_host, const voi
                             void* y_host, void* workspace, size_t workspace_bytes,
                             cudaStream_t stream);
 
+/* Pipelined host-buffer forward for a stream of batches (serving).  Not a
+ * call of the pages: their forward takes device tensors (user guide
+ * section 6); this overlaps the host copies of consecutive batches with the
+ * forward of the batch between them.
+ *   - The pipeline owns `depth` (2..4) device staging slots for x, logits and
+ *     y, one host-to-device and one device-to-host stream, and CUDA events.
+ *     Its device memory is the caller's workspace of
+ *     moe_host_pipeline_workspace_size(...) bytes (256-byte aligned), which
+ *     must outlive the pipeline.  The forward itself runs on `stream`, given
+ *     at creation.
+ *   - moe_host_pipeline_submit(p, x_host, logits_host, y_host, T), T <= T_max:
+ *     enqueues the copy of x and logits into the next slot (after that slot's
+ *     previous forward has consumed it), the forward on `stream`, and the copy
+ *     of y back to y_host (after the forward).  It returns without waiting.
+ *     Host buffers should be pinned for the copies to overlap; they must stay
+ *     valid, and y_host unread, until moe_host_pipeline_sync returns.
+ *   - moe_host_pipeline_sync waits for every submitted batch.
+ *   - moe_host_pipeline_destroy synchronises and frees the streams and events.
+ * Results are bitwise those of moe_forward on the same batch.  The device
+ * status word is the one at the start of the workspace. */
+typedef struct moe_host_pipeline* moe_host_pipeline_t;
+size_t moe_host_pipeline_workspace_size(moe_experts_t experts, int64_t T_max, int32_t top_k,
+                                        moe_dtype logits_dtype, int depth);
+moe_status moe_host_pipeline_create(moe_experts_t experts, int64_t T_max, int32_t top_k,
+                                    moe_dtype logits_dtype, int renormalize, int depth,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                                    moe_host_pipeline_t* out);
+moe_status moe_host_pipeline_submit(moe_host_pipeline_t pipeline, const void* x_host,
+                                    const void* logits_host, void* y_host, int64_t T);
+moe_status moe_host_pipeline_sync(moe_host_pipeline_t pipeline);
+moe_status moe_host_pipeline_destroy(moe_host_pipeline_t pipeline);
+
 /* Byte offsets of the intermediates moe_forward leaves in its workspace, so
  * that a caller can inspect them after the stream has finished:
  *   idx [T,k] u32, weights [T,k] logits dtype, offsets [E+1] u32,

@@ -31,7 +31,7 @@ _CODE_TORCH = {v: k for k, v in _TORCH_CODES.items()}
 __all__ = ["load", "moe_route", "moe_route_sigmoid_grouped", "moe_dispatch", "moe_combine",
            "SwiGluExperts", "Dispatched", "moe_combine_backward", "moe_dispatch_backward",
            "moe_router_weights", "moe_router_backward",
-           "moe_get_device_status", "MoeError", "library_path"]
+           "moe_get_device_status", "MoeError", "library_path", "HostPipeline"]
 
 
 def load():
@@ -352,6 +352,56 @@ class SwiGluExperts:
             _ptr(workspace), workspace.numel(), _stream(stream)))
         return y_host
 
+    def host_pipeline(self, T_max: int, top_k: int, renormalize: bool, logits_dtype=torch.bfloat16,
+                      depth: int = 2, stream=None) -> "HostPipeline":
+        """A pipelined host-buffer forward (moe_host_pipeline_*) for a stream of
+        batches of up to T_max tokens."""
+        return HostPipeline(self, T_max, top_k, renormalize, logits_dtype, depth, stream)
+
     def forward_host_workspace(self, T: int, top_k: int, logits_dtype=torch.bfloat16) -> torch.Tensor:
         n = self._lib.moe_forward_host_workspace_size(self.handle, T, top_k, _TORCH_CODES[logits_dtype])
         return _workspace(n, self.gate.device)
+
+
+class HostPipeline:
+    """moe_host_pipeline_*: host batches in, host results out; the copies of
+    consecutive batches overlap the forward of the batch between them.  Keep
+    the host tensors alive and y unread until ``sync()``."""
+
+    def __init__(self, experts: SwiGluExperts, T_max: int, top_k: int, renormalize: bool,
+                 logits_dtype, depth: int, stream):
+        self._lib = experts._lib
+        self.experts = experts
+        self.T_max = T_max
+        self.H, self.E = experts.H, experts.E
+        code = _TORCH_CODES[logits_dtype]
+        n = self._lib.moe_host_pipeline_workspace_size(experts.handle, T_max, top_k, code, depth)
+        self.workspace = _workspace(n, experts.gate.device)
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        h = ctypes.c_void_p()
+        _lib.check(self._lib.moe_host_pipeline_create(
+            experts.handle, T_max, top_k, code, int(bool(renormalize)), depth, _ptr(self.workspace),
+            self.workspace.numel(), _stream(self.stream), ctypes.byref(h)))
+        self.handle = h
+
+    def submit(self, x_host: torch.Tensor, logits_host: torch.Tensor, y_host: torch.Tensor):
+        for t in (x_host, logits_host, y_host):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError("submit takes contiguous host tensors")
+        _lib.check(self._lib.moe_host_pipeline_submit(
+            self.handle, ctypes.c_void_p(x_host.data_ptr()), ctypes.c_void_p(logits_host.data_ptr()),
+            ctypes.c_void_p(y_host.data_ptr()), x_host.shape[0]))
+
+    def sync(self):
+        _lib.check(self._lib.moe_host_pipeline_sync(self.handle))
+
+    def close(self):
+        if self.handle:
+            _lib.check(self._lib.moe_host_pipeline_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -79,6 +79,11 @@ _SIGNATURES = {
     "moe_forward_timed": (ST, [P, P, P, INT, I64, I32, INT, P, P, SZ, P, ctypes.POINTER(P), INT]),
     "moe_forward_host_workspace_size": (SZ, [P, I64, I32, INT]),
     "moe_forward_host": (ST, [P, P, P, INT, I64, I32, INT, P, P, SZ, P]),
+    "moe_host_pipeline_workspace_size": (SZ, [P, I64, I32, INT, INT]),
+    "moe_host_pipeline_create": (ST, [P, I64, I32, INT, INT, INT, P, SZ, P, ctypes.POINTER(P)]),
+    "moe_host_pipeline_submit": (ST, [P, P, P, P, I64]),
+    "moe_host_pipeline_sync": (ST, [P]),
+    "moe_host_pipeline_destroy": (ST, [P]),
     "moe_forward_layout": (ST, [P, I64, I32, INT, ctypes.POINTER(ForwardLayout)]),
     "moe_get_device_status": (ST, [P, P]),
     "moe_combine_backward": (ST, [P, INT, P, P, INT, P, I64, I32, I64, P, P, P]),

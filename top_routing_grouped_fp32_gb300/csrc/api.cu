@@ -587,6 +587,154 @@ moe_status moe_forward_host(moe_experts_t x, const void* x_host, const void* log
   return ok();
 }
 
+// ---- pipelined host-buffer forward -----------------------------------------
+struct moe_host_pipeline {
+  static constexpr int kMaxDepth = 4;
+  moe_experts* x;
+  int64_t T_max;
+  int32_t top_k;
+  moe_dtype ldt;
+  int renormalize;
+  int depth;
+  char* ws;
+  size_t fwd_bytes;
+  cudaStream_t stream, h2d, d2h;
+  struct Slot {
+    char *xs, *ls, *ys;
+    cudaEvent_t loaded, computed, stored;
+    bool used;
+  } slot[kMaxDepth];
+  uint64_t submitted;
+};
+
+namespace {
+struct PipelineSizes {
+  size_t fwd, xb, lb, per_slot;
+};
+PipelineSizes pipeline_sizes(const moe_experts* x, int64_t T, int32_t k, moe_dtype ldt) {
+  PipelineSizes z;
+  z.fwd = align_up(forward_layout(x, T, k, ldt).total, 1024);
+  z.xb = align_up((size_t)T * x->H * dtype_size(x->dt), 1024);
+  z.lb = align_up((size_t)T * x->E * dtype_size(ldt), 1024);
+  z.per_slot = 2 * z.xb + z.lb;
+  return z;
+}
+void pipeline_free(moe_host_pipeline* p) {
+  for (int i = 0; i < moe_host_pipeline::kMaxDepth; ++i) {
+    auto& sl = p->slot[i];
+    if (sl.loaded) cudaEventDestroy(sl.loaded);
+    if (sl.computed) cudaEventDestroy(sl.computed);
+    if (sl.stored) cudaEventDestroy(sl.stored);
+  }
+  if (p->h2d) cudaStreamDestroy(p->h2d);
+  if (p->d2h) cudaStreamDestroy(p->d2h);
+  delete p;
+}
+}  // namespace
+
+size_t moe_host_pipeline_workspace_size(moe_experts_t x, int64_t T_max, int32_t top_k, moe_dtype ldt,
+                                        int depth) {
+  if (!x || T_max < 1 || top_k < 1 || !valid_dtype(ldt) || depth < 2 ||
+      depth > moe_host_pipeline::kMaxDepth)
+    return 0;
+  const PipelineSizes z = pipeline_sizes(x, T_max, top_k, ldt);
+  return z.fwd + (size_t)depth * z.per_slot;
+}
+
+moe_status moe_host_pipeline_create(moe_experts_t x, int64_t T_max, int32_t top_k, moe_dtype ldt,
+                                    int renormalize, int depth, void* ws, size_t ws_bytes,
+                                    cudaStream_t stream, moe_host_pipeline_t* out) {
+  moe_status st = check_handle(x);
+  if (st != MOE_OK) return st;
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "out must be non-NULL");
+  *out = nullptr;
+  if (!valid_dtype(ldt)) return fail(MOE_ERR_DTYPE, "logits dtype %d is not F32/F16/BF16", (int)ldt);
+  if (T_max < 1) return fail(MOE_ERR_SHAPE, "T_max must be >= 1");
+  if ((st = check_tek(T_max, x->E, top_k)) != MOE_OK) return st;
+  if (depth < 2 || depth > moe_host_pipeline::kMaxDepth)
+    return fail(MOE_ERR_INVALID_ARG, "depth must be in 2..=4");
+  if ((st = check_ws(ws, ws_bytes, moe_host_pipeline_workspace_size(x, T_max, top_k, ldt, depth))) != MOE_OK)
+    return st;
+  moe_host_pipeline* p = new moe_host_pipeline();
+  p->x = x;
+  p->T_max = T_max;
+  p->top_k = top_k;
+  p->ldt = ldt;
+  p->renormalize = renormalize;
+  p->depth = depth;
+  p->ws = static_cast<char*>(ws);
+  p->stream = stream;
+  const PipelineSizes z = pipeline_sizes(x, T_max, top_k, ldt);
+  p->fwd_bytes = z.fwd;
+  cudaError_t e = cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking);
+  for (int i = 0; i < depth && e == cudaSuccess; ++i) {
+    auto& sl = p->slot[i];
+    sl.xs = p->ws + z.fwd + (size_t)i * z.per_slot;
+    sl.ys = sl.xs + z.xb;
+    sl.ls = sl.ys + z.xb;
+    e = cudaEventCreateWithFlags(&sl.loaded, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sl.computed, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sl.stored, cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) {
+    pipeline_free(p);
+    return cuda_fail(e, "host pipeline streams and events");
+  }
+  *out = p;
+  return ok();
+}
+
+moe_status moe_host_pipeline_submit(moe_host_pipeline_t p, const void* x_host, const void* logits_host,
+                                    void* y_host, int64_t T) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "pipeline is NULL");
+  if (T < 0 || T > p->T_max) return fail(MOE_ERR_SHAPE, "T=%lld outside 0..=T_max", (long long)T);
+  if (T == 0) return ok();
+  if (!x_host || !logits_host || !y_host)
+    return fail(MOE_ERR_INVALID_ARG, "x_host, logits_host and y_host must be non-NULL");
+  moe_experts* x = p->x;
+  auto& sl = p->slot[p->submitted % (uint64_t)p->depth];
+  const size_t xb = (size_t)T * x->H * dtype_size(x->dt), lb = (size_t)T * x->E * dtype_size(p->ldt);
+  // inputs: into this slot once its previous forward has read it
+  if (sl.used) MOE_TRY_CUDA(cudaStreamWaitEvent(p->h2d, sl.computed, 0), "cudaStreamWaitEvent");
+  MOE_TRY_CUDA(cudaMemcpyAsync(sl.xs, x_host, xb, cudaMemcpyHostToDevice, p->h2d), "cudaMemcpyAsync x");
+  MOE_TRY_CUDA(cudaMemcpyAsync(sl.ls, logits_host, lb, cudaMemcpyHostToDevice, p->h2d),
+               "cudaMemcpyAsync logits");
+  MOE_TRY_CUDA(cudaEventRecord(sl.loaded, p->h2d), "cudaEventRecord");
+  // forward: after the inputs landed and the slot's previous y was copied out
+  MOE_TRY_CUDA(cudaStreamWaitEvent(p->stream, sl.loaded, 0), "cudaStreamWaitEvent");
+  if (sl.used) MOE_TRY_CUDA(cudaStreamWaitEvent(p->stream, sl.stored, 0), "cudaStreamWaitEvent");
+  moe_status st = forward_impl(x, sl.xs, sl.ls, p->ldt, T, p->top_k, p->renormalize, sl.ys, p->ws,
+                               p->fwd_bytes, p->stream, nullptr);
+  if (st != MOE_OK) return st;
+  MOE_TRY_CUDA(cudaEventRecord(sl.computed, p->stream), "cudaEventRecord");
+  // output
+  MOE_TRY_CUDA(cudaStreamWaitEvent(p->d2h, sl.computed, 0), "cudaStreamWaitEvent");
+  MOE_TRY_CUDA(cudaMemcpyAsync(y_host, sl.ys, xb, cudaMemcpyDeviceToHost, p->d2h), "cudaMemcpyAsync y");
+  MOE_TRY_CUDA(cudaEventRecord(sl.stored, p->d2h), "cudaEventRecord");
+  sl.used = true;
+  ++p->submitted;
+  return ok();
+}
+
+moe_status moe_host_pipeline_sync(moe_host_pipeline_t p) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "pipeline is NULL");
+  MOE_TRY_CUDA(cudaStreamSynchronize(p->h2d), "cudaStreamSynchronize");
+  MOE_TRY_CUDA(cudaStreamSynchronize(p->stream), "cudaStreamSynchronize");
+  MOE_TRY_CUDA(cudaStreamSynchronize(p->d2h), "cudaStreamSynchronize");
+  return ok();
+}
+
+moe_status moe_host_pipeline_destroy(moe_host_pipeline_t p) {
+  if (!p) return ok();
+  const cudaError_t e1 = cudaStreamSynchronize(p->h2d);
+  const cudaError_t e2 = cudaStreamSynchronize(p->d2h);
+  pipeline_free(p);
+  if (e1 != cudaSuccess) return cuda_fail(e1, "cudaStreamSynchronize");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaStreamSynchronize");
+  return ok();
+}
+
 // ---- first-order training backward (user guide, section 12) -------------
 moe_status moe_combine_backward(const void* expert_out, moe_dtype dt, const uint32_t* perm,
                                 const void* weights, moe_dtype wdt, const void* dy, int64_t T,
