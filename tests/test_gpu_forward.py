@@ -51,6 +51,9 @@ def _check_routing_and_dispatch(experts, ws, wl, logits):
     (200, 16, 4, 512, 128, "f16", True),
     (150, 5, 2, 40, 70, "f32", True),
     (100, 4, 2, 60, 90, "bf16", False),
+    # >= 128 rows per expert: the gate/up product gathers the token rows itself
+    (1000, 4, 2, 200, 136, "bf16", True),   # H = 3*64 + 8: a one-chunk k-block tail
+    (700, 3, 3, 72, 64, "f16", False),      # H = 64 + 8
 ])
 def test_forward_small_all_tokens(cuda_lib, T, E, k, H, I, dtype, renorm):
     wl = small_workload(T, E, k, H, I, dtype=dtype, renormalize=renorm, seed=T + E)
