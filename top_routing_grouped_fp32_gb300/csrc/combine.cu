@@ -26,13 +26,14 @@ __global__ void invert_perm_kernel(const uint32_t* __restrict__ perm, int64_t N,
   if (s < (uint64_t)N) slot_row[s] = (uint32_t)r;
 }
 
+// source rows are read once: evict-first loads
 template <typename T>
 __device__ __forceinline__ void load8(const T* p, float* f) {
   if constexpr (sizeof(T) == 2) {
-    unpack8<T>(__ldg(reinterpret_cast<const uint4*>(p)), f);
+    unpack8<T>(__ldcs(reinterpret_cast<const uint4*>(p)), f);
   } else {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
     f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
     f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
   }

@@ -191,15 +191,18 @@ gather_kernel(const char* __restrict__ x, int64_t row_bytes, int k, const uint32
     const int64_t nv = row_bytes / 16;
     const uint4* s4 = reinterpret_cast<const uint4*>(src);
     uint4* d4 = reinterpret_cast<uint4*>(dst);
+    // 8 loads in flight per lane (a 4 KiB row in one round); x_disp is
+    // written with evict-first stores so that it does not push the token
+    // rows, each read top_k times, out of L2
     int64_t v = lane;
-    for (; v + 3 * 32 < nv; v += 4 * 32) {
-      uint4 a = __ldg(s4 + v), b = __ldg(s4 + v + 32), c = __ldg(s4 + v + 64), d = __ldg(s4 + v + 96);
-      d4[v] = a;
-      d4[v + 32] = b;
-      d4[v + 64] = c;
-      d4[v + 96] = d;
+    for (; v + 7 * 32 < nv; v += 8 * 32) {
+      uint4 q[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q[i] = __ldg(s4 + v + 32 * i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) __stcs(d4 + v + 32 * i, q[i]);
     }
-    for (; v < nv; v += 32) d4[v] = __ldg(s4 + v);
+    for (; v < nv; v += 32) __stcs(d4 + v, __ldg(s4 + v));
   } else {
     const int64_t nv = row_bytes / 2;
     const uint16_t* s2 = reinterpret_cast<const uint16_t*>(src);
