@@ -1084,6 +1084,29 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
       !encode_2d_mn(&mDoMN, doutP, dt, L.npad, H) || !encode_2d_mn(&mActMN, actP, dt, L.npad, I))
     return cudaErrorInvalidValue;
   MOE_TC_TRY(launch_pad_offsets(a.offsets, E, pad, s));
+  // x and dout into the padded row space on a side stream: they are needed
+  // only by products 4 and 5 and co-run with products 1-3 (whose CTAs leave
+  // registers and threads free on every SM)
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  MOE_TC_TRY(cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking));
+  err = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+  if (err == cudaSuccess) err = cudaEventRecord(fork, s);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(side, fork, 0);
+  if (err == cudaSuccess) err = launch_pad_rows(a.x_disp, H, a.offsets, pad, E, L.npad, xP, side);
+  if (err == cudaSuccess) err = launch_pad_rows(a.dout, H, a.offsets, pad, E, L.npad, doutP, side);
+  if (err == cudaSuccess) err = cudaEventRecord(join, side);
+  // destroying them now is legal: their resources go once the work is done
+  cudaStreamDestroy(side);
+  if (fork) cudaEventDestroy(fork);
+  struct EventGuard {
+    cudaEvent_t e;
+    ~EventGuard() {
+      if (e) cudaEventDestroy(e);
+    }
+  } join_guard{join};
+  if (err != cudaSuccess) return err;
   const bool pair = N >= (int64_t)BM * E;
   Params base{};
   base.offsets = a.offsets;
@@ -1127,9 +1150,8 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   p.nb = (int)((H + 255) / 256);
   p.out = a.dinput;
   MOE_TC_TRY(launch_any<T>(pair, N, E, mDgduP, mWgMN, mWuMN, p, num_sms, s));
-  // 4-5. weight gradients over the padded rows
-  MOE_TC_TRY(launch_pad_rows(a.x_disp, H, a.offsets, pad, E, L.npad, xP, s));
-  MOE_TC_TRY(launch_pad_rows(a.dout, H, a.offsets, pad, E, L.npad, doutP, s));
+  // 4-5. weight gradients over the padded rows (after the side stream's copies)
+  MOE_TC_TRY(cudaStreamWaitEvent(s, join, 0));
   constexpr int TM = Cfg<2>::TILE_M;
   p = base;
   p.mode = kWgrad;
