@@ -441,10 +441,17 @@ def run_native(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = _host_inputs(wl)
         rate, n, dt, threads = oracle_sample_rate(wl, host, args.cpu_seconds)
+        # the same oracle on one thread, on a smaller sample (a few seconds)
+        import oracle
+        oracle.set_threads(1)
+        rate1, n1, dt1, _ = oracle_sample_rate(wl, host, min(5.0, args.cpu_seconds / 3))
+        oracle.set_threads(threads)
         line["cpu_baseline"] = {
             "value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": (f"{n} tokens of {wl.name} through the FP64 oracle (route + {wl.top_k} SwiGLU "
-                       f"experts + weighted sum per token) in {dt:.1f} s")}
+                       f"experts + weighted sum per token) in {dt:.1f} s"),
+            "value_1thread": rate1,
+            "sample_1thread": f"{n1} tokens in {dt1:.1f} s on one thread"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
