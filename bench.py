@@ -36,8 +36,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch of the gate/up GEMM on the headline workload, from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel source it was taken on; reported as null once the source changes.
-GATEUP_TRAFFIC = {"workload": "finegrained_bf16", "bytes": 1144104448 + 264506624,
-                  "source_sha256": "263205887871ce899edf3b01805866d81d61406be4054f50a3452674ec181cb5"}
+GATEUP_TRAFFIC = {"workload": "finegrained_bf16", "bytes": 1143149056 + 265082880,
+                  "source_sha256": "5d38c46729a5e4199f9f5589b4ed04d4f0982055f907a609ee50742dd5c83375"}
 
 
 def parse_args(argv=None):
