@@ -38,6 +38,7 @@ BWD_CASES = [
     (200, 16, 4, 128, 96, "f16"),
     (64, 1, 1, 64, 64, "bf16"),
     (1500, 4, 2, 320, 704, "bf16"),  # 750 rows per expert: CTA-pair tiles, several m-tiles
+    (200, 256, 8, 128, 64, "bf16"),  # decode-like: single-CTA tiles, many empty experts
 ]
 
 

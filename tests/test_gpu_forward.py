@@ -54,6 +54,7 @@ def _check_routing_and_dispatch(experts, ws, wl, logits):
     # >= 128 rows per expert: the gate/up product gathers the token rows itself
     (1000, 4, 2, 200, 136, "bf16", True),   # H = 3*64 + 8: a one-chunk k-block tail
     (700, 3, 3, 72, 64, "f16", False),      # H = 64 + 8
+    (300, 1024, 8, 64, 64, "bf16", True),   # E at its limit: 8 KiB of per-expert tables in shared memory
 ])
 def test_forward_small_all_tokens(cuda_lib, T, E, k, H, I, dtype, renorm):
     wl = small_workload(T, E, k, H, I, dtype=dtype, renormalize=renorm, seed=T + E)
