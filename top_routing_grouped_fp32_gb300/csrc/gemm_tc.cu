@@ -323,8 +323,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+// An empty statement that the compiler must treat as rewriting r: placed after
+// a wait, it keeps every use of r after that wait.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                 "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
+                 "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+                 "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
+                 "+r"(r[31]));
+}
+// The same wait, naming the registers of a load still in flight as operands so
+// that no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+        "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+        "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+        "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
 }
 
 // ---------------------------------------------------------------- epilogue stores
@@ -700,7 +721,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           uint32_t g[32], u[32];
           tmem_ld32(taddr + c, g);
           tmem_ld32(taddr + 128 + c, u);
-          tmem_wait_ld();
+          tmem_wait_ld(g);
+          reg_fence(u);
           if (row_ok) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -760,7 +782,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           uint32_t g[32], u[32], wdg[16], wdu[16], wa[16];
           tmem_ld32(taddr + c, g);
           tmem_ld32(taddr + 128 + c, u);
-          tmem_wait_ld();
+          tmem_wait_ld(g);
+          reg_fence(u);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             float fdg[8], fdu[8], fa[8];
@@ -806,26 +829,41 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         }
         uint32_t* rowp = reinterpret_cast<uint32_t*>(rowf);
         const bool empty = p.mode == kWgrad && t.nk == 0;
-#pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          uint32_t o[32];
-          if (!empty) {
-            tmem_ld32(taddr + c, o);
-            tmem_wait_ld();
-          } else {
+        if (empty) {
+          uint32_t z[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll 1
+          for (int c = 0; c < 256; c += 32)
+            staged_store<32>(stg, z, rowp ? rowp + c : nullptr, valid_words<float>(p.n_out - col0 - c), lane);
+        } else {
+          // the next 32 columns are read from TMEM while this chunk is stored
+          uint32_t ob[2][32];
+          tmem_ld32(taddr, ob[0]);
+          tmem_wait_ld(ob[0]);
+#pragma unroll
+          for (int ci = 0; ci < 8; ++ci) {
+            const int c = ci * 32;
+            if (ci + 1 < 8) tmem_ld32(taddr + c + 32, ob[(ci + 1) & 1]);
+            staged_store<32>(stg, ob[ci & 1], rowp ? rowp + c : nullptr,
+                             valid_words<float>(p.n_out - col0 - c), lane);
+            if (ci + 1 < 8) tmem_wait_ld(ob[(ci + 1) & 1]);
           }
-          staged_store<32>(stg, o, rowp ? rowp + c : nullptr, valid_words<float>(p.n_out - col0 - c), lane);
         }
       } else {
+        // the next 32 columns are read from TMEM while this chunk is scaled,
+        // packed and stored
         const int64_t col0 = (int64_t)t.nb * 256;
         uint32_t* rowp = row_ok ? reinterpret_cast<uint32_t*>(out + wslot * p.n_out + col0) : nullptr;
-#pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          uint32_t o[32], w[16];
-          tmem_ld32(taddr + c, o);
-          tmem_wait_ld();
+        uint32_t ob[2][32];
+        tmem_ld32(taddr, ob[0]);
+        tmem_wait_ld(ob[0]);
+#pragma unroll
+        for (int ci = 0; ci < 8; ++ci) {
+          const int c = ci * 32;
+          if (ci + 1 < 8) tmem_ld32(taddr + c + 32, ob[(ci + 1) & 1]);
+          const uint32_t* o = ob[ci & 1];
+          uint32_t w[16];
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             float f[8];
@@ -834,6 +872,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
             put4(w + 4 * v, pack8<T>(f));
           }
           staged_store<16>(stg, w, rowp ? rowp + c / 2 : nullptr, valid_words<T>(p.n_out - col0 - c), lane);
+          if (ci + 1 < 8) tmem_wait_ld(ob[(ci + 1) & 1]);
         }
       }
       tc_fence_before();
