@@ -1125,20 +1125,30 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   MOE_TC_TRY(launch_pad_offsets(a.offsets, E, pad, s));
   // x and dout into the padded row space on a side stream: they are needed
   // only by products 4 and 5 and co-run with products 1-3 (whose CTAs leave
-  // registers and threads free on every SM)
+  // registers and threads free on every SM).  While `s` is being captured
+  // into a CUDA graph they run on `s` itself (no per-call stream then).
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  MOE_TC_TRY(cudaStreamIsCapturing(s, &capture));
+  if (capture != cudaStreamCaptureStatusNone) {
+    MOE_TC_TRY(launch_pad_rows(a.x_disp, H, a.offsets, pad, E, L.npad, xP, s));
+    MOE_TC_TRY(launch_pad_rows(a.dout, H, a.offsets, pad, E, L.npad, doutP, s));
+  }
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
-  MOE_TC_TRY(cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking));
-  err = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
-  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
-  if (err == cudaSuccess) err = cudaEventRecord(fork, s);
-  if (err == cudaSuccess) err = cudaStreamWaitEvent(side, fork, 0);
-  if (err == cudaSuccess) err = launch_pad_rows(a.x_disp, H, a.offsets, pad, E, L.npad, xP, side);
-  if (err == cudaSuccess) err = launch_pad_rows(a.dout, H, a.offsets, pad, E, L.npad, doutP, side);
-  if (err == cudaSuccess) err = cudaEventRecord(join, side);
-  // destroying them now is legal: their resources go once the work is done
-  cudaStreamDestroy(side);
-  if (fork) cudaEventDestroy(fork);
+  if (capture == cudaStreamCaptureStatusNone)
+    MOE_TC_TRY(cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking));
+  if (side) {
+    err = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+    if (err == cudaSuccess) err = cudaEventRecord(fork, s);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(side, fork, 0);
+    if (err == cudaSuccess) err = launch_pad_rows(a.x_disp, H, a.offsets, pad, E, L.npad, xP, side);
+    if (err == cudaSuccess) err = launch_pad_rows(a.dout, H, a.offsets, pad, E, L.npad, doutP, side);
+    if (err == cudaSuccess) err = cudaEventRecord(join, side);
+    // destroying them now is legal: their resources go once the work is done
+    cudaStreamDestroy(side);
+    if (fork) cudaEventDestroy(fork);
+  }
   struct EventGuard {
     cudaEvent_t e;
     ~EventGuard() {
@@ -1190,7 +1200,7 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   p.out = a.dinput;
   MOE_TC_TRY(launch_any<T>(pair, N, E, mDgduP, mWgMN, mWuMN, p, num_sms, s));
   // 4-5. weight gradients over the padded rows (after the side stream's copies)
-  MOE_TC_TRY(cudaStreamWaitEvent(s, join, 0));
+  if (join) MOE_TC_TRY(cudaStreamWaitEvent(s, join, 0));
   constexpr int TM = Cfg<2>::TILE_M;
   p = base;
   p.mode = kWgrad;
