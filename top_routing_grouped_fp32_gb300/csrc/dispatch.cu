@@ -74,38 +74,64 @@ __device__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* warp_sums) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t warp_inclusive_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t o = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v += o;
+  }
+  return v;
+}
+
+// One block of 1024 threads (32 warps).  Each warp owns experts w, w+32, ...
+// and walks their chunk columns 32 chunks at a time, so the per-expert chunk
+// loops are parallel over lanes (they were the latency of this kernel).
 __global__ void __launch_bounds__(1024)
 scan_kernel(const uint32_t* __restrict__ chunk_counts, int nchunks, int E, int64_t N,
             uint32_t* __restrict__ offsets, uint32_t* __restrict__ chunk_base,
             uint32_t* __restrict__ perm, uint32_t* __restrict__ row_experts,
             uint32_t* __restrict__ status) {
   __shared__ uint32_t warp_sums[32];
+  __shared__ uint32_t s_tot[1025];  // per-expert totals, then segment starts; [E] = invalid
   __shared__ uint32_t s_total_valid;
-  // E <= 1024 = blockDim.x: thread e owns expert e
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  // 1. totals per expert (and of the invalid column E)
+  for (int e = w; e <= E; e += 32) {
+    uint32_t sum = 0;
+    for (int b = lane; b < nchunks; b += 32) sum += chunk_counts[(size_t)b * (E + 1) + e];
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+    if (lane == 0) s_tot[e] = sum;
+  }
+  __syncthreads();
+  // 2. exclusive scan of the totals: segment starts (thread e owns expert e)
   const int e = threadIdx.x;
-  uint32_t total = 0;
-  if (e < E)
-    for (int b = 0; b < nchunks; ++b) total += chunk_counts[(size_t)b * (E + 1) + e];
+  const uint32_t total = e < E ? s_tot[e] : 0u;
+  const uint32_t invalid = s_tot[E];
   const uint32_t incl = block_inclusive_scan(total, warp_sums);
   if (e < E) {
-    const uint32_t start = incl - total;
-    offsets[e] = start;
-    uint32_t run = start;
-    for (int b = 0; b < nchunks; ++b) {
-      chunk_base[(size_t)b * E + e] = run;
-      run += chunk_counts[(size_t)b * (E + 1) + e];
-    }
+    s_tot[e] = incl - total;
+    offsets[e] = incl - total;
     if (e == E - 1) {
       offsets[E] = incl;
       s_total_valid = incl;
     }
   }
-  if (threadIdx.x == 0) {  // column E counts indices >= E
-    uint32_t invalid = 0;
-    for (int b = 0; b < nchunks; ++b) invalid += chunk_counts[(size_t)b * (E + 1) + E];
-    if (status) *status = invalid ? (uint32_t)MOE_ERR_INVALID_INDEX : 0u;
-  }
+  if (threadIdx.x == 0 && status) *status = invalid ? (uint32_t)MOE_ERR_INVALID_INDEX : 0u;
   __syncthreads();
+  // 3. first row of every (chunk, expert): the segment start plus the
+  //    expert's counts in earlier chunks
+  for (int ex = w; ex < E; ex += 32) {
+    uint32_t run = s_tot[ex];
+    for (int b0 = 0; b0 < nchunks; b0 += 32) {
+      const int b = b0 + lane;
+      const uint32_t c = b < nchunks ? chunk_counts[(size_t)b * (E + 1) + ex] : 0u;
+      const uint32_t x = warp_inclusive_scan(c);
+      if (b < nchunks) chunk_base[(size_t)b * E + ex] = run + x - c;
+      run += __shfl_sync(0xffffffffu, x, 31);
+    }
+  }
   // slots that were not dispatched leave the tail of perm / row_experts unused
   for (int64_t r = (int64_t)s_total_valid + threadIdx.x; r < N; r += blockDim.x) {
     perm[r] = kInvalid;
@@ -118,11 +144,17 @@ scatter_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
                const uint32_t* __restrict__ chunk_base, uint32_t* __restrict__ perm,
                uint32_t* __restrict__ row_experts) {
   extern __shared__ uint32_t smem[];
-  uint32_t* wcnt = smem;  // [kWarps][E]: per-warp counters / running bases
+  uint32_t* wcnt = smem;                 // [kWarps][E]: per-warp counters / running bases
+  uint32_t* sidx = smem + kWarps * E;    // this chunk's idx slice, [tokens][k]
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) wcnt[i] = 0;
+  // one coalesced load of the chunk's indices; the walks below read them from
+  // shared memory instead of issuing a dependent L2 load per token
+  const int64_t tc0 = (int64_t)blockIdx.x * kDispatchChunk;
+  const int64_t nslots = (min(T, tc0 + kDispatchChunk) - tc0) * k;
+  for (int64_t i = threadIdx.x; i < nslots; i += blockDim.x) sidx[i] = __ldg(idx + tc0 * k + i);
   __syncthreads();
-  const int64_t tw = (int64_t)blockIdx.x * kDispatchChunk + w * 32;
+  const int64_t tw = tc0 + w * 32;
   uint32_t* my = wcnt + w * E;
   const uint32_t lt_mask = (1u << lane) - 1u;
 
@@ -132,7 +164,7 @@ scatter_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
     if (t >= T) break;
     for (int j0 = 0; j0 < k; j0 += 32) {
       const int j = j0 + lane;
-      const uint32_t e = j < k ? __ldg(idx + t * k + j) : kInvalid;
+      const uint32_t e = j < k ? sidx[(t - tc0) * k + j] : kInvalid;
       const bool ok = e < (uint32_t)E;
       const uint32_t key = ok ? e : kInvalid;
       const uint32_t grp = __match_any_sync(0xffffffffu, key);
@@ -157,7 +189,7 @@ scatter_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
     if (t >= T) break;
     for (int j0 = 0; j0 < k; j0 += 32) {
       const int j = j0 + lane;
-      const uint32_t e = j < k ? __ldg(idx + t * k + j) : kInvalid;
+      const uint32_t e = j < k ? sidx[(t - tc0) * k + j] : kInvalid;
       const bool ok = e < (uint32_t)E;
       const uint32_t key = ok ? e : kInvalid;
       const uint32_t grp = __match_any_sync(0xffffffffu, key);
@@ -227,7 +259,12 @@ cudaError_t launch_dispatch(const uint32_t* idx, int64_t T, int E, int k, uint32
                                                 align_up((size_t)nc * (E + 1) * 4, 256));
   count_kernel<<<(unsigned)nc, 256, (E + 1) * sizeof(uint32_t), s>>>(idx, T, E, k, counts);
   scan_kernel<<<1, 1024, 0, s>>>(counts, (int)nc, E, T * k, offsets, bases, perm, row_experts, status);
-  const size_t smem = (size_t)kWarps * E * sizeof(uint32_t);
+  const size_t smem = ((size_t)kWarps * E + (size_t)kDispatchChunk * k) * sizeof(uint32_t);
+  if (smem > 48 * 1024) {  // large E * k (at most 8*1024 + 256*64 words = 96 KiB): opt in
+    const cudaError_t e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
+    if (e != cudaSuccess) return e;
+  }
   scatter_kernel<<<(unsigned)nc, 256, smem, s>>>(idx, T, E, k, bases, perm, row_experts);
   return cudaGetLastError();
 }
