@@ -57,6 +57,8 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const T* __restrict__ src, const uint32_t* __restrict__ slot_row,
                const void* __restrict__ w, int wdt, int64_t T_rows, int k, int64_t H,
                T* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int C = VEC ? 8 : 1;
   const int64_t groups = H / C;
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -105,12 +107,10 @@ cudaError_t launch_combine_t(const void* src, const uint32_t* slot_row, const vo
   const int64_t work = T_rows * (vec ? H / 8 : H);
   const unsigned grid = (unsigned)((work + 255) / 256);
   if (vec)
-    combine_kernel<T, WEIGHTED, true><<<grid, 256, 0, s>>>(
-        static_cast<const T*>(src), slot_row, w, (int)wdt, T_rows, k, H, static_cast<T*>(y));
-  else
-    combine_kernel<T, WEIGHTED, false><<<grid, 256, 0, s>>>(
-        static_cast<const T*>(src), slot_row, w, (int)wdt, T_rows, k, H, static_cast<T*>(y));
-  return cudaGetLastError();
+    return launch_pdl(combine_kernel<T, WEIGHTED, true>, dim3(grid), dim3(256), 0, s,
+                      static_cast<const T*>(src), slot_row, w, (int)wdt, T_rows, k, H, static_cast<T*>(y));
+  return launch_pdl(combine_kernel<T, WEIGHTED, false>, dim3(grid), dim3(256), 0, s,
+                    static_cast<const T*>(src), slot_row, w, (int)wdt, T_rows, k, H, static_cast<T*>(y));
 }
 
 // Combine backward (user guide, section 12: combine_backward gives dexpert and

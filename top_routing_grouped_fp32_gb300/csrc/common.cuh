@@ -35,6 +35,35 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
   return __float2bfloat16_rn(v);
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// Kernels of a call sequence are launched with programmatic stream
+// serialisation: a kernel may be launched (and run its prologue) before its
+// predecessor in the stream has finished.  pdl_wait() blocks until every
+// predecessor grid has completed and its memory is visible, so each kernel
+// calls it before its first read of anything a predecessor wrote;
+// pdl_trigger() lets the successor be launched once every CTA of this grid has
+// started.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Reads element i of a weights array whose dtype is only known at run time.
 __device__ __forceinline__ float load_dyn(const void* p, int dtype, size_t i) {
   if (dtype == MOE_F32) return static_cast<const float*>(p)[i];

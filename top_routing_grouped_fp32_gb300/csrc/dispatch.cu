@@ -33,6 +33,8 @@ constexpr int kWarps = kDispatchChunk / 32;  // 8 warps, 32 tokens each
 __global__ void __launch_bounds__(256)
 count_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
              uint32_t* __restrict__ chunk_counts) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t cnt[];  // E + 1
   for (int i = threadIdx.x; i <= E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
@@ -92,6 +94,8 @@ scan_kernel(const uint32_t* __restrict__ chunk_counts, int nchunks, int E, int64
             uint32_t* __restrict__ offsets, uint32_t* __restrict__ chunk_base,
             uint32_t* __restrict__ perm, uint32_t* __restrict__ row_experts,
             uint32_t* __restrict__ status) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint32_t warp_sums[32];
   __shared__ uint32_t s_tot[1025];  // per-expert totals, then segment starts; [E] = invalid
   __shared__ uint32_t s_total_valid;
@@ -143,6 +147,8 @@ __global__ void __launch_bounds__(256)
 scatter_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
                const uint32_t* __restrict__ chunk_base, uint32_t* __restrict__ perm,
                uint32_t* __restrict__ row_experts) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t smem[];
   uint32_t* wcnt = smem;                 // [kWarps][E]: per-warp counters / running bases
   uint32_t* sidx = smem + kWarps * E;    // this chunk's idx slice, [tokens][k]
@@ -211,6 +217,8 @@ template <int VEC_BYTES>
 __global__ void __launch_bounds__(256)
 gather_kernel(const char* __restrict__ x, int64_t row_bytes, int k, const uint32_t* __restrict__ perm,
               const uint32_t* __restrict__ offsets, int E, int64_t N, char* __restrict__ x_disp) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (r >= N) return;
@@ -257,16 +265,20 @@ cudaError_t launch_dispatch(const uint32_t* idx, int64_t T, int E, int k, uint32
   uint32_t* counts = static_cast<uint32_t*>(scratch);
   uint32_t* bases = reinterpret_cast<uint32_t*>(static_cast<char*>(scratch) +
                                                 align_up((size_t)nc * (E + 1) * 4, 256));
-  count_kernel<<<(unsigned)nc, 256, (E + 1) * sizeof(uint32_t), s>>>(idx, T, E, k, counts);
-  scan_kernel<<<1, 1024, 0, s>>>(counts, (int)nc, E, T * k, offsets, bases, perm, row_experts, status);
+  cudaError_t err = launch_pdl(count_kernel, dim3((unsigned)nc), dim3(256), (E + 1) * sizeof(uint32_t), s,
+                               idx, T, E, k, counts);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, counts, (int)nc, E, T * k, offsets, bases,
+                   perm, row_experts, status);
+  if (err != cudaSuccess) return err;
   const size_t smem = ((size_t)kWarps * E + (size_t)kDispatchChunk * k) * sizeof(uint32_t);
   if (smem > 48 * 1024) {  // large E * k (at most 8*1024 + 256*64 words = 96 KiB): opt in
     const cudaError_t e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)smem);
     if (e != cudaSuccess) return e;
   }
-  scatter_kernel<<<(unsigned)nc, 256, smem, s>>>(idx, T, E, k, bases, perm, row_experts);
-  return cudaGetLastError();
+  return launch_pdl(scatter_kernel, dim3((unsigned)nc), dim3(256), smem, s, idx, T, E, k, bases, perm,
+                    row_experts);
 }
 
 cudaError_t launch_gather(const void* x, moe_dtype dt, int64_t H, int k, const uint32_t* perm,
@@ -276,12 +288,10 @@ cudaError_t launch_gather(const void* x, moe_dtype dt, int64_t H, int k, const u
   const bool vec = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
                    reinterpret_cast<uintptr_t>(x_disp) % 16 == 0;
   if (vec)
-    gather_kernel<16><<<grid, 256, 0, s>>>(static_cast<const char*>(x), row_bytes, k, perm, offsets,
-                                           E, N, static_cast<char*>(x_disp));
-  else
-    gather_kernel<2><<<grid, 256, 0, s>>>(static_cast<const char*>(x), row_bytes, k, perm, offsets,
-                                          E, N, static_cast<char*>(x_disp));
-  return cudaGetLastError();
+    return launch_pdl(gather_kernel<16>, dim3(grid), dim3(256), 0, s, static_cast<const char*>(x),
+                      row_bytes, k, perm, offsets, E, N, static_cast<char*>(x_disp));
+  return launch_pdl(gather_kernel<2>, dim3(grid), dim3(256), 0, s, static_cast<const char*>(x),
+                    row_bytes, k, perm, offsets, E, N, static_cast<char*>(x_disp));
 }
 
 

@@ -524,6 +524,10 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     prefetch_map(&mapB1);
   }
   if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), TMEM_COLS);
+  // everything above overlaps the predecessor kernel (programmatic launch);
+  // from here on the kernel reads what earlier kernels wrote
+  pdl_wait();
+  pdl_trigger();
   for (int i = threadIdx.x; i <= E; i += THREADS) s_off[i] = p.offsets[i];
   __syncthreads();
   if (warp == 2) {  // s_pref[e] = number of (128*PAIR)-row tiles of experts < e
@@ -1016,17 +1020,19 @@ cudaError_t launch_t(int64_t N, int E, const CUtensorMap& mA, const CUtensorMap&
   const int64_t mt_per_expert = std::max<int64_t>(1, (N + (int64_t)TM * E - 1) / ((int64_t)TM * E));
   p.panel = (int)std::max<int64_t>(1, std::min<int64_t>(p.nb, (nclu + mt_per_expert - 1) / mt_per_expert));
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(nclu * PAIR);
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem_bytes<PAIR>(E);
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_tc<T, PAIR>, mA, mB0, mB1, p);
 }
 

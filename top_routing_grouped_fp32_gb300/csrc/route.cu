@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
 route_kernel(const T* __restrict__ logits, int64_t T_rows, int E, int k, int renorm,
              uint32_t* __restrict__ idx, T* __restrict__ w_out, float* __restrict__ w32,
              uint32_t* status_reset) {
+  pdl_wait();
+  pdl_trigger();
   if (status_reset && blockIdx.x == 0 && threadIdx.x == 0) *status_reset = 0u;
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
@@ -164,8 +166,10 @@ cudaError_t launch_typed(const void* logits, int64_t T_rows, int E, int k, int r
   dim3 block(32 * kRowsPerBlock);
   const T* l = static_cast<const T*>(logits);
   T* w = static_cast<T*>(weights);
+  cudaError_t err = cudaSuccess;
 #define MOE_ROUTE_CASE(V)                                                                     \
-  route_kernel<T, V><<<grid, block, 0, s>>>(l, T_rows, E, k, renorm, idx, w, w32, status_reset); \
+  err = launch_pdl(route_kernel<T, V>, grid, block, 0, s, l, T_rows, E, k, renorm, idx, w, w32,  \
+                   status_reset);                                                              \
   break;
   switch ((E + 31) / 32 <= 1 ? 1 : (E + 31) / 32 <= 2 ? 2 : (E + 31) / 32 <= 4 ? 4
           : (E + 31) / 32 <= 8 ? 8 : (E + 31) / 32 <= 16 ? 16 : 32) {
@@ -177,7 +181,7 @@ cudaError_t launch_typed(const void* logits, int64_t T_rows, int E, int k, int r
     default: MOE_ROUTE_CASE(32)
   }
 #undef MOE_ROUTE_CASE
-  return cudaGetLastError();
+  return err;
 }
 
 // ---------------------------------------------------------------------------
