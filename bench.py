@@ -36,8 +36,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch of the gate/up GEMM on the headline workload, from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel source it was taken on; reported as null once the source changes.
-GATEUP_TRAFFIC = {"workload": "finegrained_bf16", "bytes": 1141404416 + 264623360,
-                  "source_sha256": "83920829675bcfa3a0731907e70b6f485b1f0ee4baf5b4835d682f7a95d0a2c8"}
+GATEUP_TRAFFIC = {"workload": "finegrained_bf16", "bytes": 1164290560 + 266119936,
+                  "source_sha256": "c1e5727f659c3cf278d10bc14495b7c2bcb7e0927e9f1aaed48cf3119b4ef652"}
 
 
 def parse_args(argv=None):
