@@ -55,7 +55,9 @@ def parse_args(argv=None):
                    help="store the workload in this dtype instead of its own")
     p.add_argument("--tokens", type=int, default=None,
                    help="override the workload's token count (small cases for profiler captures)")
-    p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--e2e-steps", type=int, default=None,
+                   help="steps of the host-buffer legs (default: --steps, so that they run as long "
+                        "as the device-resident loop and see the same power-capped clocks)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target wall time of the oracle sample")
@@ -337,7 +339,7 @@ def run_native(args, rank, world, local):
     xh = [inp["x"].cpu().pin_memory() for _ in range(2)]
     lh = [inp["logits"].cpu().pin_memory() for _ in range(2)]
     yh = [torch.empty((wl.T, wl.H), dtype=inp["x"].dtype).pin_memory() for _ in range(2)]
-    Ke = max(1, args.e2e_steps)
+    Ke = max(1, args.e2e_steps if args.e2e_steps is not None else K)
     pipe = experts.host_pipeline(wl.T, wl.top_k, wl.renormalize, logits_dtype=inp["logits"].dtype,
                                  depth=2, stream=stream)
     for i in range(3):
