@@ -36,6 +36,10 @@ MUTATIONS = {
     "router_renorm_sign": ("c[m] = renorm ? scale * (dw[t * k + m] / Q - gq / (Q * Q)) : scale * dw[t * k + m];",
                            "c[m] = renorm ? scale * (dw[t * k + m] / Q + gq / (Q * Q)) : scale * dw[t * k + m];"),
     "combine_backward_unweighted": ("dexpert[r * H + h] = w[s] * dy[t * H + h];", "dexpert[r * H + h] = dy[t * H + h];"),
+    "dup_weight_grad_without_silu": ("const double cg = d * uu * silu_grad(gg), cu = d * silu(gg);",
+                                     "const double cg = d * uu * silu_grad(gg), cu = d * uu;"),
+    "ddown_weight_grad_without_up": ("sd[i] += dd * sl[r * I + i] * u[r * I + i];",
+                                     "sd[i] += dd * sl[r * I + i];"),
 }
 
 
