@@ -189,3 +189,17 @@ def test_sigmoid_group_option_rules(lib, E, opt, want):
     st = lib.moe_route_sigmoid_grouped(None, BF16, 0, E, None, ctypes.byref(o), None, None, None, None)
     assert st == want, _msg(lib)
     assert lib.moe_route_sigmoid_grouped(FAKE, BF16, 4, E, None, None, FAKE, FAKE, None, None) == INVALID_ARG
+
+
+def test_host_pipeline_and_backward_null_rules(lib):
+    """The host pipeline and the backward entry points reject null handles and
+    bad arguments on the host; destroying a null pipeline is a no-op."""
+    out = ctypes.c_void_p()
+    assert lib.moe_host_pipeline_workspace_size(None, 16, 2, BF16, 2) == 0
+    assert lib.moe_host_pipeline_create(None, 16, 2, BF16, 1, 2, None, 0, None, ctypes.byref(out)) == INVALID_ARG
+    assert lib.moe_host_pipeline_submit(None, None, None, None, 4) == INVALID_ARG
+    assert lib.moe_host_pipeline_sync(None) == INVALID_ARG
+    assert lib.moe_host_pipeline_destroy(None) == OK
+    assert lib.moe_experts_backward_workspace_size(None, 16) == 0
+    assert lib.moe_experts_backward_with_strategy(None, None, 4, None, None, None, None, None, None, 2,
+                                                  None, 0, None) == INVALID_ARG
