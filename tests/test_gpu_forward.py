@@ -55,6 +55,8 @@ def _check_routing_and_dispatch(experts, ws, wl, logits):
     (1000, 4, 2, 200, 136, "bf16", True),   # H = 3*64 + 8: a one-chunk k-block tail
     (700, 3, 3, 72, 64, "f16", False),      # H = 64 + 8
     (300, 1024, 8, 64, 64, "bf16", True),   # E at its limit: 8 KiB of per-expert tables in shared memory
+    (64, 256, 64, 64, 64, "bf16", True),    # top_k at its limit: two 32-slot groups per token in the scatter
+    (50, 4, 2, 8, 16, "bf16", False),       # the smallest tcgen05 shapes: one k-block, 8 of 64 columns
 ])
 def test_forward_small_all_tokens(cuda_lib, T, E, k, H, I, dtype, renorm):
     wl = small_workload(T, E, k, H, I, dtype=dtype, renormalize=renorm, seed=T + E)
