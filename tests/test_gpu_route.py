@@ -46,7 +46,11 @@ def test_route_workloads(cuda_lib, name):
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("T,E,k", [(1, 1, 1), (33, 37, 5), (257, 100, 33), (64, 1024, 64),
-                                   (16, 64, 64), (500, 256, 8), (7, 2, 2), (130, 160, 3)])
+                                   (16, 64, 64), (500, 256, 8), (7, 2, 2), (130, 160, 3),
+                                   # every lanes-per-row / values-per-lane form, T not a
+                                   # multiple of the rows per block
+                                   (77, 8, 8), (99, 16, 16), (101, 30, 7), (45, 512, 20),
+                                   (33, 128, 64)])
 @pytest.mark.parametrize("renorm", [False, True])
 def test_route_shapes_and_dtypes(cuda_lib, dtype, T, E, k, renorm):
     logits = make_routing_logits(T, E, dtype, seed=T * 7 + E, device="cuda")

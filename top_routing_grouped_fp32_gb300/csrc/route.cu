@@ -1,4 +1,4 @@
-// route.cu -- softmax / top-k routing, one warp per token row.
+// route.cu -- softmax / top-k routing, 8 to 32 lanes per token row.
 //
 // Implements the routing contract of the ruDNN user guide ("ruDNN
 // Benutzerhandbuch"), section 4 "Routing-Vertrag": softmax over all experts in
@@ -15,11 +15,13 @@
 //  * renormalisation divides by the FP32 sum of the k selected values added
 //    in slot order; weights are always stored in the logits dtype.
 //
-// Design: a row of E <= 1024 logits is held in registers, VPL = E/32 values
-// per lane in a blocked layout (lane l owns experts l*VPL .. l*VPL+VPL-1) so
-// that each lane reads its share with one or a few vector loads.  Max, sum and
-// each of the k arg-max rounds are warp butterflies; a butterfly leaves the
-// bit-identical value in every lane, so every lane agrees on each winner.
+// Design: a row of E <= 1024 logits is held in registers by LPR lanes (8 for
+// E <= 64, 16 for E <= 128, else 32), VPL values per lane in a blocked layout
+// (lane l owns experts l*VPL .. l*VPL+VPL-1) so that each lane reads its share
+// with one or a few vector loads; a warp routes 32/LPR rows at once.  Max,
+// sum and each of the k arg-max rounds are butterflies over the row's lanes;
+// a butterfly leaves the bit-identical value in every lane, so every lane
+// agrees on each winner.
 #include <math.h>
 
 #include "common.cuh"
@@ -66,7 +68,10 @@ __device__ __forceinline__ void load_row(const T* row, int E, int lane, float (&
   }
 }
 
-template <typename T, int VPL>
+// LPR lanes per row (8, 16 or 32), so that a warp routes 32 / LPR rows at
+// once: for E <= 64 one warp instruction serves four rows, and each butterfly
+// has three steps instead of five.
+template <typename T, int LPR, int VPL>
 __global__ void __launch_bounds__(32 * kRowsPerBlock)
 route_kernel(const T* __restrict__ logits, int64_t T_rows, int E, int k, int renorm,
              uint32_t* __restrict__ idx, T* __restrict__ w_out, float* __restrict__ w32,
@@ -74,49 +79,55 @@ route_kernel(const T* __restrict__ logits, int64_t T_rows, int E, int k, int ren
   pdl_wait();
   pdl_trigger();
   if (status_reset && blockIdx.x == 0 && threadIdx.x == 0) *status_reset = 0u;
+  constexpr int R = 32 / LPR;                 // rows per warp
+  constexpr int SLOTS = (64 + LPR - 1) / LPR;  // slots one lane may own (top_k <= 64)
   const int lane = threadIdx.x & 31;
-  const int64_t t = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-  if (t >= T_rows) return;
+  const int sub = lane % LPR;                 // lane within its row's segment
+  const int64_t t = ((int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5)) * R + lane / LPR;
+  const bool live = t < T_rows;               // the whole warp stays for the shuffles
 
   float v[VPL];
-  load_row<T, VPL>(logits + t * E, E, lane, v);
-  const int e0 = lane * VPL;
+  if (live) {
+    load_row<T, VPL>(logits + t * E, E, sub, v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) v[i] = -INFINITY;
+  }
+  const int e0 = sub * VPL;
 
   // poisoned-row detection and the row maximum (padding entries excluded)
   float m = -INFINITY;
-  bool nan_or_pinf = false;
+  int bad = 0;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     if (e0 + i < E) {
-      nan_or_pinf |= isnan(v[i]) || v[i] == INFINITY;
+      bad |= (isnan(v[i]) || v[i] == INFINITY) ? 1 : 0;
       m = fmaxf(m, v[i]);
     }
   }
-  const bool poisoned = __any_sync(0xffffffffu, nan_or_pinf);
 #pragma unroll
-  for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-
-  if (poisoned || m == -INFINITY) {
-    for (int j = lane; j < k; j += 32) {
-      idx[t * k + j] = (uint32_t)j;
-      w_out[t * k + j] = from_f32<T>(NAN);
-      if (w32) w32[t * k + j] = NAN;
-    }
-    return;
+  for (int d = LPR / 2; d > 0; d >>= 1) {
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d, LPR));
+    bad |= __shfl_xor_sync(0xffffffffu, bad, d, LPR);
   }
+  const bool dead = bad != 0 || m == -INFINITY;  // poisoned (or past the end)
 
   // FP32 softmax denominator: per-lane sum, then a butterfly
   float s = 0.f;
+  if (!dead) {
 #pragma unroll
-  for (int i = 0; i < VPL; ++i)
-    if (e0 + i < E) s += expf(v[i] - m);
+    for (int i = 0; i < VPL; ++i)
+      if (e0 + i < E) s += expf(v[i] - m);
+  }
 #pragma unroll
-  for (int d = 16; d > 0; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d);
+  for (int d = LPR / 2; d > 0; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d, LPR);
 
   // k rounds of arg-max over the not-yet-selected experts
   uint32_t taken = 0;  // bit i: expert e0+i already selected
-  uint32_t my_idx[2] = {0, 0};
-  float my_p[2] = {0.f, 0.f};
+  uint32_t my_idx[SLOTS];
+  float my_p[SLOTS];
+#pragma unroll
+  for (int h = 0; h < SLOTS; ++h) my_idx[h] = 0u, my_p[h] = 0.f;
   float sel_sum = 0.f;
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
@@ -129,26 +140,37 @@ route_kernel(const T* __restrict__ logits, int64_t T_rows, int E, int k, int ren
       }
     }
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+    for (int d = LPR / 2; d > 0; d >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, d, LPR);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, d, LPR);
       if (beats(ov, oi, bv, bi)) {
         bv = ov;
         bi = oi;
       }
     }
-    if (bi / VPL == lane) taken |= 1u << (bi % VPL);
-    const float p = expf(bv - m) / s;
+    if (bi / VPL == sub) taken |= 1u << (bi % VPL);
+    const float p = dead ? 0.f : expf(bv - m) / s;
     sel_sum += p;  // every lane adds in slot order
-    if ((j & 31) == lane) {
-      my_idx[j >> 5] = (uint32_t)bi;
-      my_p[j >> 5] = p;
+#pragma unroll
+    for (int h = 0; h < SLOTS; ++h) {
+      if (j == h * LPR + sub) {
+        my_idx[h] = (uint32_t)bi;
+        my_p[h] = p;
+      }
     }
   }
-
+  if (!live) return;
+  if (dead) {
+    for (int j = sub; j < k; j += LPR) {
+      idx[t * k + j] = (uint32_t)j;
+      w_out[t * k + j] = from_f32<T>(NAN);
+      if (w32) w32[t * k + j] = NAN;
+    }
+    return;
+  }
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int j = h * 32 + lane;
+  for (int h = 0; h < SLOTS; ++h) {
+    const int j = h * LPR + sub;
     if (j < k) {
       const float w = renorm ? my_p[h] / sel_sum : my_p[h];
       idx[t * k + j] = my_idx[h];
@@ -162,26 +184,23 @@ template <typename T>
 cudaError_t launch_typed(const void* logits, int64_t T_rows, int E, int k, int renorm,
                          uint32_t* idx, void* weights, float* w32, uint32_t* status_reset,
                          cudaStream_t s) {
-  dim3 grid((unsigned)((T_rows + kRowsPerBlock - 1) / kRowsPerBlock));
-  dim3 block(32 * kRowsPerBlock);
   const T* l = static_cast<const T*>(logits);
   T* w = static_cast<T*>(weights);
-  cudaError_t err = cudaSuccess;
-#define MOE_ROUTE_CASE(V)                                                                     \
-  err = launch_pdl(route_kernel<T, V>, grid, block, 0, s, l, T_rows, E, k, renorm, idx, w, w32,  \
-                   status_reset);                                                              \
-  break;
-  switch ((E + 31) / 32 <= 1 ? 1 : (E + 31) / 32 <= 2 ? 2 : (E + 31) / 32 <= 4 ? 4
-          : (E + 31) / 32 <= 8 ? 8 : (E + 31) / 32 <= 16 ? 16 : 32) {
-    case 1: MOE_ROUTE_CASE(1)
-    case 2: MOE_ROUTE_CASE(2)
-    case 4: MOE_ROUTE_CASE(4)
-    case 8: MOE_ROUTE_CASE(8)
-    case 16: MOE_ROUTE_CASE(16)
-    default: MOE_ROUTE_CASE(32)
-  }
-#undef MOE_ROUTE_CASE
-  return err;
+  // lanes per row and values per lane: E <= 64 on 8 lanes, E <= 128 on 16, else 32
+  auto go = [&](auto kernel, int lpr) {
+    const int64_t rows_per_block = (int64_t)kRowsPerBlock * (32 / lpr);
+    dim3 grid((unsigned)((T_rows + rows_per_block - 1) / rows_per_block));
+    return launch_pdl(kernel, grid, dim3(32 * kRowsPerBlock), 0, s, l, T_rows, E, k, renorm, idx, w,
+                      w32, status_reset);
+  };
+  if (E <= 8) return go(route_kernel<T, 8, 1>, 8);
+  if (E <= 16) return go(route_kernel<T, 8, 2>, 8);
+  if (E <= 32) return go(route_kernel<T, 8, 4>, 8);
+  if (E <= 64) return go(route_kernel<T, 8, 8>, 8);
+  if (E <= 128) return go(route_kernel<T, 16, 8>, 16);
+  if (E <= 256) return go(route_kernel<T, 32, 8>, 32);
+  if (E <= 512) return go(route_kernel<T, 32, 16>, 32);
+  return go(route_kernel<T, 32, 32>, 32);
 }
 
 // ---------------------------------------------------------------------------
