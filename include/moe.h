@@ -289,7 +289,12 @@ moe_status moe_forward_host(moe_experts_t experts, const void* x_host, const voi
  *   - moe_host_pipeline_sync waits for every submitted batch.
  *   - moe_host_pipeline_destroy synchronises and frees the streams and events.
  * Results are bitwise those of moe_forward on the same batch.  The device
- * status word is the one at the start of the workspace. */
+ * status word is the one at the start of the workspace.
+ * Errors: a NULL handle, output or pipeline, depth outside 2..4, a bad dtype
+ * or workspace -> MOE_ERR_INVALID_ARG / MOE_ERR_DTYPE (nothing created);
+ * T outside 0..=T_max in submit -> MOE_ERR_SHAPE (nothing enqueued; T == 0 is
+ * a no-op); stream or event creation failure -> MOE_ERR_CUDA.  A pipeline is
+ * used from one host thread at a time.  destroy(NULL) is a no-op. */
 typedef struct moe_host_pipeline* moe_host_pipeline_t;
 size_t moe_host_pipeline_workspace_size(moe_experts_t experts, int64_t T_max, int32_t top_k,
                                         moe_dtype logits_dtype, int depth);
