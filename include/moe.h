@@ -1,5 +1,6 @@
 /*
- * moe.h -- C ABI of the GB300 (sm_103a) local Mixture-of-Experts forward.
+ * moe.h -- C ABI of the GB300 (sm_103a) local Mixture-of-Experts forward and
+ * its first-order backward.
  *
  * The pipeline follows the ruDNN user guide ("ruDNN Benutzerhandbuch"),
  * section 3 "MoE-Workflow": router logits -> FP32 softmax / top-k ->
@@ -17,7 +18,8 @@
  *   - Work is enqueued on `stream` and the call returns without waiting for
  *     the device (except moe_get_device_status, which synchronises that
  *     stream).  Calls are therefore capturable in a CUDA graph, except
- *     moe_get_device_status and moe_forward_host with pageable memory.
+ *     moe_get_device_status, moe_forward_host with pageable memory and the
+ *     moe_host_pipeline_* calls (which own their streams).
  *   - Shapes are element counts.  T = tokens, E = experts, k = top_k,
  *     H = hidden size, I = expert intermediate size, N = T*k dispatched rows.
  *   - Every call returns a moe_status.  On any status other than MOE_OK,
