@@ -69,11 +69,15 @@ constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int MAX_E = 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-template <int PAIR>
+// KS: 64-deep K sub-blocks per ring stage.  KS = 2 (forward CTA-pair GEMMs,
+// K-major operands) halves the barrier round trips and commits per MMA: one
+// stage holds A sub-blocks 0..KS-1, then B sub-blocks 0..KS-1, each in the
+// 128-byte-swizzled layout of one TMA box.
+template <int PAIR, int KS = 1>
 struct Cfg {
-  static constexpr int STAGES = PAIR == 1 ? 4 : 6;
-  static constexpr uint32_t B_BYTES = (PAIR == 1 ? 2u : 1u) * B_HALF_BYTES;  // B staged per CTA
-  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = KS == 2 ? 3 : (PAIR == 1 ? 4 : 6);
+  static constexpr uint32_t B_BYTES = (PAIR == 1 ? 2u : 1u) * B_HALF_BYTES;  // B staged per CTA per sub-block
+  static constexpr uint32_t STAGE_BYTES = KS * (A_BYTES + B_BYTES);
   static constexpr int TILE_M = BM * PAIR;
 };
 
@@ -478,11 +482,11 @@ __device__ __forceinline__ Tile decode_wgrad(uint32_t tile, const Params& p, int
 }
 
 // ---------------------------------------------------------------- the kernel
-template <typename T, int PAIR>
+template <typename T, int PAIR, int KS>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
                 const __grid_constant__ CUtensorMap mapB1, const Params p) {
-  using C = Cfg<PAIR>;
+  using C = Cfg<PAIR, KS>;
   constexpr int STAGES = C::STAGES;
   constexpr bool kCluster = PAIR == 2;
   extern __shared__ uint8_t smem_raw[];
@@ -597,17 +601,34 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           const uint32_t fb = full0_leader + 8u * stage;
           // K coordinates of this k-block: A's, and B's (row or column)
           const bool second = p.kb_split > 0 && kb >= p.kb_split;  // [dg | du] . [W_gate ; W_up]: up half
-          const int kx = second ? p.a_k2 + (kb - p.kb_split) * BK : t.kx0 + kb * BK;
+          const int kx = second ? p.a_k2 + (kb - p.kb_split) * BK : t.kx0 + kb * BK * KS;
           const int kb_b = second ? (kb - p.kb_split) * BK : t.kx0 + kb * BK;
           const CUtensorMap* mb = second ? &mapB1 : &mapB0;
           if (leader) mbar_expect_tx(full_bar(stage), C::STAGE_BYTES * PAIR);
-          if (p.a_mn) {  // two 64-column boxes of this CTA's 128 M values
+          if constexpr (KS == 2) {  // K-major A and B only: KS sub-blocks of 64
+#pragma unroll
+            for (int sub = 0; sub < KS; ++sub) {
+              const int kxs = kx + sub * BK;
+              const uint32_t sbs = sa + KS * A_BYTES + sub * C::B_BYTES;
+              tma_load_2d<PAIR>(sa + sub * A_BYTES, &mapA, kxs, a_row, fb);
+              if constexpr (PAIR == 1) {
+                tma_load_3d<PAIR>(sbs, &mapB0, kxs, b0row, t.e, fb);
+                tma_load_3d<PAIR>(sbs + B_HALF_BYTES, &mapB1, kxs, b1row, t.e, fb);
+              } else if (leader) {
+                tma_load_3d<PAIR>(sbs, &mapB0, kxs, b0row, t.e, fb);
+              } else {
+                tma_load_3d<PAIR>(sbs, &mapB1, kxs, b1row, t.e, fb);
+              }
+            }
+          } else if (p.a_mn) {  // two 64-column boxes of this CTA's 128 M values
             tma_load_2d<PAIR>(sa, &mapA, a_row, kx, fb);
             tma_load_2d<PAIR>(sa + MN_BOX_BYTES, &mapA, a_row + 64, kx, fb);
           } else {
             tma_load_2d<PAIR>(sa, &mapA, kx, a_row, fb);
           }
-          if (p.b_form == kBKmajor3d) {
+          if (KS == 2) {
+            // loaded above
+          } else if (p.b_form == kBKmajor3d) {
             if constexpr (PAIR == 1) {
               tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kx, b0row, t.e, fb);
               tma_load_3d<PAIR>(sa + A_BYTES + B_HALF_BYTES, &mapB1, kx, b1row, t.e, fb);
@@ -669,12 +690,13 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           }
           tc_fence_after();
           const uint32_t sa = ring + stage * C::STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sb = sa + KS * A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            const uint32_t ak = sa + kk * a_step, bk = sb + kk * b_step;
+          for (int q = 0; q < KS * (BK / UMMA_K); ++q) {
+            const int sub = q / (BK / UMMA_K), kk = q % (BK / UMMA_K);
+            const uint32_t ak = sa + sub * A_BYTES + kk * a_step, bk = sb + sub * C::B_BYTES + kk * b_step;
             umma_f16<PAIR>(d_tmem, a_hi | ((ak & 0x3FFFFu) >> 4), b_hi | ((bk & 0x3FFFFu) >> 4), idesc,
-                           (kb | kk) != 0 ? 1u : 0u);
+                           (kb | q) != 0 ? 1u : 0u);
           }
           umma_commit<PAIR>(empty_bar(stage));  // ring stage free (in every CTA) once done
           if (++stage == STAGES) {
@@ -969,20 +991,21 @@ bool encode_3d(CUtensorMap* m, const void* base, moe_dtype dt, uint64_t E, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int PAIR>
+template <int PAIR, int KS = 1>
 size_t smem_bytes(int E) {
-  return 1024 + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES + STG_BYTES + 256 + 8 * (size_t)(E + 1);
+  return 1024 + (size_t)Cfg<PAIR, KS>::STAGES * Cfg<PAIR, KS>::STAGE_BYTES + STG_BYTES + 256 +
+         8 * (size_t)(E + 1);
 }
 
 // Clusters of PAIR CTAs that can be resident at once (one CTA per SM).
-template <typename T, int PAIR>
+template <typename T, int PAIR, int KS = 1>
 cudaError_t resident_clusters(int num_sms, int* out) {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   static int clusters = 0;
   std::call_once(once, [num_sms] {
-    err = cudaFuncSetAttribute(grouped_gemm_tc<T, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem_bytes<PAIR>(MAX_E));
+    err = cudaFuncSetAttribute(grouped_gemm_tc<T, PAIR, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_bytes<PAIR, KS>(MAX_E));
     if (err != cudaSuccess) return;
     if (PAIR == 1) {
       clusters = num_sms;
@@ -996,20 +1019,20 @@ cudaError_t resident_clusters(int num_sms, int* out) {
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(PAIR * (num_sms / PAIR));
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = smem_bytes<PAIR>(MAX_E);
+    cfg.dynamicSmemBytes = smem_bytes<PAIR, KS>(MAX_E);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_tc<T, PAIR>, &cfg);
+    err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_tc<T, PAIR, KS>, &cfg);
   });
   *out = clusters;
   return err;
 }
 
-template <typename T, int PAIR>
+template <typename T, int PAIR, int KS = 1>
 cudaError_t launch_t(int64_t N, int E, const CUtensorMap& mA, const CUtensorMap& mB0,
                      const CUtensorMap& mB1, Params p, int num_sms, cudaStream_t s) {
   int clusters = 0;
-  cudaError_t err = resident_clusters<T, PAIR>(num_sms, &clusters);
+  cudaError_t err = resident_clusters<T, PAIR, KS>(num_sms, &clusters);
   if (err != cudaSuccess) return err;
   if (clusters < 1) return cudaErrorLaunchOutOfResources;
   constexpr int TM = Cfg<PAIR>::TILE_M;
@@ -1034,11 +1057,11 @@ cudaError_t launch_t(int64_t N, int E, const CUtensorMap& mA, const CUtensorMap&
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(nclu * PAIR);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = smem_bytes<PAIR>(E);
+  cfg.dynamicSmemBytes = smem_bytes<PAIR, KS>(E);
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc<T, PAIR>, mA, mB0, mB1, p);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc<T, PAIR, KS>, mA, mB0, mB1, p);
 }
 
 template <typename T>
@@ -1311,8 +1334,14 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, c
   // expert (decode-sized batches) the GEMM streams weights from HBM and single
   // CTAs keep twice as many independent streams in flight.
   const bool pair = a.N >= (int64_t)tc::BM * a.E;
-  if (a.dt == MOE_BF16) return tc::launch_any<__nv_bfloat16>(pair, a.N, a.E, mA, *b0, *b1, p, num_sms, s);
-  return tc::launch_any<__half>(pair, a.N, a.E, mA, *b0, *b1, p, num_sms, s);
+  if (pair) {  // 128-deep k-blocks: two 64-deep sub-blocks per ring stage
+    p.k_blocks = (int)((a.K + 2 * tc::BK - 1) / (2 * tc::BK));
+    if (a.dt == MOE_BF16)
+      return tc::launch_t<__nv_bfloat16, 2, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
+    return tc::launch_t<__half, 2, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
+  }
+  if (a.dt == MOE_BF16) return tc::launch_t<__nv_bfloat16, 1>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
+  return tc::launch_t<__half, 1>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
 }
 
 size_t experts_backward_tc_workspace(int64_t N, int E, int64_t H, int64_t I) {
