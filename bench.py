@@ -36,8 +36,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch of the gate/up GEMM on the headline workload, from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel source it was taken on; reported as null once the source changes.
-GATEUP_TRAFFIC = {"workload": "finegrained_bf16", "bytes": 1164290560 + 266119936,
-                  "source_sha256": "7becafbd24d385b8c39cfa80cb29762770d8b8a6fab83c0eb2c39f40036af92f"}
+GATEUP_TRAFFIC = {"workload": "finegrained_bf16", "bytes": 1140995584 + 263942144,
+                  "source_sha256": "0aa5f00349626cb9834a0f8e2bfbd2921864465a4c32b6e3952386586bf40caa"}
 
 
 def parse_args(argv=None):
