@@ -50,6 +50,10 @@ def parse_args(argv=None):
                    help="backward: time the first-order training backward chain instead")
     p.add_argument("--bwd-strategy", choices=["scalar", "auto", "tensor_core"], default="auto",
                    help="expert backward strategy of --mode backward")
+    p.add_argument("--routing", choices=["softmax", "sigmoid"], default="softmax",
+                   help="sigmoid: time the fused forward with sigmoid group-limited routing "
+                        "(groups of 8 experts, half the groups kept, top-two group score, "
+                        "renormalised, scale 2.5)")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--dtype", choices=["bf16", "f16"], default=None,
                    help="store the workload in this dtype instead of its own")
@@ -534,6 +538,69 @@ def run_backward(args, rank, world, local):
     return 0
 
 
+def run_sigmoid(args, rank, world, local):
+    """The fused forward with sigmoid group-limited routing (user guide section
+    10) on the workload's shapes; one event pair around the timed steps, and
+    the routing kernel timed on its own."""
+    import torch
+    import top_routing_grouped_fp32_gb300 as moe
+    from top_routing_grouped_fp32_gb300.inputs import make_inputs
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = bench_workload(args)
+    inp = make_inputs(wl, device=dev)
+    ex = moe.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    groups = max(1, wl.E // 8)
+    opts = dict(groups=groups, selected_groups=max(1, groups // 2), group_top_two=wl.E // groups >= 2,
+                renormalize=True, scale=2.5)
+    y = torch.empty((wl.T, wl.H), dtype=inp["x"].dtype, device=dev)
+    ws = ex.forward_workspace(wl.T, wl.top_k, inp["logits"].dtype)
+
+    def step():
+        ex.forward_sigmoid_grouped(inp["x"], inp["logits"], wl.top_k, y=y, workspace=ws, **opts)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    w0 = time.time()
+    e0.record()
+    for _ in range(K):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop(w0, time.time())
+    ms = e0.elapsed_time(e1) / K
+    # the routing kernel alone
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record()
+    for _ in range(K):
+        moe.moe_route_sigmoid_grouped(inp["logits"], wl.top_k, **opts)
+    r1.record()
+    torch.cuda.synchronize(dev)
+    route_ms = r0.elapsed_time(r1) / K
+    peaks, peaks_src = load_peaks()
+    sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    N = wl.T * wl.top_k
+    ach = 6.0 * N * wl.H * wl.I / (ms * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": wl.T / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "routing": "sigmoid",
+            "routing_options": opts, "dtype": wl.dtype, "data": "synthetic",
+            "config": workload_config(wl), "route_sigmoid_ms": route_ms,
+            "roofline": {"bound": "tensor", "kernel": "whole fused forward (per-kernel split not instrumented)",
+                         "achieved": ach, "peak": sus, "unit": "TFLOP/s", "frac": ach / sus,
+                         "peak_source": f"{peaks_src} bf16_tflops_sustained",
+                         "algorithmic_per_step": f"6*N*H*I = {6.0 * N * wl.H * wl.I:.4e} FLOP"},
+            "clocks": clock_info, "device_status": moe.moe_get_device_status(ws)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
@@ -541,6 +608,8 @@ def main(argv=None):
         return run_reference(args, rank, world)
     if args.mode == "backward":
         return run_backward(args, rank, world, local)
+    if args.routing == "sigmoid":
+        return run_sigmoid(args, rank, world, local)
     return run_native(args, rank, world, local)
 
 
