@@ -313,10 +313,12 @@ moe_status moe_host_pipeline_destroy(moe_host_pipeline_t pipeline);
  * that a caller can inspect them after the stream has finished:
  *   idx [T,k] u32, weights [T,k] logits dtype, offsets [E+1] u32,
  *   perm [T*k] u32, x_disp [T*k,H], h [T*k,I], slots [T*k,H] (weighted
- *   expert outputs at token-slot order).  Returns MOE_ERR_INVALID_ARG for a
+ *   expert outputs at token-slot order), slot_row [T*k] u32 (the dispatched
+ *   row of slot t*k+j, the inverse of perm; written only when a row of x is
+ *   a whole number of 16-byte vectors).  Returns MOE_ERR_INVALID_ARG for a
  *   null handle or output. */
 typedef struct {
-    size_t idx, weights, offsets, perm, x_disp, h, slots, total;
+    size_t idx, weights, offsets, perm, x_disp, h, slots, slot_row, total;
 } moe_forward_layout_t;
 moe_status moe_forward_layout(moe_experts_t experts, int64_t T, int32_t top_k,
                               moe_dtype logits_dtype, moe_forward_layout_t* out);

@@ -23,7 +23,7 @@ def _ws_views(experts, ws, T, k, ldtype):
     idx = b[lay["idx"]:lay["idx"] + 4 * N].view(torch.int32).view(T, k)
     offsets = b[lay["offsets"]:lay["offsets"] + 4 * (E + 1)].view(torch.int32)
     perm = b[lay["perm"]:lay["perm"] + 4 * N].view(torch.int32)
-    return idx, offsets, perm
+    return idx, offsets, perm, lay
 
 
 def _forward(moe, wl, inp, **kw):
@@ -34,14 +34,26 @@ def _forward(moe, wl, inp, **kw):
     return experts, ws, y
 
 
-def _check_routing_and_dispatch(experts, ws, wl, logits):
-    idx, offsets, perm = _ws_views(experts, ws, wl.T, wl.top_k, logits.dtype)
+def _check_routing_and_dispatch(experts, ws, wl, logits, x=None):
+    idx, offsets, perm, lay = _ws_views(experts, ws, wl.T, wl.top_k, logits.dtype)
     o_idx, _, _ = oracle_route(logits, wl.top_k, wl.renormalize)
     assert np.array_equal(u32(idx), o_idx), "routing indices differ"
     o_off, _, o_perm, bad = oracle.dispatch(o_idx, wl.E)
     assert bad == 0
     assert np.array_equal(u32(offsets), o_off), "offsets differ"
     assert np.array_equal(u32(perm), o_perm), "perm differs"
+    N, rows = wl.T * wl.top_k, int(o_off[-1])
+    if x is not None and (wl.H * x.element_size()) % 16 == 0:
+        # token-order gather: slot_row is the inverse of perm on every slot
+        slot_row = ws[lay["slot_row"]:lay["slot_row"] + 4 * N].view(torch.int32)
+        inv = np.full(N, 0xFFFFFFFF, dtype=np.uint32)
+        inv[o_perm[:rows]] = np.arange(rows, dtype=np.uint32)
+        assert np.array_equal(u32(slot_row), inv), "slot_row is not the inverse of perm"
+    if x is not None:
+        s = x.element_size()
+        x_disp = ws[lay["x_disp"]:lay["x_disp"] + rows * wl.H * s].view(x.dtype).view(rows, wl.H)
+        src = x[torch.from_numpy((o_perm[:rows] // wl.top_k).astype(np.int64)).to(x.device)]
+        assert torch.equal(x_disp.view(torch.uint8), src.contiguous().view(torch.uint8)), "x_disp differs"
     return o_idx, o_off
 
 
@@ -51,7 +63,7 @@ def _check_routing_and_dispatch(experts, ws, wl, logits):
     (200, 16, 4, 512, 128, "f16", True),
     (150, 5, 2, 40, 70, "f32", True),
     (100, 4, 2, 60, 90, "bf16", False),
-    # >= 128 rows per expert: the gate/up product gathers the token rows itself
+    # >= 128 rows per expert: CTA-pair tiles with k-block tails
     (1000, 4, 2, 200, 136, "bf16", True),   # H = 3*64 + 8: a one-chunk k-block tail
     (700, 3, 3, 72, 64, "f16", False),      # H = 64 + 8
     (300, 1024, 8, 64, 64, "bf16", True),   # E at its limit: 8 KiB of per-expert tables in shared memory
@@ -62,7 +74,7 @@ def test_forward_small_all_tokens(cuda_lib, T, E, k, H, I, dtype, renorm):
     wl = small_workload(T, E, k, H, I, dtype=dtype, renormalize=renorm, seed=T + E)
     inp = make_inputs(wl, device="cuda")
     experts, ws, y = _forward(cuda_lib, wl, inp)
-    _check_routing_and_dispatch(experts, ws, wl, inp["logits"])
+    _check_routing_and_dispatch(experts, ws, wl, inp["logits"], inp["x"])
     _, _, ref = oracle_forward_sample(inp, k, renorm, np.arange(T), dtype)
     assert_y_close(y, ref, dtype)
     assert cuda_lib.moe_get_device_status(ws) == 0
@@ -72,7 +84,7 @@ def test_forward_tiny_fp32_workload(cuda_lib):
     wl = WORKLOADS["tiny_fp32"]
     inp = make_inputs(wl, device="cuda")
     experts, ws, y = _forward(cuda_lib, wl, inp)
-    o_idx, _ = _check_routing_and_dispatch(experts, ws, wl, inp["logits"])
+    o_idx, _ = _check_routing_and_dispatch(experts, ws, wl, inp["logits"], inp["x"])
     assert o_idx[:8].tolist() == [[0, 1], [1, 2], [0, 1], [0, 1], [0, 2], [3, 1], [0, 1], [0, 3]]
     _, _, ref = oracle_forward_sample(inp, wl.top_k, wl.renormalize, np.arange(wl.T), "f32")
     assert_y_close(y, ref, "f32")
@@ -94,7 +106,7 @@ def test_forward_full_workloads(cuda_lib, name, dtype):
     wl = with_dtype(WORKLOADS[name], dtype)
     inp = make_inputs(wl, device="cuda")
     experts, ws, y = _forward(cuda_lib, wl, inp)
-    _check_routing_and_dispatch(experts, ws, wl, inp["logits"])
+    _check_routing_and_dispatch(experts, ws, wl, inp["logits"], inp["x"])
     toks = _sample_tokens(wl, inp)
     _, _, ref = oracle_forward_sample(inp, wl.top_k, wl.renormalize, toks, wl.dtype)
     assert_y_close(y[torch.as_tensor(toks, device="cuda")], ref, wl.dtype)
@@ -130,7 +142,7 @@ def test_forward_fp32_logits_bf16_experts(cuda_lib):
     wl = small_workload(300, 8, 2, 256, 256, dtype="bf16", renormalize=True, seed=8)
     inp = make_inputs(wl, device="cuda", logits_dtype="f32")
     experts, ws, y = _forward(cuda_lib, wl, inp)
-    _check_routing_and_dispatch(experts, ws, wl, inp["logits"])
+    _check_routing_and_dispatch(experts, ws, wl, inp["logits"], inp["x"])
     _, _, ref = oracle.forward_tokens(stored(inp["x"]), stored(inp["logits"]), stored(inp["gate"]),
                                       stored(inp["up"]), stored(inp["down"]), "bf16", "f32", 2, True,
                                       np.arange(wl.T))

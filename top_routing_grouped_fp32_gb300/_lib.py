@@ -37,7 +37,7 @@ class MoeError(RuntimeError):
 
 class ForwardLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("idx", "weights", "offsets", "perm", "x_disp", "h", "slots", "total")]
+                ("idx", "weights", "offsets", "perm", "x_disp", "h", "slots", "slot_row", "total")]
 
 
 class GroupRoutingOptions(ctypes.Structure):

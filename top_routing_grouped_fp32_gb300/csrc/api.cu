@@ -149,7 +149,7 @@ struct Cursor {
 };
 
 struct ForwardLayout {
-  size_t idx, weights, offsets, perm, scratch, x_disp, h, slots, total;
+  size_t idx, weights, offsets, perm, scratch, x_disp, h, slots, slot_row, total;
 };
 
 ForwardLayout forward_layout(const moe_experts* x, int64_t T, int32_t k, moe_dtype ldt) {
@@ -164,6 +164,7 @@ ForwardLayout forward_layout(const moe_experts* x, int64_t T, int32_t k, moe_dty
   L.x_disp = c.take(N * (size_t)x->H * s);
   L.h = c.take(N * (size_t)x->I * s);
   L.slots = c.take(N * (size_t)x->H * s);
+  L.slot_row = c.take(N * 4);
   L.total = c.off;
   return L;
 }
@@ -256,11 +257,19 @@ moe_status forward_core(moe_experts_t x, const void* xin, const void* logits, mo
   MOE_TRY_CUDA(rec(0), "cudaEventRecord");
   MOE_TRY_CUDA(route(idx, w, s), "routing kernel launch");
   MOE_TRY_CUDA(rec(1), "cudaEventRecord");
+  // the gather walks tokens (each row read once, written to its top_k rows)
+  // where rows are whole 16-byte vectors, else dispatched rows in order
+  uint32_t* slot_row = at<uint32_t>(ws, L.slot_row);
+  const bool by_token = (x->H * (int64_t)dtype_size(x->dt)) % 16 == 0;
   MOE_TRY_CUDA(moe::launch_dispatch(idx, T, E, k, offsets, nullptr, perm, at<void>(ws, L.scratch),
-                                    status, s),
+                                    status, s, by_token ? slot_row : nullptr),
                "dispatch kernel launch");
-  MOE_TRY_CUDA(moe::launch_gather(xin, x->dt, x->H, k, perm, offsets, E, N, at<void>(ws, L.x_disp), s),
-               "gather kernel launch");
+  if (by_token)
+    MOE_TRY_CUDA(moe::launch_gather_tokens(xin, x->dt, x->H, k, slot_row, T, at<void>(ws, L.x_disp), s),
+                 "gather kernel launch");
+  else
+    MOE_TRY_CUDA(moe::launch_gather(xin, x->dt, x->H, k, perm, offsets, E, N, at<void>(ws, L.x_disp), s),
+                 "gather kernel launch");
   MOE_TRY_CUDA(rec(2), "cudaEventRecord");
   st = run_experts(x, at<void>(ws, L.x_disp), N, offsets, at<void>(ws, L.h), at<void>(ws, L.slots),
                    moe::kDownWeighted, perm, w, ldt, status, s, ev ? ev[3] : nullptr);
@@ -516,6 +525,7 @@ moe_status moe_forward_layout(moe_experts_t x, int64_t T, int32_t top_k, moe_dty
   out->x_disp = L.x_disp;
   out->h = L.h;
   out->slots = L.slots;
+  out->slot_row = L.slot_row;
   out->total = L.total;
   return ok();
 }

@@ -146,7 +146,7 @@ scan_kernel(const uint32_t* __restrict__ chunk_counts, int nchunks, int E, int64
 __global__ void __launch_bounds__(256)
 scatter_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
                const uint32_t* __restrict__ chunk_base, uint32_t* __restrict__ perm,
-               uint32_t* __restrict__ row_experts) {
+               uint32_t* __restrict__ row_experts, uint32_t* __restrict__ slot_row) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint32_t smem[];
@@ -205,7 +205,10 @@ scatter_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
         const uint32_t r = base + __popc(grp & lt_mask);
         perm[r] = (uint32_t)(t * k + j);
         if (row_experts) row_experts[r] = e;
+        if (slot_row) slot_row[t * k + j] = r;
         if ((grp & lt_mask) == 0) my[e] = base + __popc(grp);
+      } else if (slot_row && j < k) {
+        slot_row[t * k + j] = kInvalid;  // not dispatched
       }
       __syncwarp();
     }
@@ -251,6 +254,43 @@ gather_kernel(const char* __restrict__ x, int64_t row_bytes, int k, const uint32
   }
 }
 
+// The same rows in token order: one warp per token reads its row once (a
+// 4 KiB chunk per round, 8 loads in flight per lane) and writes it to each of
+// its top_k dispatched rows, slot_row[t*k+j] (kInvalid: not dispatched).  A
+// token row is then fetched from DRAM once, instead of top_k times far apart.
+__global__ void __launch_bounds__(256)
+gather_tokens_kernel(const uint4* __restrict__ x, int64_t vecs, int k, const uint32_t* __restrict__ slot_row,
+                     int64_t T, uint4* __restrict__ x_disp) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  // lane j holds the rows of slots j and 32 + j (top_k <= 64)
+  const uint32_t* sr = slot_row + t * k;
+  const uint32_t r_lo = lane < k ? __ldg(sr + lane) : kInvalid;
+  const uint32_t r_hi = lane + 32 < k ? __ldg(sr + 32 + lane) : kInvalid;
+  const uint4* src = x + t * vecs;
+  for (int64_t v0 = 0; v0 < vecs; v0 += 8 * 32) {
+    uint4 q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t v = v0 + 32 * i + lane;
+      if (v < vecs) q[i] = __ldg(src + v);
+    }
+    for (int j = 0; j < k; ++j) {
+      const uint32_t r = __shfl_sync(0xffffffffu, j < 32 ? r_lo : r_hi, j & 31);
+      if (r == kInvalid) continue;
+      uint4* dst = x_disp + (int64_t)r * vecs;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int64_t v = v0 + 32 * i + lane;
+        if (v < vecs) __stcs(dst + v, q[i]);
+      }
+    }
+  }
+}
+
 }  // namespace
 
 size_t dispatch_scratch_bytes(int64_t T, int E) {
@@ -260,7 +300,7 @@ size_t dispatch_scratch_bytes(int64_t T, int E) {
 
 cudaError_t launch_dispatch(const uint32_t* idx, int64_t T, int E, int k, uint32_t* offsets,
                             uint32_t* row_experts, uint32_t* perm, void* scratch,
-                            uint32_t* status, cudaStream_t s) {
+                            uint32_t* status, cudaStream_t s, uint32_t* slot_row) {
   const int64_t nc = dispatch_chunks(T);
   uint32_t* counts = static_cast<uint32_t*>(scratch);
   uint32_t* bases = reinterpret_cast<uint32_t*>(static_cast<char*>(scratch) +
@@ -278,7 +318,18 @@ cudaError_t launch_dispatch(const uint32_t* idx, int64_t T, int E, int k, uint32
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(scatter_kernel, dim3((unsigned)nc), dim3(256), smem, s, idx, T, E, k, bases, perm,
-                    row_experts);
+                    row_experts, slot_row);
+}
+
+cudaError_t launch_gather_tokens(const void* x, moe_dtype dt, int64_t H, int k, const uint32_t* slot_row,
+                                 int64_t T, void* x_disp, cudaStream_t s) {
+  const int64_t row_bytes = H * (int64_t)dtype_size(dt);
+  if (row_bytes % 16 != 0 || reinterpret_cast<uintptr_t>(x) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(x_disp) % 16 != 0 || k > 64)
+    return cudaErrorInvalidValue;
+  return launch_pdl(gather_tokens_kernel, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, s,
+                    static_cast<const uint4*>(x), row_bytes / 16, k, slot_row, T,
+                    static_cast<uint4*>(x_disp));
 }
 
 cudaError_t launch_gather(const void* x, moe_dtype dt, int64_t H, int k, const uint32_t* perm,

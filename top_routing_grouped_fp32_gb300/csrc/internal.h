@@ -32,7 +32,11 @@ inline int64_t dispatch_chunks(int64_t T) { return (T + kDispatchChunk - 1) / kD
 size_t dispatch_scratch_bytes(int64_t T, int E);
 cudaError_t launch_dispatch(const uint32_t* idx, int64_t T, int E, int k, uint32_t* offsets,
                             uint32_t* row_experts, uint32_t* perm, void* scratch,
-                            uint32_t* status, cudaStream_t s);
+                            uint32_t* status, cudaStream_t s, uint32_t* slot_row = nullptr);
+// x_disp in token order from the slot -> row map the scatter wrote (16-byte
+// rows and pointers, top_k <= 64; cudaErrorInvalidValue otherwise)
+cudaError_t launch_gather_tokens(const void* x, moe_dtype dt, int64_t H, int k, const uint32_t* slot_row,
+                                 int64_t T, void* x_disp, cudaStream_t s);
 // fixed device scratch for moe_dispatch_noalloc (size limit and address)
 size_t dispatch_noalloc_scratch_limit();
 cudaError_t dispatch_noalloc_scratch(void** out);
