@@ -46,6 +46,9 @@ def test_dispatch_workloads(cuda_lib, name):
 @pytest.mark.parametrize("T,E,k,H,dtype", [
     (1, 1, 1, 8, "bf16"), (255, 7, 3, 64, "bf16"), (257, 7, 3, 64, "f16"), (1000, 64, 6, 136, "bf16"),
     (300, 1024, 64, 16, "bf16"), (40, 50, 33, 24, "f32"), (513, 9, 2, 30, "bf16"), (100, 3, 3, 12, "f32"),
+    # 15 chunks x 1025 histogram words: the scatter blocks scan the table themselves;
+    # 16 chunks x 1025 words: over the limit, the one-block scan kernel runs
+    (3840, 1024, 8, 16, "bf16"), (4000, 1024, 8, 16, "bf16"), (70000, 64, 2, 8, "bf16"),
 ])
 def test_dispatch_shapes(cuda_lib, T, E, k, H, dtype):
     rng = np.random.default_rng(T + E + k)

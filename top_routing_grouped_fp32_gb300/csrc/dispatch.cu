@@ -15,6 +15,8 @@
 //  2. scan:    one block turns the chunk histograms into offsets[E+1] and the
 //              first row of every (chunk, expert) pair; it also writes the
 //              device status and fills the unused tail of perm/row_experts.
+//              For a small histogram table (chunks * (E+1) <= 16384 words) the
+//              scatter blocks do this themselves and the kernel is skipped.
 //  3. scatter: each warp walks its 32 tokens in order; lanes hold the k slots
 //              of one token and __match_any_sync ranks equal experts among
 //              them, so ranks follow s exactly, duplicates included.  A first
@@ -29,6 +31,9 @@ namespace moe {
 namespace {
 
 constexpr int kWarps = kDispatchChunk / 32;  // 8 warps, 32 tokens each
+// histogram tables up to this many words are scanned by every scatter block
+// (at most 64 KiB of L2 reads per block, instead of a one-block scan kernel)
+constexpr int64_t kFusedScanWords = 16384;
 
 __global__ void __launch_bounds__(256)
 count_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
@@ -143,10 +148,18 @@ scan_kernel(const uint32_t* __restrict__ chunk_counts, int nchunks, int E, int64
   }
 }
 
+// SCAN: the scan is done here too (two kernels instead of three).  Every
+// block reads the whole chunk histogram table (small: the launcher takes this
+// form when chunks * (E+1) <= kFusedScanWords) and forms the per-expert totals
+// and its own chunk's first rows; block 0 also writes offsets, the status and
+// the tail of perm / row_experts, as the scan kernel does otherwise.
+template <bool SCAN>
 __global__ void __launch_bounds__(256)
 scatter_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
                const uint32_t* __restrict__ chunk_base, uint32_t* __restrict__ perm,
-               uint32_t* __restrict__ row_experts, uint32_t* __restrict__ slot_row) {
+               uint32_t* __restrict__ row_experts, uint32_t* __restrict__ slot_row,
+               const uint32_t* __restrict__ chunk_counts, int nchunks, uint32_t* __restrict__ offsets,
+               uint32_t* __restrict__ status) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint32_t smem[];
@@ -159,6 +172,65 @@ scatter_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
   const int64_t tc0 = (int64_t)blockIdx.x * kDispatchChunk;
   const int64_t nslots = (min(T, tc0 + kDispatchChunk) - tc0) * k;
   for (int64_t i = threadIdx.x; i < nslots; i += blockDim.x) sidx[i] = __ldg(idx + tc0 * k + i);
+  uint32_t* s_base = sidx + kDispatchChunk * k;  // SCAN: [E+1] this chunk's first rows
+  if constexpr (SCAN) {
+    uint32_t* s_tot = s_base + (E + 1);           // [E+1] totals, then segment starts
+    __shared__ uint32_t warp_sums[32];
+    __shared__ uint32_t s_valid;
+    // per expert (and the invalid column E): the total over all chunks and
+    // the part in the chunks before this one; a warp per expert, lanes over chunks
+    for (int e = w; e <= E; e += kWarps) {
+      uint32_t tot = 0, pre = 0;
+      for (int b = lane; b < nchunks; b += 32) {
+        const uint32_t v = __ldg(chunk_counts + (size_t)b * (E + 1) + e);
+        tot += v;
+        pre += b < (int)blockIdx.x ? v : 0u;
+      }
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, d);
+        pre += __shfl_xor_sync(0xffffffffu, pre, d);
+      }
+      if (lane == 0) {
+        s_tot[e] = tot;
+        s_base[e] = pre;
+      }
+    }
+    __syncthreads();
+    // exclusive scan of the totals over experts, 4 experts per thread (E <= 1024)
+    const int e0 = threadIdx.x * 4;
+    uint32_t v[4], loc = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[i] = e0 + i < E ? s_tot[e0 + i] : 0u;
+      loc += v[i];
+    }
+    const uint32_t incl = block_inclusive_scan(loc, warp_sums);
+    const uint32_t invalid = s_tot[E];
+    __syncthreads();  // every total read before the starts overwrite them
+    uint32_t run = incl - loc;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (e0 + i < E) {
+        s_tot[e0 + i] = run;
+        s_base[e0 + i] += run;
+        if (blockIdx.x == 0) offsets[e0 + i] = run;
+      }
+      run += v[i];
+    }
+    if (threadIdx.x == blockDim.x - 1) s_valid = incl;
+    __syncthreads();
+    if (blockIdx.x == 0) {
+      if (threadIdx.x == 0) {
+        offsets[E] = s_valid;
+        if (status) *status = invalid ? (uint32_t)MOE_ERR_INVALID_INDEX : 0u;
+      }
+      for (int64_t r = (int64_t)s_valid + threadIdx.x; r < T * k; r += blockDim.x) {
+        perm[r] = kInvalid;
+        if (row_experts) row_experts[r] = kInvalid;
+      }
+    }
+  }
   __syncthreads();
   const int64_t tw = tc0 + w * 32;
   uint32_t* my = wcnt + w * E;
@@ -181,7 +253,7 @@ scatter_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
   __syncthreads();
   // per-expert exclusive prefix over the warps, starting at the chunk's base
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    uint32_t run = chunk_base[(size_t)blockIdx.x * E + e];
+    uint32_t run = SCAN ? s_base[e] : chunk_base[(size_t)blockIdx.x * E + e];
     for (int ww = 0; ww < kWarps; ++ww) {
       const uint32_t c = wcnt[ww * E + e];
       wcnt[ww * E + e] = run;
@@ -308,17 +380,23 @@ cudaError_t launch_dispatch(const uint32_t* idx, int64_t T, int E, int k, uint32
   cudaError_t err = launch_pdl(count_kernel, dim3((unsigned)nc), dim3(256), (E + 1) * sizeof(uint32_t), s,
                                idx, T, E, k, counts);
   if (err != cudaSuccess) return err;
-  err = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, counts, (int)nc, E, T * k, offsets, bases,
-                   perm, row_experts, status);
-  if (err != cudaSuccess) return err;
-  const size_t smem = ((size_t)kWarps * E + (size_t)kDispatchChunk * k) * sizeof(uint32_t);
-  if (smem > 48 * 1024) {  // large E * k (at most 8*1024 + 256*64 words = 96 KiB): opt in
-    const cudaError_t e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem);
+  // a small histogram table: every scatter block scans it itself
+  const bool fused = nc * (E + 1) <= kFusedScanWords;
+  if (!fused) {
+    err = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, counts, (int)nc, E, T * k, offsets, bases,
+                     perm, row_experts, status);
+    if (err != cudaSuccess) return err;
+  }
+  // at most 8*1024 + 256*64 + 2*1025 words = 104 KiB
+  const size_t smem = ((size_t)kWarps * E + (size_t)kDispatchChunk * k + (fused ? 2 * (E + 1) : 0)) *
+                      sizeof(uint32_t);
+  auto kern = fused ? scatter_kernel<true> : scatter_kernel<false>;
+  if (smem > 48 * 1024) {  // large E * k: opt in
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(scatter_kernel, dim3((unsigned)nc), dim3(256), smem, s, idx, T, E, k, bases, perm,
-                    row_experts, slot_row);
+  return launch_pdl(kern, dim3((unsigned)nc), dim3(256), smem, s, idx, T, E, k, bases, perm, row_experts,
+                    slot_row, counts, (int)nc, offsets, status);
 }
 
 cudaError_t launch_gather_tokens(const void* x, moe_dtype dt, int64_t H, int k, const uint32_t* slot_row,
