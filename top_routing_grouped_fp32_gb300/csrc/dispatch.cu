@@ -17,10 +17,11 @@
 //              device status and fills the unused tail of perm/row_experts.
 //              For a small histogram table (chunks * (E+1) <= 16384 words) the
 //              scatter blocks do this themselves and the kernel is skipped.
-//  3. scatter: each warp walks its 32 tokens in order; lanes hold the k slots
-//              of one token and __match_any_sync ranks equal experts among
-//              them, so ranks follow s exactly, duplicates included.  A first
-//              pass counts per warp, a second writes perm/row_experts.
+//  3. scatter: each warp walks the slots of its 32 tokens in order, 32
+//              consecutive slots per step; __match_any_sync ranks equal
+//              experts among the lanes, so ranks follow s exactly, duplicates
+//              included.  A first pass counts per warp, a second writes
+//              perm/row_experts.
 // A fourth kernel gathers x rows into x_disp, one warp per dispatched row.
 #include <mutex>
 
@@ -232,23 +233,22 @@ scatter_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
     }
   }
   __syncthreads();
+  // warp w walks the slots s = t*k + j of its 32 tokens in order, 32
+  // consecutive slots per step (a step may span tokens): lane order is slot
+  // order, so __match_any_sync ranks equal experts exactly as the stable sort
   const int64_t tw = tc0 + w * 32;
+  const int64_t s_begin = tw * k, s_end = min(T, tw + 32) * k, s_chunk = tc0 * k;
   uint32_t* my = wcnt + w * E;
   const uint32_t lt_mask = (1u << lane) - 1u;
 
   // pass 1: per-warp counts
-  for (int i = 0; i < 32; ++i) {
-    const int64_t t = tw + i;
-    if (t >= T) break;
-    for (int j0 = 0; j0 < k; j0 += 32) {
-      const int j = j0 + lane;
-      const uint32_t e = j < k ? sidx[(t - tc0) * k + j] : kInvalid;
-      const bool ok = e < (uint32_t)E;
-      const uint32_t key = ok ? e : kInvalid;
-      const uint32_t grp = __match_any_sync(0xffffffffu, key);
-      if (ok && (grp & lt_mask) == 0) my[e] += __popc(grp);
-      __syncwarp();
-    }
+  for (int64_t q = s_begin; q < s_end; q += 32) {
+    const int64_t sl = q + lane;
+    const uint32_t e = sl < s_end ? sidx[sl - s_chunk] : kInvalid;
+    const bool ok = e < (uint32_t)E;
+    const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : kInvalid);
+    if (ok && (grp & lt_mask) == 0) my[e] += __popc(grp);
+    __syncwarp();
   }
   __syncthreads();
   // per-expert exclusive prefix over the warps, starting at the chunk's base
@@ -262,28 +262,24 @@ scatter_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
   }
   __syncthreads();
   // pass 2: the same walk, now writing rows
-  for (int i = 0; i < 32; ++i) {
-    const int64_t t = tw + i;
-    if (t >= T) break;
-    for (int j0 = 0; j0 < k; j0 += 32) {
-      const int j = j0 + lane;
-      const uint32_t e = j < k ? sidx[(t - tc0) * k + j] : kInvalid;
-      const bool ok = e < (uint32_t)E;
-      const uint32_t key = ok ? e : kInvalid;
-      const uint32_t grp = __match_any_sync(0xffffffffu, key);
-      uint32_t base = ok ? my[e] : 0u;
-      __syncwarp();
-      if (ok) {
-        const uint32_t r = base + __popc(grp & lt_mask);
-        perm[r] = (uint32_t)(t * k + j);
-        if (row_experts) row_experts[r] = e;
-        if (slot_row) slot_row[t * k + j] = r;
-        if ((grp & lt_mask) == 0) my[e] = base + __popc(grp);
-      } else if (slot_row && j < k) {
-        slot_row[t * k + j] = kInvalid;  // not dispatched
-      }
-      __syncwarp();
+  for (int64_t q = s_begin; q < s_end; q += 32) {
+    const int64_t sl = q + lane;
+    const bool in = sl < s_end;
+    const uint32_t e = in ? sidx[sl - s_chunk] : kInvalid;
+    const bool ok = e < (uint32_t)E;
+    const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : kInvalid);
+    const uint32_t base = ok ? my[e] : 0u;
+    __syncwarp();
+    if (ok) {
+      const uint32_t r = base + __popc(grp & lt_mask);
+      perm[r] = (uint32_t)sl;
+      if (row_experts) row_experts[r] = e;
+      if (slot_row) slot_row[sl] = r;
+      if ((grp & lt_mask) == 0) my[e] = base + __popc(grp);
+    } else if (slot_row && in) {
+      slot_row[sl] = kInvalid;  // not dispatched
     }
+    __syncwarp();
   }
 }
 
