@@ -253,7 +253,9 @@ moe_status moe_forward_sigmoid_grouped(moe_experts_t experts, const void* x, con
  * boundaries: events[0] before routing, [1] after routing, [2] after
  * dispatch, [3] after the gate/up projection, [4] after the down projection,
  * [5] after the combine.  `events` holds n_events (>= 6) cudaEvent_t handles
- * created by the caller; the library records them and nothing else. */
+ * created by the caller, or NULL for a boundary that is not to be recorded
+ * (each record sits between two kernels of the forward, so record only the
+ * boundaries you need); the library records them and nothing else. */
 moe_status moe_forward_timed(moe_experts_t experts, const void* x, const void* logits,
                              moe_dtype logits_dtype, int64_t T, int32_t top_k, int renormalize,
                              void* y, void* workspace, size_t workspace_bytes,

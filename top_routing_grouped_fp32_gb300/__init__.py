@@ -285,7 +285,7 @@ class SwiGluExperts:
                 y=None, workspace=None, stream=None, events=None) -> torch.Tensor:
         """Fused route -> dispatch -> experts -> combine (SwiGluExperts::forward).
         ``events``: optional list of 6 recorded-capable torch.cuda.Event objects
-        marking the stage boundaries."""
+        (or None for a boundary not to record) marking the stage boundaries."""
         T = x.shape[0]
         if y is None:
             y = torch.empty((T, self.H), dtype=self.dtype, device=x.device)
@@ -296,7 +296,8 @@ class SwiGluExperts:
         if events is None:
             _lib.check(self._lib.moe_forward(*args))
         else:
-            arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+            arr = (ctypes.c_void_p * len(events))(
+                *[ctypes.c_void_p(e.cuda_event if e is not None else None) for e in events])
             _lib.check(self._lib.moe_forward_timed(*args, arr, len(events)))
         return y
 
