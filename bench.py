@@ -30,7 +30,13 @@ if ROOT not in sys.path:
 METRIC = "MoE fwd tokens/s; grouped-GEMM TFLOP/s as % of GB300 BF16 peak (1 GPU)"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "finegrained_bf16"
-LAUNCHES_PER_STEP = 8  # route, count, scan, scatter, gather, gate/up GEMM, down GEMM, combine
+def launches_per_step(T: int, E: int) -> int:
+    """Kernels of one fused forward: route, count, [scan], scatter, gather,
+    gate/up GEMM, down GEMM, combine.  The scan kernel runs only when the
+    chunk histogram table (256-token chunks x (E+1) words) exceeds 16384
+    words; below that the scatter blocks scan it themselves."""
+    chunks = (T + 255) // 256
+    return 7 + (1 if chunks * (E + 1) > 16384 else 0)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic per launch of the gate/up GEMM on the headline workload, from one
@@ -437,7 +443,7 @@ def run_native(args, rank, world, local):
             "e2e": {"value": wl.T * world * Ke / (e2e_ms * 1e-3), "unit": UNIT,
                     "api": "moe_host_pipeline_submit (depth 2), one call per step",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": LAUNCHES_PER_STEP * K,
+            "gpu_launches": launches_per_step(wl.T, wl.E) * K,
             "clocks": clock_info,
             "device_status": status,
         }
