@@ -121,6 +121,22 @@ def test_forward_full_workloads(cuda_lib, name, dtype):
     torch.cuda.empty_cache()
 
 
+def test_forward_timed_partial_events(cuda_lib):
+    """moe_forward_timed records only the boundaries it is given and computes the same bits."""
+    wl = small_workload(1000, 16, 4, 512, 256, dtype="bf16", renormalize=True, seed=22)
+    inp = make_inputs(wl, device="cuda")
+    experts, ws, y1 = _forward(cuda_lib, wl, inp)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in ev:
+        e.record()
+    torch.cuda.synchronize()
+    y2 = experts.forward(inp["x"], inp["logits"], wl.top_k, wl.renormalize, workspace=ws,
+                         events=[None, None, ev[2], ev[3], None, None])
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert ev[2].elapsed_time(ev[3]) > 0.0  # the gate/up product lies between them
+
+
 def test_forward_deterministic_and_host_variant(cuda_lib):
     wl = small_workload(1000, 16, 4, 512, 256, dtype="bf16", renormalize=True, seed=21)
     inp = make_inputs(wl, device="cuda")

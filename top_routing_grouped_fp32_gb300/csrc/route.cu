@@ -24,6 +24,8 @@
 // agrees on each winner.
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -68,6 +70,32 @@ __device__ __forceinline__ void load_row(const T* row, int E, int lane, float (&
   }
 }
 
+// Selection key of a 16-bit logit: the logit's bits mapped to an unsigned
+// order (negative values reversed; -0 taken as +0), above 0xFFFF - id, so that
+// the larger unsigned key is the larger logit and, between equal logits, the
+// lower id.  Key 0 is below every real key and marks a selected expert.  The
+// logit is exact in its 16-bit type, so the key orders exactly what the FP32
+// comparison (larger logit, then lower id) orders.
+template <typename T>
+__device__ __forceinline__ uint32_t bits16_of(float v) {
+  if constexpr (std::is_same<T, __half>::value) return (uint32_t)__half_as_ushort(__float2half_rn(v));
+  else return __float_as_uint(v) >> 16;  // bf16: the high half of the exact FP32 value
+}
+template <typename T>
+__device__ __forceinline__ uint32_t sel_key(float v, int id) {
+  uint32_t b = bits16_of<T>(v);
+  if (b == 0x8000u) b = 0u;
+  const uint32_t o = (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+  return (o << 16) | (0xFFFFu - (uint32_t)id);
+}
+template <typename T>
+__device__ __forceinline__ float key_logit(uint32_t key) {
+  const uint32_t o = key >> 16;
+  const uint32_t b = (o & 0x8000u) ? (o & 0x7FFFu) : (~o & 0xFFFFu);
+  if constexpr (std::is_same<T, __half>::value) return __half2float(__ushort_as_half((unsigned short)b));
+  else return __uint_as_float(b << 16);
+}
+
 // LPR lanes per row (8, 16 or 32), so that a warp routes 32 / LPR rows at
 // once: for E <= 64 one warp instruction serves four rows, and each butterfly
 // has three steps instead of five.
@@ -95,15 +123,16 @@ route_kernel(const T* __restrict__ logits, int64_t T_rows, int E, int k, int ren
   }
   const int e0 = sub * VPL;
 
-  // poisoned-row detection and the row maximum (padding entries excluded)
+  // poisoned-row detection and the row maximum.  Padding entries (past E)
+  // hold -inf: they move neither the maximum nor the sum, and in the arg-max
+  // rounds a real expert beats them (a real -inf on the lower id), so with
+  // k <= E they are never selected.
   float m = -INFINITY;
   int bad = 0;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
-    if (e0 + i < E) {
-      bad |= (isnan(v[i]) || v[i] == INFINITY) ? 1 : 0;
-      m = fmaxf(m, v[i]);
-    }
+    bad |= (isnan(v[i]) || v[i] == INFINITY) ? 1 : 0;
+    m = fmaxf(m, v[i]);
   }
 #pragma unroll
   for (int d = LPR / 2; d > 0; d >>= 1) {
@@ -116,44 +145,66 @@ route_kernel(const T* __restrict__ logits, int64_t T_rows, int E, int k, int ren
   float s = 0.f;
   if (!dead) {
 #pragma unroll
-    for (int i = 0; i < VPL; ++i)
-      if (e0 + i < E) s += expf(v[i] - m);
+    for (int i = 0; i < VPL; ++i) s += expf(v[i] - m);
   }
 #pragma unroll
   for (int d = LPR / 2; d > 0; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d, LPR);
 
-  // k rounds of arg-max over the not-yet-selected experts
-  uint32_t taken = 0;  // bit i: expert e0+i already selected
+  // k rounds of arg-max over the not-yet-selected experts; slot j is kept by
+  // lane j % LPR of the row, in its register slot j / LPR
+  constexpr bool kKeys = sizeof(T) == 2;
+  uint32_t key[kKeys ? VPL : 1];
+  uint32_t taken = 0;  // FP32 logits: bit i set once expert e0+i is selected
+  if constexpr (kKeys) {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) key[i] = sel_key<T>(v[i], e0 + i);
+  }
   uint32_t my_idx[SLOTS];
   float my_p[SLOTS];
 #pragma unroll
   for (int h = 0; h < SLOTS; ++h) my_idx[h] = 0u, my_p[h] = 0.f;
   float sel_sum = 0.f;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      if (e0 + i < E && !(taken >> i & 1u) && beats(v[i], e0 + i, bv, bi)) {
-        bv = v[i];
-        bi = e0 + i;
+  for (int h = 0; h < SLOTS; ++h) {
+    if (h * LPR >= k) break;
+    const int jn = min(LPR, k - h * LPR);
+    for (int jj = 0; jj < jn; ++jj) {
+      float bv;
+      int bi;
+      if constexpr (kKeys) {
+        uint32_t bk = key[0];
+#pragma unroll
+        for (int i = 1; i < VPL; ++i) bk = max(bk, key[i]);
+#pragma unroll
+        for (int d = LPR / 2; d > 0; d >>= 1) bk = max(bk, __shfl_xor_sync(0xffffffffu, bk, d, LPR));
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) key[i] = key[i] == bk ? 0u : key[i];  // keys are unique per row
+        bi = (int)(0xFFFFu - (bk & 0xFFFFu));
+        bv = key_logit<T>(bk);
+      } else {
+        bv = -INFINITY;
+        bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          if (!(taken >> i & 1u) && beats(v[i], e0 + i, bv, bi)) {
+            bv = v[i];
+            bi = e0 + i;
+          }
+        }
+#pragma unroll
+        for (int d = LPR / 2; d > 0; d >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, d, LPR);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, d, LPR);
+          if (beats(ov, oi, bv, bi)) {
+            bv = ov;
+            bi = oi;
+          }
+        }
+        if (bi / VPL == sub) taken |= 1u << (bi % VPL);
       }
-    }
-#pragma unroll
-    for (int d = LPR / 2; d > 0; d >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, d, LPR);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, d, LPR);
-      if (beats(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (bi / VPL == sub) taken |= 1u << (bi % VPL);
-    const float p = dead ? 0.f : expf(bv - m) / s;
-    sel_sum += p;  // every lane adds in slot order
-#pragma unroll
-    for (int h = 0; h < SLOTS; ++h) {
-      if (j == h * LPR + sub) {
+      const float p = dead ? 0.f : expf(bv - m) / s;
+      sel_sum += p;  // every lane adds in slot order
+      if (jj == sub) {
         my_idx[h] = (uint32_t)bi;
         my_p[h] = p;
       }
