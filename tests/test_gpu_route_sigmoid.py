@@ -50,6 +50,17 @@ def test_sigmoid_routing_matches_oracle(cuda_lib, dtype, T, E, k, groups, sel, t
     _check(cuda_lib, logits, k, groups, sel, top_two, renorm, scale, bias)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_sigmoid_routing_every_16bit_logit(cuda_lib, dtype):
+    """Every non-NaN 16-bit logit pattern once, 64 to a row and all 64 selected: the
+    scores are ranked exactly as the oracle ranks its FP64 sigmoid rounded to FP32
+    (saturated values near 0 and 1 tie in FP32 and fall back to the lower id)."""
+    bits = torch.from_numpy(np.random.default_rng(7).permutation(65536).astype(np.int16))
+    logits = bits.view(torch.bfloat16 if dtype == "bf16" else torch.float16).clone()
+    logits[torch.isnan(logits)] = 0.0
+    _check(cuda_lib, logits.view(1024, 64).cuda(), 64, 1, 1, False, False, 1.0)
+
+
 def test_sigmoid_routing_ties_and_nan(cuda_lib):
     vals = torch.tensor([-1.0, 0.0, 0.0, 0.5, 2.0], device="cuda")
     g = torch.Generator(device="cuda").manual_seed(3)

@@ -24,6 +24,8 @@
 // agrees on each winner.
 #include <math.h>
 
+#include <map>
+#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -266,13 +268,31 @@ cudaError_t launch_typed(const void* logits, int64_t T_rows, int E, int k, int r
 // times `scale`, rounded to the logits dtype.
 //
 // The selection is an FP32 decision, so the sigmoid is the correctly rounded
-// FP32 value: computed with a double-precision exp and rounded once.  A row
+// FP32 value: computed with a double-precision exp and rounded once (for
+// 16-bit logits looked up in a table of those values for all 65536 patterns).  A row
 // with a NaN logit or NaN corrected score gets idx = 0..k-1 and NaN weights.
 //
 // One warp per row; the corrected scores of the row sit in the warp's slice
 // of shared memory so that any group size can be scanned; the arg-max rounds
 // run on registers as in the softmax router.
 constexpr int kSigMaxGroups = 128;
+
+// The selection score's sigmoid, correctly rounded to FP32 through FP64.
+__device__ __forceinline__ float sigmoid_rn(float x) { return (float)(1.0 / (1.0 + exp(-(double)x))); }
+
+// sigmoid_rn of every 16-bit logit pattern: [0] bf16, [1] f16.  Filled on the
+// device by sigmoid_table_kernel with the same arithmetic, so a lookup gives
+// the bits a per-element evaluation gives; 16-bit logits then need no FP64
+// exp per expert (FP64 runs at a small fraction of the FP32 rate here).
+__device__ float g_sigmoid16[2][65536];
+
+__global__ void sigmoid_table_kernel() {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= 2 * 65536) return;
+  const uint32_t b = (uint32_t)i & 0xFFFFu;
+  const float x = i < 65536 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((unsigned short)b));
+  g_sigmoid16[i >> 16][b] = sigmoid_rn(x);
+}
 
 template <typename T, int VPL>
 __global__ void __launch_bounds__(32 * kRowsPerBlock)
@@ -297,7 +317,10 @@ route_sigmoid_grouped_kernel(const T* __restrict__ logits, int64_t T_rows, int E
   for (int i = 0; i < VPL; ++i) {
     const int e = e0 + i;
     if (e < E) {
-      sg[i] = (float)(1.0 / (1.0 + exp(-(double)v[i])));
+      if constexpr (sizeof(T) == 2)
+        sg[i] = g_sigmoid16[std::is_same<T, __half>::value ? 1 : 0][bits16_of<T>(v[i])];
+      else
+        sg[i] = sigmoid_rn(v[i]);
       c[i] = sg[i] + (bias ? __ldg(bias + e) : 0.f);
       bad |= isnan(v[i]) || isnan(c[i]);
       c_row[e] = c[i];
@@ -487,11 +510,54 @@ router_backward_kernel(const T* __restrict__ logits, int64_t T_rows, int E,
   }
 }
 
+// Fills g_sigmoid16 before the first 16-bit sigmoid routing on a device, with
+// no host synchronisation: the first call enqueues the fill on its stream;
+// later calls on other streams wait for that fill's event until it is seen
+// complete.  A stream being captured into a graph gets a fill of its own in
+// the graph.  Refills write the same bits, so they cannot disturb a reader.
+cudaError_t ensure_sigmoid_table(cudaStream_t s) {
+  struct Fill {
+    cudaEvent_t done_ev = nullptr;
+    bool done = false;
+  };
+  static std::mutex mu;
+  static std::map<int, Fill> fills;
+  auto fill = [s]() {
+    sigmoid_table_kernel<<<2 * 65536 / 256, 256, 0, s>>>();
+    return cudaGetLastError();
+  };
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if ((e = cudaStreamIsCapturing(s, &cap)) != cudaSuccess) return e;
+  if (cap != cudaStreamCaptureStatusNone) return fill();
+  std::lock_guard<std::mutex> lock(mu);
+  Fill& f = fills[dev];
+  if (f.done) return cudaSuccess;
+  if (!f.done_ev) {
+    if ((e = fill()) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&f.done_ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+    return cudaEventRecord(f.done_ev, s);
+  }
+  e = cudaEventQuery(f.done_ev);
+  if (e == cudaSuccess) {
+    f.done = true;
+    return cudaSuccess;
+  }
+  if (e != cudaErrorNotReady) return e;
+  return cudaStreamWaitEvent(s, f.done_ev, 0);
+}
+
 template <typename T>
 cudaError_t launch_sigmoid_typed(const void* logits, int64_t T_rows, int E, const float* bias,
                                  int k, int groups, int sel_groups, int top_two, int renorm,
                                  float scale, uint32_t* idx, void* weights, float* w32,
                                  cudaStream_t s) {
+  if constexpr (sizeof(T) == 2) {
+    const cudaError_t e = ensure_sigmoid_table(s);
+    if (e != cudaSuccess) return e;
+  }
   dim3 grid((unsigned)((T_rows + kRowsPerBlock - 1) / kRowsPerBlock));
   dim3 block(32 * kRowsPerBlock);
   const size_t smem = (size_t)kRowsPerBlock * (E + 2 * kSigMaxGroups) * sizeof(float);
