@@ -15,6 +15,7 @@ method has) on the host cores, on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -581,11 +582,23 @@ def run_sigmoid(args, rank, world, local):
     torch.cuda.synchronize(dev)
     clock_info = clocks.stop(w0, time.time())
     ms = e0.elapsed_time(e1) / K
-    # the routing kernel alone
+    # the routing kernel alone: outputs allocated once and the C ABI called
+    # directly, so that the loop is not bound by per-call host work
+    from top_routing_grouped_fp32_gb300 import _lib
+    lib = moe.load()
+    ridx = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device=dev)
+    rw = torch.empty((wl.T, wl.top_k), dtype=inp["logits"].dtype, device=dev)
+    ropt = moe.group_options(wl.top_k, opts["groups"], opts["selected_groups"], opts["group_top_two"],
+                             opts["renormalize"], opts["scale"])
+    rargs = (inp["logits"].data_ptr(), moe._code(inp["logits"]), wl.T, wl.E, None, ctypes.byref(ropt),
+             ridx.data_ptr(), rw.data_ptr(), None, torch.cuda.current_stream(dev).cuda_stream)
+    for _ in range(3):
+        _lib.check(lib.moe_route_sigmoid_grouped(*rargs))
+    torch.cuda.synchronize(dev)
     r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     r0.record()
     for _ in range(K):
-        moe.moe_route_sigmoid_grouped(inp["logits"], wl.top_k, **opts)
+        lib.moe_route_sigmoid_grouped(*rargs)
     r1.record()
     torch.cuda.synchronize(dev)
     route_ms = r0.elapsed_time(r1) / K

@@ -24,6 +24,7 @@
 // agrees on each winner.
 #include <math.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <type_traits>
@@ -510,6 +511,168 @@ router_backward_kernel(const T* __restrict__ logits, int64_t T_rows, int E,
   }
 }
 
+// The same routing with the softmax router's layout: LPR lanes per row (a warp
+// routes 32/LPR rows), VPL values per lane in a blocked layout, for group
+// sizes gs that are VPL times a power of two: a group is then LG = gs/VPL
+// whole lanes.  A group's top-two score is each lane's top two, merged over
+// the group's lanes; the kept groups and the top_k experts come from
+// (score, id) arg-max butterflies over the row's lanes.  Every reduction is
+// over a strict order of (value, id) pairs or an exact max, so the result is
+// the oracle's sequential scan.  Other group sizes take the kernel above.
+template <typename T, int LPR, int VPL>
+__global__ void __launch_bounds__(32 * kRowsPerBlock)
+route_sigmoid_lanes_kernel(const T* __restrict__ logits, int64_t T_rows, int E,
+                           const float* __restrict__ bias, int k, int groups, int sel_groups,
+                           int top_two, int renorm, float scale, uint32_t* __restrict__ idx,
+                           T* __restrict__ w_out, float* __restrict__ w32) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int R = 32 / LPR;
+  constexpr int SLOTS = (64 + LPR - 1) / LPR;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % LPR;
+  const int64_t t = ((int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5)) * R + lane / LPR;
+  const bool live = t < T_rows;  // the whole warp stays for the shuffles
+  float v[VPL];
+  if (live) {
+    load_row<T, VPL>(logits + t * E, E, sub, v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) v[i] = -INFINITY;
+  }
+  const int e0 = sub * VPL;
+  float sg[VPL], c[VPL];
+  int bad = 0;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = e0 + i;
+    if (e < E) {
+      if constexpr (sizeof(T) == 2)
+        sg[i] = g_sigmoid16[std::is_same<T, __half>::value ? 1 : 0][bits16_of<T>(v[i])];
+      else
+        sg[i] = sigmoid_rn(v[i]);
+      c[i] = sg[i] + (bias ? __ldg(bias + e) : 0.f);
+      bad |= (isnan(v[i]) || isnan(c[i])) ? 1 : 0;
+    } else {
+      sg[i] = 0.f;
+      c[i] = -INFINITY;
+    }
+  }
+#pragma unroll
+  for (int d = LPR / 2; d > 0; d >>= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, d, LPR);
+
+  // group score: this lane's two largest corrected scores, merged over the
+  // LG lanes of its group (the two largest of a multiset of pairs)
+  const int gs = E / groups;
+  const int LG = gs / VPL;
+  const int my_g = sub / LG;
+  float b1 = -INFINITY, b2 = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    if (c[i] > b1) {
+      b2 = b1;
+      b1 = c[i];
+    } else if (c[i] > b2) {
+      b2 = c[i];
+    }
+  }
+  for (int d = 1; d < LG; d <<= 1) {
+    const float o1 = __shfl_xor_sync(0xffffffffu, b1, d, LPR);
+    const float o2 = __shfl_xor_sync(0xffffffffu, b2, d, LPR);
+    const float n2 = fmaxf(fminf(b1, o1), fmaxf(b2, o2));
+    b1 = fmaxf(b1, o1);
+    b2 = n2;
+  }
+  const float gscore = top_two ? b1 + b2 : b1;
+  // keep the sel_groups best groups; a group competes through its first lane
+  bool kept = false;
+  const bool leader = sub % LG == 0 && my_g < groups;
+  for (int r = 0; r < sel_groups; ++r) {
+    float bv = -INFINITY;
+    int bg = 0x7fffffff;
+    if (leader && !kept) {
+      bv = gscore;
+      bg = my_g;
+    }
+#pragma unroll
+    for (int d = LPR / 2; d > 0; d >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, d, LPR);
+      const int og = __shfl_xor_sync(0xffffffffu, bg, d, LPR);
+      if (beats(ov, og, bv, bg)) {
+        bv = ov;
+        bg = og;
+      }
+    }
+    kept |= bg == my_g;
+  }
+  // top_k experts of the kept groups by corrected score; slot j is kept by
+  // lane j % LPR of the row, in its register slot j / LPR
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (!kept || e0 + i >= E) taken |= 1u << i;
+  uint32_t my_idx[SLOTS];
+  float my_p[SLOTS];
+#pragma unroll
+  for (int h = 0; h < SLOTS; ++h) my_idx[h] = 0u, my_p[h] = 0.f;
+  float sel_sum = 0.f;
+  const int row_lane0 = lane - sub;
+#pragma unroll
+  for (int h = 0; h < SLOTS; ++h) {
+    if (h * LPR >= k) break;
+    const int jn = min(LPR, k - h * LPR);
+    for (int jj = 0; jj < jn; ++jj) {
+      float bv = -INFINITY, bs = 0.f;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        if (!(taken >> i & 1u) && beats(c[i], e0 + i, bv, bi)) {
+          bv = c[i];
+          bi = e0 + i;
+          bs = sg[i];
+        }
+      }
+#pragma unroll
+      for (int d = LPR / 2; d > 0; d >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, d, LPR);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, d, LPR);
+        if (beats(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      // the winner's sigmoid, from the lane that holds it
+      const int owner = row_lane0 + min(bi / VPL, LPR - 1);
+      const float p = __shfl_sync(0xffffffffu, bs, owner);
+      if (bi / VPL == sub) taken |= 1u << (bi % VPL);
+      sel_sum += p;  // every lane adds in slot order
+      if (jj == sub) {
+        my_idx[h] = (uint32_t)bi;
+        my_p[h] = p;
+      }
+    }
+  }
+  if (!live) return;
+  if (bad) {
+    for (int j = sub; j < k; j += LPR) {
+      idx[t * k + j] = (uint32_t)j;
+      w_out[t * k + j] = from_f32<T>(NAN);
+      if (w32) w32[t * k + j] = NAN;
+    }
+    return;
+  }
+#pragma unroll
+  for (int h = 0; h < SLOTS; ++h) {
+    const int j = h * LPR + sub;
+    if (j < k) {
+      const float w = (renorm ? my_p[h] / sel_sum : my_p[h]) * scale;
+      idx[t * k + j] = my_idx[h];
+      w_out[t * k + j] = from_f32<T>(w);
+      if (w32) w32[t * k + j] = w;
+    }
+  }
+}
+
 // Fills g_sigmoid16 before the first 16-bit sigmoid routing on a device, with
 // no host synchronisation: the first call enqueues the fill on its stream;
 // later calls on other streams wait for that fill's event until it is seen
@@ -522,6 +685,7 @@ cudaError_t ensure_sigmoid_table(cudaStream_t s) {
   };
   static std::mutex mu;
   static std::map<int, Fill> fills;
+  static std::atomic<uint64_t> done_mask{0};  // devices 0..63 whose fill is known complete
   auto fill = [s]() {
     sigmoid_table_kernel<<<2 * 65536 / 256, 256, 0, s>>>();
     return cudaGetLastError();
@@ -529,6 +693,7 @@ cudaError_t ensure_sigmoid_table(cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 64 && (done_mask.load(std::memory_order_acquire) >> dev & 1u)) return cudaSuccess;
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if ((e = cudaStreamIsCapturing(s, &cap)) != cudaSuccess) return e;
   if (cap != cudaStreamCaptureStatusNone) return fill();
@@ -543,6 +708,7 @@ cudaError_t ensure_sigmoid_table(cudaStream_t s) {
   e = cudaEventQuery(f.done_ev);
   if (e == cudaSuccess) {
     f.done = true;
+    if (dev < 64) done_mask.fetch_or(1ull << dev, std::memory_order_release);
     return cudaSuccess;
   }
   if (e != cudaErrorNotReady) return e;
@@ -557,6 +723,34 @@ cudaError_t launch_sigmoid_typed(const void* logits, int64_t T_rows, int E, cons
   if constexpr (sizeof(T) == 2) {
     const cudaError_t e = ensure_sigmoid_table(s);
     if (e != cudaSuccess) return e;
+  }
+  {
+    // the lanes layout of the softmax router, when a group is a power-of-two
+    // number of whole lanes
+    const T* l = static_cast<const T*>(logits);
+    T* w = static_cast<T*>(weights);
+    const int gs = E / groups;
+    auto go = [&](auto kernel, int lpr, int vpl) -> int {
+      if (gs % vpl != 0) return 0;
+      const int lg = gs / vpl;
+      if ((lg & (lg - 1)) != 0 || lg > lpr) return 0;
+      const int64_t rows_per_block = (int64_t)kRowsPerBlock * (32 / lpr);
+      dim3 grid((unsigned)((T_rows + rows_per_block - 1) / rows_per_block));
+      const cudaError_t e = launch_pdl(kernel, grid, dim3(32 * kRowsPerBlock), 0, s, l, T_rows, E, bias, k,
+                                       groups, sel_groups, top_two, renorm, scale, idx, w, w32);
+      return e == cudaSuccess ? 1 : -(int)e;
+    };
+    int r;
+    if (E <= 8) r = go(route_sigmoid_lanes_kernel<T, 8, 1>, 8, 1);
+    else if (E <= 16) r = go(route_sigmoid_lanes_kernel<T, 8, 2>, 8, 2);
+    else if (E <= 32) r = go(route_sigmoid_lanes_kernel<T, 8, 4>, 8, 4);
+    else if (E <= 64) r = go(route_sigmoid_lanes_kernel<T, 8, 8>, 8, 8);
+    else if (E <= 128) r = go(route_sigmoid_lanes_kernel<T, 16, 8>, 16, 8);
+    else if (E <= 256) r = go(route_sigmoid_lanes_kernel<T, 32, 8>, 32, 8);
+    else if (E <= 512) r = go(route_sigmoid_lanes_kernel<T, 32, 16>, 32, 16);
+    else r = go(route_sigmoid_lanes_kernel<T, 32, 32>, 32, 32);
+    if (r == 1) return cudaSuccess;
+    if (r < 0) return (cudaError_t)(-r);
   }
   dim3 grid((unsigned)((T_rows + kRowsPerBlock - 1) / kRowsPerBlock));
   dim3 block(32 * kRowsPerBlock);
