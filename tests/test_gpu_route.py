@@ -68,6 +68,32 @@ def test_route_ties_at_scale(cuda_lib):
         _check(cuda_lib, logits, k, True)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_route_every_16bit_logit(cuda_lib, dtype):
+    """Every 16-bit pattern except NaN and +inf once, 64 to a row and all 64 selected:
+    the indices give the full selection order (subnormals, -0 against +0, -inf,
+    saturated weights) against the oracle's."""
+    bits = torch.from_numpy(np.random.default_rng(11).permutation(65536).astype(np.int16))
+    logits = bits.view(TORCH_DTYPES[dtype]).clone()
+    logits[torch.isnan(logits) | (logits == float("inf"))] = 0.0
+    _check(cuda_lib, logits.view(1024, 64).cuda(), 64, False)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_route_minus_inf_picks_and_padding(cuda_lib, dtype):
+    """E = 37 leaves padding entries in the last lane of a row; rows with fewer finite
+    logits than k must pick real -inf experts, lowest id first, never padding."""
+    g = torch.Generator(device="cuda").manual_seed(13)
+    logits = torch.full((64, 37), float("-inf"), device="cuda")
+    for r in range(64):
+        n = r % 5  # 0..4 finite logits, k = 8
+        cols = torch.randperm(37, generator=g, device="cuda")[:n]
+        logits[r, cols] = torch.randn(n, generator=g, device="cuda")
+    logits[0, 36] = 1.0  # keep row 0 from being all -inf (that row is poisoned)
+    got, _ = _check(cuda_lib, logits.to(TORCH_DTYPES[dtype]), 8, True)
+    assert (got < 37).all()
+
+
 def test_route_nan_rule(cuda_lib):
     rows = [
         [0.0, float("nan"), 1.0, 2.0, -1.0],
