@@ -39,6 +39,31 @@ __device__ __forceinline__ void load8(const T* p, float* f) {
   }
 }
 
+// 8 elements as raw bits: one 16-byte vector (16-bit types) or two (FP32)
+template <typename T>
+struct Raw8 {
+  uint4 q[sizeof(T) == 2 ? 1 : 2];
+};
+template <typename T, bool STREAM>
+__device__ __forceinline__ Raw8<T> load_raw8(const T* p) {
+  Raw8<T> r;
+  const uint4* s = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < (sizeof(T) == 2 ? 1 : 2); ++i) r.q[i] = STREAM ? __ldcs(s + i) : __ldg(s + i);
+  return r;
+}
+template <typename T>
+__device__ __forceinline__ void unpack_raw8(const Raw8<T>& r, float* f) {
+  if constexpr (sizeof(T) == 2) {
+    unpack8<T>(r.q[0], f);
+  } else {
+    f[0] = __uint_as_float(r.q[0].x); f[1] = __uint_as_float(r.q[0].y);
+    f[2] = __uint_as_float(r.q[0].z); f[3] = __uint_as_float(r.q[0].w);
+    f[4] = __uint_as_float(r.q[1].x); f[5] = __uint_as_float(r.q[1].y);
+    f[6] = __uint_as_float(r.q[1].z); f[7] = __uint_as_float(r.q[1].w);
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ void store8(T* p, const float* f) {
   if constexpr (sizeof(T) == 2) {
@@ -52,8 +77,10 @@ __device__ __forceinline__ void store8(T* p, const float* f) {
 // WEIGHTED: y[t] = sum_j w[t,j] * src[slot_row[t*k+j]]   (moe_combine)
 // !WEIGHTED: y[t] = sum_j src[t*k+j]                      (fused forward)
 // VEC: H % 8 == 0 and 16-byte aligned rows, else one column per thread.
+constexpr int kBatch = 4;  // slots whose rows are loaded together in the weighted combine
+
 template <typename T, bool WEIGHTED, bool VEC>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 combine_kernel(const T* __restrict__ src, const uint32_t* __restrict__ slot_row,
                const void* __restrict__ w, int wdt, int64_t T_rows, int k, int64_t H,
                T* __restrict__ y) {
@@ -68,7 +95,48 @@ combine_kernel(const T* __restrict__ src, const uint32_t* __restrict__ slot_row,
   float acc[C];
 #pragma unroll
   for (int i = 0; i < C; ++i) acc[i] = 0.f;
-  for (int j = 0; j < k; ++j) {
+  if constexpr (WEIGHTED) {
+    // kBatch slots at a time: their row indices, then their rows, are loaded
+    // together, and then added in slot order (the sum's order is unchanged)
+    for (int j0 = 0; j0 < k; j0 += kBatch) {
+      uint32_t rr[kBatch];
+      float ww[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        rr[q] = kInvalid;
+        ww[q] = 1.f;
+        if (j0 + q < k) {
+          rr[q] = __ldg(slot_row + t * k + j0 + q);
+          if (w) ww[q] = load_dyn(w, wdt, (size_t)(t * k + j0 + q));  // no weights: dispatch backward
+        }
+      }
+      // raw loads first, so that all of them are in flight before any is used
+      Raw8<T> raw[VEC ? kBatch : 1];
+      T one[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        if (j0 + q < k && rr[q] != kInvalid) {
+          if constexpr (VEC) raw[q] = load_raw8<T, true>(src + (int64_t)rr[q] * H + c0);
+          else one[q] = src[(int64_t)rr[q] * H + c0];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        if (j0 + q >= k) break;
+        if (rr[q] == kInvalid) {
+#pragma unroll
+          for (int i = 0; i < C; ++i) acc[i] = NAN;
+        } else {
+          float v[C];
+          if constexpr (VEC) unpack_raw8<T>(raw[q], v);
+          else v[0] = to_f32<T>(one[q]);
+#pragma unroll
+          for (int i = 0; i < C; ++i) acc[i] += ww[q] * v[i];
+        }
+      }
+    }
+  }
+  for (int j = 0; !WEIGHTED && j < k; ++j) {
     int64_t row;
     float wj = 1.f;
     if constexpr (WEIGHTED) {
@@ -119,11 +187,16 @@ cudaError_t launch_combine_t(const void* src, const uint32_t* slot_row, const vo
 // The dot product is summed per lane in column order, then by a butterfly
 // (a fixed order).  Rows holding no slot get dexpert = 0; slots no row holds
 // keep the NaN the caller's buffer was filled with.
-template <typename T>
+// VEC (H % 8 == 0, 16-byte aligned rows): each lane takes 8-column vectors
+// lane, lane+32, ..., four in flight; its dot product runs over its vectors in
+// order and over the 8 columns of each in order, then the butterfly.
+template <typename T, bool VEC>
 __global__ void __launch_bounds__(256)
 combine_backward_kernel(const T* __restrict__ eo, const uint32_t* __restrict__ perm,
                         const void* __restrict__ w, int wdt, const T* __restrict__ dy, int64_t N,
                         int k, int64_t H, T* __restrict__ dexpert, float* __restrict__ dweights) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (r >= N) return;
@@ -138,10 +211,40 @@ combine_backward_kernel(const T* __restrict__ eo, const uint32_t* __restrict__ p
   const T* src = eo + r * H;
   const T* g = dy + t * H;
   float dot = 0.f;
-  for (int64_t c = lane; c < H; c += 32) {
-    const float gv = to_f32<T>(g[c]);
-    dst[c] = from_f32<T>(wv * gv);
-    dot = fmaf(to_f32<T>(src[c]), gv, dot);
+  if constexpr (VEC) {
+    const int64_t nv = H / 8;
+    for (int64_t v0 = 0; v0 < nv; v0 += 4 * 32) {
+      Raw8<T> ra[4], rb[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t v = v0 + q * 32 + lane;
+        if (v < nv) {
+          ra[q] = load_raw8<T, true>(src + v * 8);
+          rb[q] = load_raw8<T, false>(g + v * 8);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t v = v0 + q * 32 + lane;
+        if (v < nv) {
+          float a[8], b[8], o[8];
+          unpack_raw8<T>(ra[q], a);
+          unpack_raw8<T>(rb[q], b);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            o[i] = wv * b[i];
+            dot = fmaf(a[i], b[i], dot);
+          }
+          store8<T>(dst + v * 8, o);
+        }
+      }
+    }
+  } else {
+    for (int64_t c = lane; c < H; c += 32) {
+      const float gv = to_f32<T>(g[c]);
+      dst[c] = from_f32<T>(wv * gv);
+      dot = fmaf(to_f32<T>(src[c]), gv, dot);
+    }
   }
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, d);
@@ -183,24 +286,23 @@ cudaError_t launch_combine_backward(const void* expert_out, moe_dtype dt, const 
   cudaError_t err = cudaMemsetAsync(dweights, 0xFF, (size_t)N * sizeof(float), s);  // NaN
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)((N + 7) / 8);
+  const bool vec = H % 8 == 0 && reinterpret_cast<uintptr_t>(expert_out) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(dy) % 16 == 0 && reinterpret_cast<uintptr_t>(dexpert) % 16 == 0;
+  auto go = [&](auto tag) {
+    using T = decltype(tag);
+    const T* eo = static_cast<const T*>(expert_out);
+    const T* g = static_cast<const T*>(dy);
+    T* dx = static_cast<T*>(dexpert);
+    return vec ? launch_pdl(combine_backward_kernel<T, true>, dim3(grid), dim3(256), 0, s, eo, perm, weights,
+                            (int)wdt, g, N, k, H, dx, dweights)
+               : launch_pdl(combine_backward_kernel<T, false>, dim3(grid), dim3(256), 0, s, eo, perm, weights,
+                            (int)wdt, g, N, k, H, dx, dweights);
+  };
   switch (dt) {
-    case MOE_F32:
-      combine_backward_kernel<float><<<grid, 256, 0, s>>>(
-          static_cast<const float*>(expert_out), perm, weights, (int)wdt,
-          static_cast<const float*>(dy), N, k, H, static_cast<float*>(dexpert), dweights);
-      break;
-    case MOE_F16:
-      combine_backward_kernel<__half><<<grid, 256, 0, s>>>(
-          static_cast<const __half*>(expert_out), perm, weights, (int)wdt,
-          static_cast<const __half*>(dy), N, k, H, static_cast<__half*>(dexpert), dweights);
-      break;
-    default:
-      combine_backward_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(expert_out), perm, weights, (int)wdt,
-          static_cast<const __nv_bfloat16*>(dy), N, k, H, static_cast<__nv_bfloat16*>(dexpert),
-          dweights);
+    case MOE_F32: return go(float{});
+    case MOE_F16: return go(__half{});
+    default: return go(__nv_bfloat16{});
   }
-  return cudaGetLastError();
 }
 
 }  // namespace moe
