@@ -74,12 +74,48 @@ __device__ __forceinline__ void store8(T* p, const float* f) {
   }
 }
 
-// WEIGHTED: y[t] = sum_j w[t,j] * src[slot_row[t*k+j]]   (moe_combine)
-// !WEIGHTED: y[t] = sum_j src[t*k+j]                      (fused forward)
-// VEC: H % 8 == 0 and 16-byte aligned rows, else one column per thread.
+// y[t] = sum_j src[t*k+j], j in order (the fused forward's combine of the
+// weighted slot rows).  VEC: H % 8 == 0 and 16-byte aligned rows, else one
+// column per thread.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(256)
+slot_sum_kernel(const T* __restrict__ src, int64_t T_rows, int k, int64_t H, T* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int C = VEC ? 8 : 1;
+  const int64_t groups = H / C;
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= T_rows * groups) return;
+  const int64_t t = gid / groups;
+  const int64_t c0 = (gid - t * groups) * C;
+  float acc[C];
+#pragma unroll
+  for (int i = 0; i < C; ++i) acc[i] = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const int64_t row = t * k + j;
+    float v[C];
+    if constexpr (VEC) {
+      load8<T>(src + row * H + c0, v);
+    } else {
+      v[0] = to_f32<T>(src[row * H + c0]);
+    }
+#pragma unroll
+    for (int i = 0; i < C; ++i) acc[i] += v[i];
+  }
+  if constexpr (VEC) {
+    store8<T>(y + t * H + c0, acc);
+  } else {
+    y[t * H + c0] = from_f32<T>(acc[0]);
+  }
+}
+
 constexpr int kBatch = 4;  // slots whose rows are loaded together in the weighted combine
 
-template <typename T, bool WEIGHTED, bool VEC>
+// y[t] = sum_j w[t,j] * src[slot_row[t*k+j]], j in order (moe_combine; with
+// no weights, the dispatch backward).  kBatch slots at a time: their row
+// indices, then their raw rows, are loaded together and then added in slot
+// order.  An undispatched slot makes the row NaN.
+template <typename T, bool VEC>
 __global__ void __launch_bounds__(256, 4)
 combine_kernel(const T* __restrict__ src, const uint32_t* __restrict__ slot_row,
                const void* __restrict__ w, int wdt, int64_t T_rows, int k, int64_t H,
@@ -95,70 +131,42 @@ combine_kernel(const T* __restrict__ src, const uint32_t* __restrict__ slot_row,
   float acc[C];
 #pragma unroll
   for (int i = 0; i < C; ++i) acc[i] = 0.f;
-  if constexpr (WEIGHTED) {
-    // kBatch slots at a time: their row indices, then their rows, are loaded
-    // together, and then added in slot order (the sum's order is unchanged)
-    for (int j0 = 0; j0 < k; j0 += kBatch) {
-      uint32_t rr[kBatch];
-      float ww[kBatch];
+  for (int j0 = 0; j0 < k; j0 += kBatch) {
+    uint32_t rr[kBatch];
+    float ww[kBatch];
 #pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        rr[q] = kInvalid;
-        ww[q] = 1.f;
-        if (j0 + q < k) {
-          rr[q] = __ldg(slot_row + t * k + j0 + q);
-          if (w) ww[q] = load_dyn(w, wdt, (size_t)(t * k + j0 + q));  // no weights: dispatch backward
-        }
-      }
-      // raw loads first, so that all of them are in flight before any is used
-      Raw8<T> raw[VEC ? kBatch : 1];
-      T one[kBatch];
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        if (j0 + q < k && rr[q] != kInvalid) {
-          if constexpr (VEC) raw[q] = load_raw8<T, true>(src + (int64_t)rr[q] * H + c0);
-          else one[q] = src[(int64_t)rr[q] * H + c0];
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        if (j0 + q >= k) break;
-        if (rr[q] == kInvalid) {
-#pragma unroll
-          for (int i = 0; i < C; ++i) acc[i] = NAN;
-        } else {
-          float v[C];
-          if constexpr (VEC) unpack_raw8<T>(raw[q], v);
-          else v[0] = to_f32<T>(one[q]);
-#pragma unroll
-          for (int i = 0; i < C; ++i) acc[i] += ww[q] * v[i];
-        }
+    for (int q = 0; q < kBatch; ++q) {
+      rr[q] = kInvalid;
+      ww[q] = 1.f;
+      if (j0 + q < k) {
+        rr[q] = __ldg(slot_row + t * k + j0 + q);
+        if (w) ww[q] = load_dyn(w, wdt, (size_t)(t * k + j0 + q));
       }
     }
-  }
-  for (int j = 0; !WEIGHTED && j < k; ++j) {
-    int64_t row;
-    float wj = 1.f;
-    if constexpr (WEIGHTED) {
-      const uint32_t r = __ldg(slot_row + t * k + j);
-      wj = w ? load_dyn(w, wdt, (size_t)(t * k + j)) : 1.f;  // no weights: dispatch backward
-      if (r == kInvalid) {
+    // raw loads first, so that all of them are in flight before any is used
+    Raw8<T> raw[VEC ? kBatch : 1];
+    T one[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      if (j0 + q < k && rr[q] != kInvalid) {
+        if constexpr (VEC) raw[q] = load_raw8<T, true>(src + (int64_t)rr[q] * H + c0);
+        else one[q] = src[(int64_t)rr[q] * H + c0];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      if (j0 + q >= k) break;
+      if (rr[q] == kInvalid) {
 #pragma unroll
         for (int i = 0; i < C; ++i) acc[i] = NAN;
-        continue;
-      }
-      row = r;
-    } else {
-      row = t * k + j;
-    }
-    float v[C];
-    if constexpr (VEC) {
-      load8<T>(src + row * H + c0, v);
-    } else {
-      v[0] = to_f32<T>(src[row * H + c0]);
-    }
+      } else {
+        float v[C];
+        if constexpr (VEC) unpack_raw8<T>(raw[q], v);
+        else v[0] = to_f32<T>(one[q]);
 #pragma unroll
-    for (int i = 0; i < C; ++i) acc[i] += WEIGHTED ? wj * v[i] : v[i];
+        for (int i = 0; i < C; ++i) acc[i] += ww[q] * v[i];
+      }
+    }
   }
   if constexpr (VEC) {
     store8<T>(y + t * H + c0, acc);
@@ -174,11 +182,18 @@ cudaError_t launch_combine_t(const void* src, const uint32_t* slot_row, const vo
                    reinterpret_cast<uintptr_t>(y) % 16 == 0;
   const int64_t work = T_rows * (vec ? H / 8 : H);
   const unsigned grid = (unsigned)((work + 255) / 256);
-  if (vec)
-    return launch_pdl(combine_kernel<T, WEIGHTED, true>, dim3(grid), dim3(256), 0, s,
-                      static_cast<const T*>(src), slot_row, w, (int)wdt, T_rows, k, H, static_cast<T*>(y));
-  return launch_pdl(combine_kernel<T, WEIGHTED, false>, dim3(grid), dim3(256), 0, s,
-                    static_cast<const T*>(src), slot_row, w, (int)wdt, T_rows, k, H, static_cast<T*>(y));
+  const T* sp = static_cast<const T*>(src);
+  T* yp = static_cast<T*>(y);
+  if constexpr (WEIGHTED) {
+    if (vec)
+      return launch_pdl(combine_kernel<T, true>, dim3(grid), dim3(256), 0, s, sp, slot_row, w, (int)wdt,
+                        T_rows, k, H, yp);
+    return launch_pdl(combine_kernel<T, false>, dim3(grid), dim3(256), 0, s, sp, slot_row, w, (int)wdt,
+                      T_rows, k, H, yp);
+  } else {
+    if (vec) return launch_pdl(slot_sum_kernel<T, true>, dim3(grid), dim3(256), 0, s, sp, T_rows, k, H, yp);
+    return launch_pdl(slot_sum_kernel<T, false>, dim3(grid), dim3(256), 0, s, sp, T_rows, k, H, yp);
+  }
 }
 
 // Combine backward (user guide, section 12: combine_backward gives dexpert and
