@@ -43,8 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch of the gate/up GEMM on the headline workload, from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel source it was taken on; reported as null once the source changes.
-GATEUP_TRAFFIC = {"workload": "finegrained_bf16", "bytes": 1140995584 + 263942144,
-                  "source_sha256": "0aa5f00349626cb9834a0f8e2bfbd2921864465a4c32b6e3952386586bf40caa"}
+GATEUP_TRAFFIC = {"workload": "finegrained_bf16", "bytes": 1178498560 + 266697472,
+                  "source_sha256": "18b93dfd4ad596e2ff1dd23aaf06fd7770269f6799b340aa63409ecf23927126"}
 
 
 def parse_args(argv=None):

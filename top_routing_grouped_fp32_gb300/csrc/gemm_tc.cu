@@ -1334,7 +1334,13 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, c
   // expert (decode-sized batches) the GEMM streams weights from HBM and single
   // CTAs keep twice as many independent streams in flight.
   const bool pair = a.N >= (int64_t)tc::BM * a.E;
-  if (pair) {  // 128-deep k-blocks: two 64-deep sub-blocks per ring stage
+  if (pair && a.mode != kGateUpSwiglu) {
+    // down projection: six 64-deep stages rather than three 128-deep ones (the
+    // same ring bytes); measured equal at K = 1408 and 5 % faster at K = 14336
+    if (a.dt == MOE_BF16) return tc::launch_t<__nv_bfloat16, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
+    return tc::launch_t<__half, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
+  }
+  if (pair) {  // gate/up: 128-deep k-blocks, two 64-deep sub-blocks per ring stage
     p.k_blocks = (int)((a.K + 2 * tc::BK - 1) / (2 * tc::BK));
     if (a.dt == MOE_BF16)
       return tc::launch_t<__nv_bfloat16, 2, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
