@@ -103,6 +103,11 @@ moe_status moe_route(const void* logits, moe_dtype logits_dtype, int64_t T, int6
  * 1 <= selected_groups <= groups, 1 <= top_k <= 64 and top_k <=
  * selected_groups * E/groups, group_top_two needs E/groups >= 2, scale
  * finite and > 0.  Outputs as for moe_route.
+ * With F16/BF16 logits the sigmoid is read from a device table of all 65536
+ * patterns.  The first such call on a device enqueues the table's fill on
+ * its stream, and later calls on other streams wait for that fill (a stream
+ * event, no host synchronisation).  A stream being captured into a CUDA
+ * graph gets a fill of its own in the graph.
  * ---------------------------------------------------------------------- */
 typedef struct {
     int32_t top_k;
