@@ -179,22 +179,28 @@ scatter_kernel(const uint32_t* __restrict__ idx, int64_t T, int E, int k,
     __shared__ uint32_t warp_sums[32];
     __shared__ uint32_t s_valid;
     // per expert (and the invalid column E): the total over all chunks and
-    // the part in the chunks before this one; a warp per expert, lanes over chunks
-    for (int e = w; e <= E; e += kWarps) {
-      uint32_t tot = 0, pre = 0;
-      for (int b = lane; b < nchunks; b += 32) {
-        const uint32_t v = __ldg(chunk_counts + (size_t)b * (E + 1) + e);
-        tot += v;
-        pre += b < (int)blockIdx.x ? v : 0u;
+    // the part in the chunks before this one.  The table is read flat, 8
+    // words per thread in flight, and summed with shared-memory integer
+    // atomics (exact in any order).
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) s_tot[i] = s_base[i] = 0u;
+    __syncthreads();
+    const int64_t words = (int64_t)nchunks * (E + 1);
+    const int64_t before = (int64_t)blockIdx.x * (E + 1);  // flat indices of earlier chunks
+    for (int64_t f0 = threadIdx.x; f0 < words; f0 += 8 * (int64_t)blockDim.x) {
+      uint32_t v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int64_t f = f0 + q * (int64_t)blockDim.x;
+        v[q] = f < words ? __ldg(chunk_counts + f) : 0u;
       }
 #pragma unroll
-      for (int d = 16; d > 0; d >>= 1) {
-        tot += __shfl_xor_sync(0xffffffffu, tot, d);
-        pre += __shfl_xor_sync(0xffffffffu, pre, d);
-      }
-      if (lane == 0) {
-        s_tot[e] = tot;
-        s_base[e] = pre;
+      for (int q = 0; q < 8; ++q) {
+        const int64_t f = f0 + q * (int64_t)blockDim.x;
+        if (v[q] != 0u) {
+          const int e = (int)(f % (E + 1));
+          atomicAdd(&s_tot[e], v[q]);
+          if (f < before) atomicAdd(&s_base[e], v[q]);
+        }
       }
     }
     __syncthreads();
