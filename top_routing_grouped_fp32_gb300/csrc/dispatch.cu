@@ -21,8 +21,12 @@
 //              consecutive slots per step; __match_any_sync ranks equal
 //              experts among the lanes, so ranks follow s exactly, duplicates
 //              included.  A first pass counts per warp, a second writes
-//              perm/row_experts.
-// A fourth kernel gathers x rows into x_disp, one warp per dispatched row.
+//              perm/row_experts (and slot_row, the inverse of perm, for the
+//              fused forward).
+// A fourth kernel gathers x rows into x_disp: in the fused forward one warp
+// per token, which reads the token's row once and writes its top_k rows;
+// in moe_dispatch (and for rows that are not whole 16-byte vectors) one
+// warp per dispatched row.
 #include <mutex>
 
 #include "common.cuh"
