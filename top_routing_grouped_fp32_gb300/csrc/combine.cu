@@ -6,9 +6,10 @@
 // with FP32 accumulation in ascending j (a fixed order, so the result is
 // bit-reproducible), rounded once to the output dtype.
 //
-// All kernels are HBM-bound streaming passes: each thread owns 8 consecutive
+// The combines are HBM-bound streaming passes: each thread owns 8 consecutive
 // columns of one token (one 16-byte vector for 16-bit types, two for FP32)
-// and reads the k source rows of that token.
+// and reads the k source rows of that token.  The combine backward (section
+// 12) is one warp per dispatched row with 8-column vectors per lane.
 #include <math.h>
 
 #include "common.cuh"
