@@ -1,13 +1,22 @@
 """Benchmark of the fused local MoE forward on the fine-grained headline workload.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload NAME] [--no-cpu-baseline]
+                    [--workload NAME] [--dtype f16] [--l2-flush] [--no-cpu-baseline]
 
 One step = one moe_forward (route -> dispatch -> grouped gate/up + SwiGLU ->
 grouped down with weighted un-permute -> combine) over T tokens whose inputs
 are already resident in HBM.  Prints ONE JSON line (rank 0).  Under torchrun
 each rank runs the same workload on its own GPU (tokens are independent, so
 ranks need no data exchange: weak scaling); the time is the max over ranks.
+
+Exactly K steps are timed between a barrier and device synchronisations; when
+K steps take less than --min-seconds (0.5 s), that timed loop is repeated so
+that the nvidia-smi sampler (50 ms) records at least ~10 clock samples inside
+the window, and the per-step figures are the mean over all repetitions.  The
+roofline's peak follows that clock record: the burst BF16 figure when the
+median SM clock sat at its maximum with no sw_power_cap sample, else the
+sustained one.  The default run then measures the other four workloads and
+the headline in FP16 the same way, under the line's "workloads" key.
 
 ``--impl reference`` times the FP64 CPU oracle (the only reference this
 method has) on the host cores, on a bounded sample of the same workload.
@@ -18,6 +27,7 @@ import argparse
 import ctypes
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -40,17 +50,17 @@ def launches_per_step(T: int, E: int) -> int:
     return 7 + (1 if chunks * (E + 1) > 16384 else 0)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic per launch of the gate/up GEMM on the headline workload, from one
-# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
-# of the kernel source it was taken on; reported as null once the source changes.
-GATEUP_TRAFFIC = {"workload": "finegrained_bf16", "bytes": 1178498560 + 266697472,
-                  "source_sha256": "18b93dfd4ad596e2ff1dd23aaf06fd7770269f6799b340aa63409ecf23927126"}
+# DRAM traffic per grouped_gemm_tc launch (mean of the gate/up and the down
+# launch, dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
+# each workload, with the SHA-256 of the kernel source it was taken on; it is
+# reported as null once that source changes.
+GEMM_TRAFFIC = {}
 
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=600)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--mode", choices=["forward", "backward"], default="forward",
@@ -67,9 +77,18 @@ def parse_args(argv=None):
     p.add_argument("--tokens", type=int, default=None,
                    help="override the workload's token count (small cases for profiler captures)")
     p.add_argument("--e2e-steps", type=int, default=None,
-                   help="steps of the host-buffer legs (default: --steps, so that they run as long "
-                        "as the device-resident loop and see the same power-capped clocks)")
+                   help="steps of the host-buffer legs (default: the device loop's steps x repeats, so "
+                        "that they run as long and see the same clocks)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the other workloads measured after the headline in the default run")
+    p.add_argument("--min-seconds", type=float, default=0.5,
+                   help="repeat the K timed steps until this much timed work (clock samples >= 10)")
+    p.add_argument("--side-steps", type=int, default=20, help="timed steps per repetition, other workloads")
+    p.add_argument("--side-seconds", type=float, default=0.5, help="--min-seconds of the other workloads")
+    p.add_argument("--l2-flush", action="store_true",
+                   help="write a 256 MB buffer before every step (outside the forward's events); "
+                        "the per-step time is then the forward's own event span")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target wall time of the oracle sample")
     return p.parse_args(argv)
@@ -269,88 +288,196 @@ def run_reference(args, rank, world):
     return 0
 
 
-def workload_config(wl):
+def workload_config(wl, l2_flush=False):
+    s = 4 if wl.dtype == "f32" else 2
+    if l2_flush:
+        l2 = "flushed: a 256 MB buffer is written before every step (outside the timed events)"
+    else:
+        l2 = ("no flush: every step streams all expert weights "
+              f"({3 * wl.E * wl.H * wl.I * s / 1e9:.3g} GB) and the dispatched rows; above the "
+              "129 MB L2 for every workload but the tiny one, which is launch-bound")
     return {"workload": wl.name, "T": wl.T, "E": wl.E, "top_k": wl.top_k, "H": wl.H, "I": wl.I,
-            "renormalize": wl.renormalize, "seed": wl.seed, "weights_dtype": wl.dtype,
-            "l2": ("no flush: every step streams all expert weights "
-                   f"({3 * wl.E * wl.H * wl.I * 2 / 1e9:.2f} GB) and the dispatched rows, "
-                   "far above the 129 MB L2")}
+            "renormalize": wl.renormalize, "seed": wl.seed, "weights_dtype": wl.dtype, "l2": l2}
 
 
 # --------------------------------------------------------------------------
 # native arm
 # --------------------------------------------------------------------------
 
-def run_native(args, rank, world, local):
-    import torch
-    import top_routing_grouped_fp32_gb300 as moe
-    from top_routing_grouped_fp32_gb300.inputs import WORKLOADS, make_inputs, with_dtype
+# workloads measured after the headline in the default run, each a few hundred
+# milliseconds: (workload, dtype override)
+SIDE_WORKLOADS = [("mixtral_bf16", None), ("skewed_bf16", None), ("decode_bf16", None),
+                  ("tiny_fp32", None), ("finegrained_bf16", "f16")]
+STAGES = ["route", "dispatch", "gate_up_gemm", "down_gemm", "combine"]
+L2_FLUSH_BYTES = 256 << 20
 
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA device (the native arm has no CPU path)")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    moe.load()
-    wl = bench_workload(args)
+
+def tensor_peak(peaks, src, clocks):
+    """The BF16 tensor peak that matches the timed window's own clock record:
+    the burst figure when the median SM clock sat at its maximum and no
+    sw_power_cap sample fell inside the window (or no record exists), else the
+    sustained figure measured under the power cap."""
+    burst = float(peaks["bf16_tflops"])
+    sus = float(peaks.get("bf16_tflops_sustained", burst))
+    sm, smax = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    capped = "sw_power_cap" in clocks.get("reasons", [])
+    if sm is None or smax is None:
+        return burst, f"{src} bf16_tflops (burst; no clock record for the window)"
+    if sm >= smax - 15 and not capped:
+        return burst, f"{src} bf16_tflops (burst: median SM clock {sm:.0f} of {smax:.0f} MHz, no sw_power_cap)"
+    why = "sw_power_cap active" if capped else "clock below max"
+    return sus, (f"{src} bf16_tflops_sustained (median SM clock {sm:.0f} of {smax:.0f} MHz, {why})")
+
+
+def roofline_for(wl, stage, touched, clocks, peaks, peaks_src, traffic=None):
+    """Roofline of the dominant kernel, grouped_gemm_tc (its two launches per
+    step: gate/up + SwiGLU and down + weighted un-permute).  Tensor-bound
+    workloads: 6*N*H*I FLOP over the two launches' summed time against the BF16
+    peak that the clock record selects.  The decode workload streams weights:
+    the touched experts' 3*H*I weights over the same time against the measured
+    copy bandwidth.  FP32 experts run on the FFMA pipe: against 152 SMs x 128
+    lanes x 2 FLOP x the max SM clock."""
+    N = wl.T * wl.top_k
+    t_gu, t_dn = stage["gate_up_gemm"], stage["down_gemm"]
+    gemm_s = (t_gu + t_dn) * 1e-3
+    flops = 6.0 * N * wl.H * wl.I
+    s_el = 4 if wl.dtype == "f32" else 2
+    wbytes = touched * 3.0 * wl.H * wl.I * s_el
+    hbm = float(peaks["hbm_gbs"])
+    if wl.dtype == "f32":
+        smax = clocks.get("sm_max_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+        peak = 152 * 128 * 2 * smax * 1e6 / 1e12
+        ach = flops / gemm_s / 1e12
+        return {"bound": "alu", "kernel": "grouped_gemm_simt (FP32 FFMA, gate/up + down)", "achieved": ach,
+                "peak": peak, "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                "peak_source": f"152 SMs x 128 FP32 lanes x 2 FLOP x {smax:.0f} MHz",
+                "algorithmic_per_launch": f"6*N*H*I / 2 launches = {flops / 2:.4e} FLOP"}
+    if wl.name.startswith("decode"):
+        ach = wbytes / gemm_s / 1e9
+        return {"bound": "hbm", "kernel": "grouped_gemm_tc (gate/up + SwiGLU, down + weighted un-permute)",
+                "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": traffic,
+                "peak_source": f"{peaks_src} hbm_gbs",
+                "algorithmic_per_launch": (f"touched experts' weights 3*H*I*2 x {touched} / 2 launches = "
+                                           f"{wbytes / 2:.4e} B"),
+                "gate_up_only": {"achieved": touched * 2.0 * wl.H * wl.I * s_el / (t_gu * 1e-3) / 1e9,
+                                 "unit": "GB/s"}}
+    peak, psrc = tensor_peak(peaks, peaks_src, clocks)
+    burst = float(peaks["bf16_tflops"])
+    sus = float(peaks.get("bf16_tflops_sustained", burst))
+    ach = flops / gemm_s / 1e12
+    gu = 4.0 * N * wl.H * wl.I / (t_gu * 1e-3) / 1e12
+    dn = 2.0 * N * wl.H * wl.I / (t_dn * 1e-3) / 1e12
+    return {"bound": "tensor", "kernel": "grouped_gemm_tc (gate/up + SwiGLU, down + weighted un-permute)",
+            "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic,
+            "peak_source": psrc, "frac_of_burst": ach / burst, "frac_of_sustained": ach / sus,
+            "algorithmic_per_launch": f"6*N*H*I / 2 launches = {flops / 2:.4e} FLOP",
+            "gate_up": {"achieved": gu, "frac": gu / peak, "flop": 4.0 * N * wl.H * wl.I},
+            "down": {"achieved": dn, "frac": dn / peak, "flop": 2.0 * N * wl.H * wl.I}}
+
+
+def gemm_traffic(wl):
+    """Mean DRAM bytes per grouped_gemm_tc launch from the committed ncu capture
+    of this workload, or None once the kernel source has changed."""
+    rec = GEMM_TRAFFIC.get(wl.name)
+    if not rec or rec["source_sha256"] != source_sha256("top_routing_grouped_fp32_gb300/csrc/gemm_tc.cu"):
+        return None
+    return rec["bytes_per_launch"]
+
+
+def measure_forward(moe, wl, args, world, dev, min_seconds, K, warmup, keep=False):
+    """Warm-up, then repetitions of exactly K timed forward steps (each between
+    a barrier and device synchronisations, events on the launching stream)
+    until at least `min_seconds` of timed work, so that the clock sampler sees
+    at least ~10 samples inside the window.  Returns per-step figures over all
+    repetitions."""
+    import torch
+    from top_routing_grouped_fp32_gb300.inputs import make_inputs
     inp = make_inputs(wl, device=dev)
     experts = moe.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
     ws = experts.forward_workspace(wl.T, wl.top_k, inp["logits"].dtype)
     y = torch.empty((wl.T, wl.H), dtype=inp["x"].dtype, device=dev)
-    assert inp["x"].dtype == {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[wl.dtype]
     stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if args.l2_flush else None
 
-    def step(events=None):
+    def step(events=None, i=0):
+        if flush is not None:
+            flush.fill_(i & 0xFF)  # 256 MB written: nothing of the last step stays in the 129 MB L2
         experts.forward(inp["x"], inp["logits"], wl.top_k, wl.renormalize, y=y, workspace=ws,
                         stream=stream, events=events)
 
-    for _ in range(max(3, args.warmup)):
-        step()
+    for i in range(max(3, warmup)):
+        step(i=i)
     torch.cuda.synchronize(dev)
     assert moe.moe_get_device_status(ws) == 0
-
-    K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for e in [x for row in ev for x in row]:
         e.record(stream)  # torch creates the CUDA event on its first record
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local)
-    barrier(world, dev)
-    torch.cuda.synchronize(dev)
+
+    stage_sum = {n: 0.0 for n in STAGES}
+    span_sum = 0.0  # route start -> combine end, summed over steps (flush excluded)
+    rep_ms = []
+    clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.3)  # let the sampler start before the timed region
     w0 = time.time()
-    start.record(stream)
-    for i in range(K):
-        step(ev[i])
-    end.record(stream)
-    torch.cuda.synchronize(dev)
+    reps = 1
+    r = 0
+    while r < reps:
+        barrier(world, dev)
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for i in range(K):
+            step(ev[i], i)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        rep_ms.append(max_over_ranks(start.elapsed_time(end), world, dev))
+        for i in range(K):
+            for j, n in enumerate(STAGES):
+                stage_sum[n] += ev[i][j].elapsed_time(ev[i][j + 1])
+            span_sum += ev[i][0].elapsed_time(ev[i][5])
+        if r == 0:  # the same repetition count on every rank
+            reps = max(1, int(math.ceil(min_seconds * 1e3 / max(rep_ms[0], 1e-3))))
+            reps = int(max_over_ranks(float(reps), world, dev))
+        r += 1
     w1 = time.time()
     clock_info = clocks.stop(w0, w1)
-    barrier(world, dev)
-    ms_local = start.elapsed_time(end)
-    ms_total = max_over_ranks(ms_local, world, dev)
     status = moe.moe_get_device_status(ws)
+    steps = K * reps
+    stage = {n: v / steps for n, v in stage_sum.items()}
+    if flush is not None:
+        # the flush is outside the forward: the per-step time is its event span
+        ms_step = max_over_ranks(span_sum / steps, world, dev)
+    else:
+        ms_step = sum(rep_ms) / steps
+    lay = experts.forward_layout(wl.T, wl.top_k, inp["logits"].dtype)
+    off = ws[lay["offsets"]:lay["offsets"] + 4 * (wl.E + 1)].view(torch.int32).cpu()
+    touched = int(((off[1:] - off[:-1]) != 0).sum().item())
+    res = {"value": wl.T * world / (ms_step * 1e-3), "ms_per_step": ms_step, "repeats": reps,
+           "rep_ms_per_step": [m / K for m in rep_ms], "stages_ms": stage, "clocks": clock_info,
+           "touched": touched, "device_status": status,
+           "gpu_launches": launches_per_step(wl.T, wl.E) * steps}
+    if keep:
+        res["_state"] = (inp, experts, ws, y, stream)
+    else:
+        del inp, experts, ws, y, flush
+        torch.cuda.empty_cache()
+    return res
 
-    # per-stage device time inside the timed region (events on the launching stream)
-    names = ["route", "dispatch", "gate_up_gemm", "down_gemm", "combine"]
-    stage = {n: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
-             for j, n in enumerate(names)}
 
-    # end to end through the host-buffer entry points: every step copies its
-    # inputs in from pinned host memory and its result out, inside the timed
-    # region.  `e2e` is the pipelined entry point (moe_host_pipeline_*, the
-    # copies of neighbouring steps overlap the forward between them; two sets
-    # of host buffers alternate); `e2e_serial` is one moe_forward_host call per
-    # step (copy in, forward, copy out on one stream).  Host wall clock between
-    # two device synchronisations.
+def measure_e2e(wl, world, dev, inp, experts, stream, Ke):
+    """End to end through the host-buffer entry points: every step copies its
+    inputs in from pinned host memory and its result out, inside the timed
+    region.  `e2e` is the pipelined entry point (moe_host_pipeline_*, the
+    copies of neighbouring steps overlap the forward between them; two sets of
+    host buffers alternate); `e2e_serial` is one moe_forward_host call per
+    step (copy in, forward, copy out on one stream).  Host wall clock between
+    two device synchronisations."""
+    import torch
     xh = [inp["x"].cpu().pin_memory() for _ in range(2)]
     lh = [inp["logits"].cpu().pin_memory() for _ in range(2)]
     yh = [torch.empty((wl.T, wl.H), dtype=inp["x"].dtype).pin_memory() for _ in range(2)]
-    Ke = max(1, args.e2e_steps if args.e2e_steps is not None else K)
     pipe = experts.host_pipeline(wl.T, wl.top_k, wl.renormalize, logits_dtype=inp["logits"].dtype,
                                  depth=2, stream=stream)
     for i in range(3):
@@ -376,81 +503,76 @@ def run_native(args, rank, world, local):
         experts.forward_host(xh[0], lh[0], wl.top_k, wl.renormalize, yh[0], wsh, stream=stream)
     torch.cuda.synchronize(dev)
     e2e_serial_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev)
-    xh, lh, yh = xh[0], lh[0], yh[0]
-    h2d = xh.numel() * xh.element_size() + lh.numel() * lh.element_size()
-    d2h = yh.numel() * yh.element_size()
+    h2d = xh[0].numel() * xh[0].element_size() + lh[0].numel() * lh[0].element_size()
+    d2h = yh[0].numel() * yh[0].element_size()
+    del wsh
+    return ({"value": wl.T * world * Ke / (e2e_ms * 1e-3), "unit": UNIT,
+             "api": "moe_host_pipeline_submit (depth 2), one call per step",
+             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            {"value": wl.T * world * Ke / (e2e_serial_ms * 1e-3), "unit": UNIT,
+             "api": "moe_forward_host, one call per step"})
 
-    # experts that received rows (read back after the timed region): the
-    # weight bytes a weight-streaming roofline charges
-    lay = experts.forward_layout(wl.T, wl.top_k, inp["logits"].dtype)
-    off = ws[lay["offsets"]:lay["offsets"] + 4 * (wl.E + 1)].view(torch.int32).cpu()
-    touched = int(((off[1:] - off[:-1]) != 0).sum().item())
+
+def run_native(args, rank, world, local):
+    import torch
+    import top_routing_grouped_fp32_gb300 as moe
+    from top_routing_grouped_fp32_gb300.inputs import WORKLOADS, with_dtype
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the native arm has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    moe.load()
+    wl = bench_workload(args)
+    K = args.steps
+    res = measure_forward(moe, wl, args, world, dev, args.min_seconds, K, args.warmup, keep=True)
+    inp, experts, ws, y, stream = res.pop("_state")
+    assert inp["x"].dtype == {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[wl.dtype]
+    Ke = max(1, args.e2e_steps if args.e2e_steps is not None else K * res["repeats"])
+    e2e, e2e_serial = measure_e2e(wl, world, dev, inp, experts, stream, Ke)
+    del inp, experts, ws, y
+    torch.cuda.empty_cache()
+    peaks, peaks_src = load_peaks()
 
     line = None
     if rank == 0:
-        peaks, peaks_src = load_peaks()
-        N = wl.T * wl.top_k
-        gemm_flops = 6.0 * N * wl.H * wl.I
-        gateup_flops = 4.0 * N * wl.H * wl.I
-        gemm_ms = stage["gate_up_gemm"] + stage["down_gemm"]
-        tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
-        gateup_tflops = gateup_flops / (stage["gate_up_gemm"] * 1e-3) / 1e12
-        peak = float(peaks["bf16_tflops"])
-        # the GEMMs are timed inside the step loop (hundreds of steps, under the
-        # power cap: the clock record shows sw_power_cap), so their roofline is
-        # the measured sustained bf16 rate; the burst fraction is kept beside it
-        peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
-        src = "top_routing_grouped_fp32_gb300/csrc/gemm_tc.cu"
-        traffic = (GATEUP_TRAFFIC["bytes"] if GATEUP_TRAFFIC["source_sha256"] == source_sha256(src)
-                   and GATEUP_TRAFFIC["workload"] == wl.name else None)
-        s_el = 4 if wl.dtype == "f32" else 2
-        w_gateup = touched * 2.0 * wl.H * wl.I * s_el
-        w_all = touched * 3.0 * wl.H * wl.I * s_el
-        hbm_peak = float(peaks["hbm_gbs"])
-        weights_hbm = {"touched_experts": touched, "bytes": w_all,
-                       "achieved": w_all / (gemm_ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                       "frac": w_all / (gemm_ms * 1e-3) / 1e9 / hbm_peak}
-        if wl.name.startswith("decode"):
-            # few rows per expert: the projections stream weights, HBM is the bound
-            ach = w_gateup / (stage["gate_up_gemm"] * 1e-3) / 1e9
-            roofline = {"bound": "hbm", "kernel": "grouped_gemm_tc (gate/up + SwiGLU)",
-                        "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
-                        "traffic": None, "peak_source": f"{peaks_src} hbm_gbs",
-                        "algorithmic_per_launch": f"touched*2*H*I*2 = {w_gateup:.4e} B"}
-        else:
-            roofline = {"bound": "tensor", "kernel": "grouped_gemm_tc (gate/up + SwiGLU)",
-                        "achieved": gateup_tflops, "peak": peak_sus, "unit": "TFLOP/s",
-                        "frac": gateup_tflops / peak_sus,
-                        "traffic": traffic,
-                        "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside the step loop)",
-                        "frac_of_burst": gateup_tflops / peak,
-                        "algorithmic_per_launch": f"4*N*H*I = {gateup_flops:.4e} FLOP"}
+        roof = roofline_for(wl, res["stages_ms"], res["touched"], res["clocks"], peaks, peaks_src,
+                            gemm_traffic(wl))
         line = {
-            "metric": METRIC,
-            "value": wl.T * world * K / (ms_total * 1e-3),
-            "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-            "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": wl.dtype,
+            "metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "repeats": res["repeats"],
+            "rep_ms_per_step": res["rep_ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
             "data": "synthetic (seeded randn, BF16 weights ~N(0,1/fan_in)); no dataset, random-init weights",
-            "config": workload_config(wl),
-            "gemm_tflops": tflops,
-            "gemm_frac_of_peak": tflops / peak,
-            "gemm_frac_of_sustained_peak": tflops / peak_sus,
-            "stages_ms": stage,
-            "roofline": roofline,
-            "weights_hbm": weights_hbm,
-            "e2e_serial": {"value": wl.T * world * Ke / (e2e_serial_ms * 1e-3), "unit": UNIT,
-                           "api": "moe_forward_host, one call per step"},
-            "e2e": {"value": wl.T * world * Ke / (e2e_ms * 1e-3), "unit": UNIT,
-                    "api": "moe_host_pipeline_submit (depth 2), one call per step",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step(wl.T, wl.E) * K,
-            "clocks": clock_info,
-            "device_status": status,
+            "config": workload_config(wl, args.l2_flush),
+            "stages_ms": res["stages_ms"],
+            "roofline": roof,
+            "e2e": e2e, "e2e_serial": e2e_serial,
+            "gpu_launches": res["gpu_launches"],
+            "clocks": res["clocks"],
+            "device_status": res["device_status"],
         }
-    # free the GPU before the CPU leg
-    del experts, ws, wsh, inp, y
-    torch.cuda.empty_cache()
+    # the other workloads (and the headline in FP16), a few hundred ms each
+    if args.workload == DEFAULT_WORKLOAD and args.tokens is None and args.dtype is None \
+            and not args.no_workloads:
+        side = {}
+        for name, dt in SIDE_WORKLOADS:
+            swl = with_dtype(WORKLOADS[name], dt or WORKLOADS[name].dtype)
+            key = swl.name
+            r = measure_forward(moe, swl, args, world, dev, args.side_seconds, args.side_steps, 5)
+            if rank == 0:
+                side[key] = {"config": workload_config(swl, args.l2_flush), "value": r["value"], "unit": UNIT,
+                             "ms_per_step": r["ms_per_step"], "steps": args.side_steps,
+                             "repeats": r["repeats"], "stages_ms": r["stages_ms"],
+                             "roofline": roofline_for(swl, r["stages_ms"], r["touched"], r["clocks"],
+                                                      peaks, peaks_src, gemm_traffic(swl)),
+                             "touched_experts": r["touched"], "clocks": r["clocks"],
+                             "device_status": r["device_status"]}
+        if rank == 0:
+            line["workloads"] = side
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = _host_inputs(wl)
         rate, n, dt, threads = oracle_sample_rate(wl, host, args.cpu_seconds)
