@@ -168,9 +168,11 @@ moe_status moe_dispatch(const uint32_t* idx, int64_t T, int64_t E, int32_t top_k
  * T <= 65,280 at E = 1024, T <= ~1M at E = 64) get MOE_ERR_UNSUPPORTED with a
  * message.  The call allocates nothing.
  *
- * The first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream
- * capture.  All calls share the array and it keeps the last call's contents;
+ * The first call in a CUDA context (for runtime-API callers: the first call
+ * on each device) looks up the array's device address with that device
+ * current and caches it under the context's unique id; make that first call
+ * before any stream capture.  A context created later on the same device
+ * (after cudaDeviceReset, or a driver-API context) gets its own lookup.  All calls share the array and it keeps the last call's contents;
  * nothing in it needs clearing because each call writes every entry it reads.
  * Calls whose kernels overlap on the GPU (unordered streams) race on the
  * array and give wrong results.  There is no device status word: an index

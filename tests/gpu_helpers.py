@@ -80,3 +80,15 @@ def oracle_forward_sample(inp: dict, top_k: int, renorm: bool, tokens, dtype: st
     d = stored(inp["down"].index_select(0, sel))
     return oracle.forward_tokens(stored(inp["x"]), stored(logits), g, u, d, dtype, ldt, top_k,
                                  renorm, tokens, experts_held=held)
+
+
+def oracle_dispatch_of(idx: torch.Tensor, E: int, x: torch.Tensor | None = None):
+    """The oracle's own dispatch of a routing result: (offsets [E+1], perm [N],
+    x_disp rows in dispatch order as float64, or None).  Stage tests build the
+    oracle's inputs from this and never from a dispatch output of the GPU."""
+    ix = u32(idx)
+    k = ix.shape[1]
+    off, _, perm, _ = oracle.dispatch(ix, E)
+    n = int(off[-1])
+    xd = None if x is None else values(x)[perm[:n].astype(np.int64) // k]
+    return off, perm, xd

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import DT, assert_y_close, stored, u32, values
+from gpu_helpers import DT, assert_y_close, oracle_dispatch_of, stored, u32, values
 from top_routing_grouped_fp32_gb300.inputs import TORCH_DTYPES, WORKLOADS, make_inputs, small_workload
 
 pytestmark = pytest.mark.gpu
@@ -56,8 +56,10 @@ def test_expert_backward(cuda_lib, T, E, k, H, I, dtype, strategy):
     dout = torch.randn((T * k, H), generator=g, device="cuda").to(TORCH_DTYPES[dtype])
     dinput, dgate, dup, ddown = experts.backward(d.x_disp, d.offsets, dout, strategy=strategy)
     torch.cuda.synchronize()
-    ref = oracle.experts_backward(values(d.x_disp), u32(d.offsets), stored(inp["gate"]), stored(inp["up"]),
-                                  stored(inp["down"]), dtype, values(dout))
+    off, _, xd = oracle_dispatch_of(idx, E, inp["x"])
+    assert np.array_equal(u32(d.offsets), off), "offsets differ"
+    ref = oracle.experts_backward(xd, off, stored(inp["gate"]), stored(inp["up"]), stored(inp["down"]),
+                                  dtype, values(dout[:int(off[-1])]))
     assert_y_close(dinput, ref[0], dtype, "dinput")
     for name, got, r in (("dgate", dgate, ref[1]), ("dup", dup, ref[2]), ("ddown", ddown, ref[3])):
         _close(got, r, _wgrad_tol(dtype, strategy), name)
@@ -119,10 +121,12 @@ def test_combine_and_dispatch_backward(cuda_lib, dtype, wdtype):
     dexpert, dweights = cuda_lib.moe_combine_backward(eo, d.perm, w, dy, k)
     dx = cuda_lib.moe_dispatch_backward(eo, d.perm, T, k)
     torch.cuda.synchronize()
-    r_dex, r_dw = oracle.combine_backward(values(eo), u32(d.perm), values(w), values(dy))
+    _, o_perm, _ = oracle_dispatch_of(idx, E)
+    assert np.array_equal(u32(d.perm), o_perm), "perm differs"
+    r_dex, r_dw = oracle.combine_backward(values(eo), o_perm, values(w), values(dy))
     assert_y_close(dexpert, r_dex, dtype, "dexpert")
     _close(dweights, r_dw, 1e-5, "dweights")
-    assert_y_close(dx, oracle.dispatch_backward(values(eo), u32(d.perm), T, k), dtype, "dx")
+    assert_y_close(dx, oracle.dispatch_backward(values(eo), o_perm, T, k), dtype, "dx")
 
 
 @pytest.mark.parametrize("scoring", ["softmax", "sigmoid"])
@@ -163,7 +167,9 @@ def test_tensor_core_backward_full_size(cuda_lib, name):
     experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
     idx, _ = cuda_lib.moe_route(inp["logits"], wl.top_k, wl.renormalize)
     d = cuda_lib.moe_dispatch(idx, wl.E, x=inp["x"])
-    off = u32(d.offsets).astype(np.int64)
+    o_off, _, xd = oracle_dispatch_of(idx, wl.E, inp["x"])
+    assert np.array_equal(u32(d.offsets), o_off), "offsets differ"
+    off = o_off.astype(np.int64)
     N = int(off[-1])
     g = torch.Generator(device="cuda").manual_seed(17)
     dout = torch.randn((d.x_disp.shape[0], wl.H), generator=g, device="cuda").to(TORCH_DTYPES[wl.dtype])
@@ -173,7 +179,7 @@ def test_tensor_core_backward_full_size(cuda_lib, name):
     e = int(np.argmin(np.where(cnt > 0, cnt, np.iinfo(np.int64).max)))
     r0, r1 = int(off[e]), int(off[e + 1])
     sel = torch.as_tensor([e], device="cuda")
-    ref = oracle.experts_backward(values(d.x_disp[r0:r1]), np.array([0, r1 - r0], np.uint32),
+    ref = oracle.experts_backward(xd[r0:r1], np.array([0, r1 - r0], np.uint32),
                                   stored(inp["gate"].index_select(0, sel)), stored(inp["up"].index_select(0, sel)),
                                   stored(inp["down"].index_select(0, sel)), wl.dtype, values(dout[r0:r1]))
     assert_y_close(dinput[r0:r1], ref[0], wl.dtype, "dinput")

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import assert_y_close, u32, values
+from gpu_helpers import assert_y_close, oracle_dispatch_of, u32, values
 from top_routing_grouped_fp32_gb300.inputs import TORCH_DTYPES
 
 pytestmark = pytest.mark.gpu
@@ -18,7 +18,9 @@ def _case(moe, T, E, k, H, dtype, wdtype, seed):
     eo = torch.randn((T * k, H), generator=g, device="cuda").to(TORCH_DTYPES[dtype])
     y = moe.moe_combine(eo, d.perm, w, k)
     torch.cuda.synchronize()
-    ref = oracle.combine(values(eo), u32(d.perm), values(w))
+    _, o_perm, _ = oracle_dispatch_of(idx, E)
+    assert np.array_equal(u32(d.perm), o_perm), "perm differs"
+    ref = oracle.combine(values(eo), o_perm, values(w))
     return y, ref
 
 
@@ -46,7 +48,9 @@ def test_combine_nan_rows(cuda_lib):
     eo = torch.randn((T * k, H), device="cuda").to(torch.bfloat16)
     y = cuda_lib.moe_combine(eo, d.perm, w, k)
     torch.cuda.synchronize()
-    ref = oracle.combine(values(eo), u32(d.perm), values(w))
+    _, o_perm, _ = oracle_dispatch_of(idx, E)
+    assert np.array_equal(u32(d.perm), o_perm), "perm differs"
+    ref = oracle.combine(values(eo), o_perm, values(w))
     assert_y_close(y, ref, "bf16")
     assert torch.isnan(y[3]).all() and torch.isnan(y[7]).all()
     assert torch.isfinite(y[0]).all()

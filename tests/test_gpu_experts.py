@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import DT, assert_y_close, stored, u32, values
+from gpu_helpers import DT, assert_y_close, oracle_dispatch_of, stored, u32, values
 from top_routing_grouped_fp32_gb300.inputs import make_inputs, small_workload
 
 pytestmark = pytest.mark.gpu
@@ -21,9 +21,10 @@ def _run(moe, T, E, k, H, I, dtype, seed=0, skew=0.0):
     d = moe.moe_dispatch(idx, E, x=inp["x"])
     out = experts.forward_dispatched(d.x_disp, d.offsets)
     torch.cuda.synchronize()
-    off = u32(d.offsets)
-    ref = oracle.experts(values(d.x_disp), off, stored(inp["gate"]), stored(inp["up"]),
-                         stored(inp["down"]), dtype)
+    # the oracle's inputs come from its own dispatch of the routing result
+    off, _, xd = oracle_dispatch_of(idx, E, inp["x"])
+    assert np.array_equal(u32(d.offsets), off), "offsets differ"
+    ref = oracle.experts(xd, off, stored(inp["gate"]), stored(inp["up"]), stored(inp["down"]), dtype)
     n = int(off[-1])
     assert_y_close(out[:n], ref[:n], dtype, "expert_out")
     return experts, d, out

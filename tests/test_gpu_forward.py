@@ -3,7 +3,8 @@
 Small cases: every token against the oracle.  The five workloads at full
 size: routing indices, offsets and perm read back from the workspace and
 compared bit-exactly with the oracle over ALL tokens; y compared on a sample
-of tokens evaluated one by one by the oracle (including poisoned rows)."""
+of tokens evaluated one by one by the oracle, chosen so that every GEMM tile
+holds a checked row (including poisoned rows)."""
 import numpy as np
 import pytest
 import torch
@@ -90,24 +91,66 @@ def test_forward_tiny_fp32_workload(cuda_lib):
     assert_y_close(y, ref, "f32")
 
 
-def _sample_tokens(wl, inp, n=24, seed=0):
+# Rows per m-tile of the grouped GEMMs: 128 for a single-CTA tile, 256 for a
+# CTA pair (two 128-row halves).  Covering every 128-row block of every
+# expert's segment covers every tile and every half of every pair tile.
+TILE_ROWS = 128
+
+
+def _tile_cover_tokens(wl, o_off, o_perm, seed=0):
+    """Tokens such that every 128-row block of every expert's segment (counted
+    from the segment start, as the GEMM tiles are) holds at least one of their
+    rows, plus the token of each segment's last row.  From the oracle's own
+    dispatch of the full routing result."""
     rng = np.random.default_rng(seed)
-    toks = set(rng.choice(wl.T, size=min(n, wl.T), replace=False).tolist()) | {0, wl.T - 1}
-    meta = inp["meta"].get("poison")
-    if meta:
-        toks |= set(meta["rows"][:6]) | {meta["control"]}
-    return np.array(sorted(toks))
+    toks = set()
+    for e in range(wl.E):
+        a, b = int(o_off[e]), int(o_off[e + 1])
+        for m0 in range(a, b, TILE_ROWS):
+            toks.add(int(o_perm[rng.integers(m0, min(b, m0 + TILE_ROWS))]) // wl.top_k)
+        if b > a:
+            toks.add(int(o_perm[b - 1]) // wl.top_k)
+    return toks
+
+
+def _assert_every_tile_hit(wl, o_off, o_perm, toks):
+    row_of_slot = np.empty(wl.T * wl.top_k, np.int64)
+    n = int(o_off[-1])
+    row_of_slot[o_perm[:n].astype(np.int64)] = np.arange(n)
+    t = np.asarray(sorted(toks), np.int64)
+    rows = row_of_slot[(t[:, None] * wl.top_k + np.arange(wl.top_k)).ravel()]
+    hit = set()
+    for r in rows.tolist():
+        e = int(np.searchsorted(o_off, r, side="right")) - 1
+        hit.add((e, (r - int(o_off[e])) // TILE_ROWS))
+    for e in range(wl.E):
+        cnt = int(o_off[e + 1] - o_off[e])
+        for m in range((cnt + TILE_ROWS - 1) // TILE_ROWS):
+            assert (e, m) in hit, f"expert {e} m-block {m} holds no checked row"
+        if cnt:
+            assert row_of_slot[int(o_perm[int(o_off[e + 1]) - 1])] in set(rows.tolist())
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("name", ["mixtral_bf16", "finegrained_bf16", "skewed_bf16", "decode_bf16"])
 def test_forward_full_workloads(cuda_lib, name, dtype):
+    """Full size: routing and dispatch over every token; y on a token sample
+    chosen (from the oracle's dispatch) so that every 128-row block of every
+    expert's segment and every segment's last row is checked, on all H
+    columns (every n-block), plus the first and last tokens and, for the
+    skewed workload, poisoned rows and the control row."""
     wl = with_dtype(WORKLOADS[name], dtype)
     inp = make_inputs(wl, device="cuda")
     experts, ws, y = _forward(cuda_lib, wl, inp)
-    _check_routing_and_dispatch(experts, ws, wl, inp["logits"], inp["x"])
-    toks = _sample_tokens(wl, inp)
+    o_idx, o_off = _check_routing_and_dispatch(experts, ws, wl, inp["logits"], inp["x"])
+    _, _, o_perm, _ = oracle.dispatch(o_idx, wl.E)
+    toks = _tile_cover_tokens(wl, o_off, o_perm) | {0, wl.T - 1}
+    meta = inp["meta"].get("poison")
+    if meta:
+        toks |= set(meta["rows"][:6]) | {meta["control"]}
+    _assert_every_tile_hit(wl, o_off, o_perm, toks)
+    toks = np.array(sorted(toks))
     _, _, ref = oracle_forward_sample(inp, wl.top_k, wl.renormalize, toks, wl.dtype)
     assert_y_close(y[torch.as_tensor(toks, device="cuda")], ref, wl.dtype)
     if wl.poison_frac:

@@ -6,8 +6,10 @@ that fixed its memory plan at start-up must not call cudaMalloc later.  For
 them moe_dispatch_noalloc keeps its scratch in a fixed device array inside the
 library.  This test calls it through the C ABI and checks that it gives the
 same offsets, row_experts, perm and gathered rows as moe_dispatch (which takes
-a workspace), bit for bit as the dispatch tests require, on two calls in a
-row, and that problems too large for the array are refused.
+a workspace), bit for bit as the dispatch tests require, on calls in a row
+of different shapes (one of them at the array's size limit, where the chunk
+scan runs as its own kernel), with slots holding indices >= E, and that
+problems too large for the array are refused.
 
 The file is named so that pytest collects it last."""
 import ctypes
@@ -47,19 +49,59 @@ def _case(moe, T, E, k, H, seed):
     return idx, x
 
 
+def _check_equal(got, ref):
+    assert torch.equal(got[0], ref.offsets)
+    assert torch.equal(got[1], ref.row_experts)
+    assert torch.equal(got[2], ref.perm)
+    # rows past offsets[E] (slots holding an index >= E) are not written
+    nv = int(ref.offsets[-1].item())
+    assert torch.equal(got[3][:nv].view(torch.int16), ref.x_disp[:nv].view(torch.int16))
+
+
 def test_noalloc_dispatch_matches_workspace_dispatch(cuda_lib):
     lib = cuda_lib.load()
-    # two calls in a row, the second smaller than the first, so that the
-    # scratch still holds the first call's larger contents
-    for T, E, k, H, seed in [(16384, 64, 6, 256, 1), (1000, 8, 2, 64, 2)]:
+    # calls in a row with different shapes, so that the scratch still holds an
+    # earlier call's contents.  (16384, 64, 6) and (1000, 8, 2) have small
+    # chunk-histogram tables, which the scatter blocks scan themselves;
+    # (65280, 1024, 2) is at the array's limit (255 chunks x 2049 words) and
+    # takes the separate scan kernel, whose chunk bases fill the array's
+    # second region.
+    for T, E, k, H, seed in [(16384, 64, 6, 256, 1), (65280, 1024, 2, 64, 3), (1000, 8, 2, 64, 2)]:
         idx, x = _case(cuda_lib, T, E, k, H, seed)
         ref = cuda_lib.moe_dispatch(idx, E, x=x)
         got = _noalloc(lib, idx, E, x)
         torch.cuda.synchronize()
-        assert torch.equal(got[0], ref.offsets)
-        assert torch.equal(got[1], ref.row_experts)
-        assert torch.equal(got[2], ref.perm)
-        assert torch.equal(got[3].view(torch.int16), ref.x_disp.view(torch.int16))
+        _check_equal(got, ref)
+
+
+def test_noalloc_dispatch_invalid_indices(cuda_lib):
+    """Indices >= E are not dispatched: offsets[E] counts only the valid
+    slots, and perm and row_experts end in 0xFFFFFFFF (-1 as int32)."""
+    lib = cuda_lib.load()
+    T, E, k, H = 700, 16, 3, 64
+    g = np.random.default_rng(7)
+    idx_h = np.stack([g.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    bad = g.choice(T * k, size=41, replace=False)
+    idx_h.reshape(-1)[bad] = E + g.integers(0, 1000, size=bad.size)
+    idx = torch.from_numpy(idx_h).cuda()
+    x = torch.randn((T, H), generator=torch.Generator(device="cuda").manual_seed(5),
+                    device="cuda").to(torch.bfloat16)
+    for _ in range(2):
+        ref = cuda_lib.moe_dispatch(idx, E, x=x)
+        got = _noalloc(lib, idx, E, x)
+        torch.cuda.synchronize()
+        _check_equal(got, ref)
+    flat = idx_h.reshape(-1)
+    valid = np.flatnonzero(flat < E)
+    nv = valid.size
+    assert nv == T * k - bad.size
+    offsets, rows, perm = (t.cpu().numpy() for t in got[:3])
+    assert offsets[E] == nv
+    # the valid slots as a stable sort by expert (the dispatch order)
+    order = valid[np.argsort(flat[valid], kind="stable")]
+    assert np.array_equal(perm[:nv], order)
+    assert np.array_equal(rows[:nv], flat[order])
+    assert np.all(perm[nv:] == -1) and np.all(rows[nv:] == -1)
 
 
 def test_noalloc_dispatch_rejects_oversized_problems(cuda_lib):

@@ -451,25 +451,63 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 size_t dispatch_noalloc_scratch_limit() { return kNoAllocScratchBytes; }
 
-// Device address of g_noalloc_scratch on the current device.  The host-side
-// name of the array is only a stand-in, so the address is looked up once per
-// device with cudaGetSymbolAddress (with that device current) and cached.
+// Device address of g_noalloc_scratch in the current CUDA context.  The
+// host-side name of the array is only a stand-in, so the address is looked up
+// with cudaGetSymbolAddress (with the device current) the first time a context
+// calls, and cached under that context's unique id (cuCtxGetId): a context
+// created later on the same device -- after cudaDeviceReset, or a driver-API
+// context of its own -- loads the module anew and gets its own lookup, so a
+// stale address is never reused.  For runtime-API callers this is once per
+// device.
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+template <typename F>
+F driver_fn(const char* name, int version) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(f);
+}
+}  // namespace
+
 cudaError_t dispatch_noalloc_scratch(void** out) {
-  constexpr int kMaxDevices = 64;
+  constexpr int kSlots = 64;
   static std::mutex mu;
-  static void* addr[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  static unsigned long long ids[kSlots] = {};
+  static void* addr[kSlots] = {};
+  static int next = 0;
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 4000);
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+  if (!get_current || !get_id) return cudaErrorNotSupported;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  CUcontext ctx = nullptr;
+  void* p = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) {
+    // no context yet on this thread (or the driver not yet initialised): the
+    // lookup itself makes the device's primary context current
+    cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (err != cudaSuccess) return err;
-    addr[dev] = p;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorInvalidDevice;
   }
-  *out = addr[dev];
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS || id == 0) return cudaErrorInvalidDevice;
+  for (int i = 0; i < kSlots; ++i) {
+    if (ids[i] == id) {
+      *out = addr[i];
+      return cudaSuccess;
+    }
+  }
+  if (!p) {
+    cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (err != cudaSuccess) return err;
+  }
+  ids[next] = id;  // contexts beyond kSlots replace the oldest entry
+  addr[next] = p;
+  next = (next + 1) % kSlots;
+  *out = p;
   return cudaSuccess;
 }
 
