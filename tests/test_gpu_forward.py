@@ -164,6 +164,31 @@ def test_forward_full_workloads(cuda_lib, name, dtype):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("T,E,k,H,I,dtype", [
+    (1000, 16, 4, 512, 256, "bf16"),   # CTA-pair tiles
+    (700, 3, 3, 72, 64, "f16"),        # a 72-column row
+    (300, 1024, 8, 264, 64, "bf16"),   # single-CTA tiles, a 264-column row
+    (64, 256, 64, 64, 64, "bf16"),     # top_k at its limit
+])
+def test_forward_combine_is_the_slot_sum(cuda_lib, T, E, k, H, I, dtype):
+    """The fused forward's combine: y is bit for bit the ascending-j FP32 sum
+    of the weighted slot rows the down epilogue left in the workspace,
+    rounded once to the dtype, and a second call gives the same bits."""
+    wl = small_workload(T, E, k, H, I, dtype=dtype, renormalize=True, seed=T + k)
+    inp = make_inputs(wl, device="cuda")
+    experts, ws, y = _forward(cuda_lib, wl, inp)
+    lay = experts.forward_layout(T, k, inp["logits"].dtype)
+    s = y.element_size()
+    slots = ws[lay["slots"]:lay["slots"] + T * k * H * s].view(y.dtype).view(T, k, H)
+    acc = torch.zeros((T, H), dtype=torch.float32, device="cuda")
+    for j in range(k):
+        acc += slots[:, j].float()
+    assert torch.equal(y.view(torch.int16), acc.to(y.dtype).view(torch.int16))
+    y2 = experts.forward(inp["x"], inp["logits"], k, True, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
 def test_forward_timed_partial_events(cuda_lib):
     """moe_forward_timed records only the boundaries it is given and computes the same bits."""
     wl = small_workload(1000, 16, 4, 512, 256, dtype="bf16", renormalize=True, seed=22)
