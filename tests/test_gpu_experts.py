@@ -66,6 +66,33 @@ def test_experts_simt(cuda_lib, T, E, k, H, I, dtype):
     _run(cuda_lib, T, E, k, H, I, dtype, seed=T)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_experts_segment_tails(cuda_lib, dtype):
+    """Chosen segment lengths on CTA-pair tiles (N >= 128 E): the last tile of
+    a segment holds 1, 63, 64, 65, 127, 128 (a half tile: M = 128 over the
+    pair), 129, 255 or 256 rows (a full 256-row tile), plus segments of 1, 64
+    and 128 rows alone and an empty expert."""
+    counts = [257, 319, 320, 321, 383, 384, 385, 511, 512, 1, 64, 128, 0]
+    E, H, I = len(counts), 264, 200
+    N = sum(counts)
+    assert N >= 128 * E
+    wl = small_workload(64, E, 1, H, I, dtype=dtype, seed=41)
+    inp = make_inputs(wl, device="cuda")
+    experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    g = torch.Generator(device="cuda").manual_seed(42)
+    x_disp = torch.randn((N, H), generator=g, device="cuda").to(inp["x"].dtype)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.uint32)
+    offsets = torch.from_numpy(off.view(np.int32)).cuda()
+    out = experts.forward_dispatched(x_disp, offsets)
+    torch.cuda.synchronize()
+    ref = oracle.experts(values(x_disp), off, stored(inp["gate"]), stored(inp["up"]), stored(inp["down"]),
+                         dtype)
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            assert_y_close(out[a:b], ref[a:b], dtype, f"expert {e} ({b - a} rows)")
+
+
 def test_experts_deterministic(cuda_lib):
     experts, d, out = _run(cuda_lib, 500, 8, 2, 256, 384, "bf16", seed=4)
     again = experts.forward_dispatched(d.x_disp, d.offsets)

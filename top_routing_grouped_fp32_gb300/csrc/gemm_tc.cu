@@ -112,6 +112,15 @@ struct Params {
   int mb;              // m-tiles per expert
   int64_t m_total;     // M of the product
   int64_t split;       // output rows per buffer (M, or I for the [dgate; dup] pair)
+  // forward products on CTA pairs: a segment's last m-tile holding at most
+  // 128 rows runs as a half tile, an M = 128 tcgen05.mma.cta_group::2 (64 rows
+  // per CTA, A loaded through mapA64): half the MMA work of a padded 256-row tile
+  int half_tails;
+  // gate/up on CTA pairs: B is staged interleaved, each CTA's 128-row half of
+  // the N = 256 operand being [64 gate rows | the same 64 up rows] (mapB0 /
+  // mapB1 then have 64-row boxes), so that every accumulator lane holds the
+  // gate and up values of the same features in both tile forms
+  int b_inter;
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -441,6 +450,7 @@ struct Tile {
   int64_t m0;  // first row of the (pair) tile
   int kx0;     // first K coordinate (0, or pad[e] for weight gradients)
   int nk;      // k-blocks of this tile
+  bool half;   // M = 128 pair tile (64 rows per CTA): see Params::half_tails
 };
 
 __device__ __forceinline__ Tile decode_tile(uint32_t tile, const Params& p, const uint32_t* s_pref,
@@ -463,6 +473,7 @@ __device__ __forceinline__ Tile decode_tile(uint32_t tile, const Params& p, cons
   t.m0 = (int64_t)s_off[lo] + (int64_t)(rem / width) * tile_m;
   t.kx0 = 0;
   t.nk = p.k_blocks;
+  t.half = p.half_tails && (int64_t)s_off[lo + 1] - t.m0 <= BM;
   return t;
 }
 
@@ -478,6 +489,7 @@ __device__ __forceinline__ Tile decode_wgrad(uint32_t tile, const Params& p, int
   const uint32_t k0 = __ldg(p.pad + t.e), k1 = __ldg(p.pad + t.e + 1);
   t.kx0 = (int)k0;
   t.nk = (int)((k1 - k0) / BK);
+  t.half = false;
   return t;
 }
 
@@ -485,7 +497,8 @@ __device__ __forceinline__ Tile decode_wgrad(uint32_t tile, const Params& p, int
 template <typename T, int PAIR, int KS>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
-                const __grid_constant__ CUtensorMap mapB1, const Params p) {
+                const __grid_constant__ CUtensorMap mapB1, const __grid_constant__ CUtensorMap mapA64,
+                const Params p) {
   using C = Cfg<PAIR, KS>;
   constexpr int STAGES = C::STAGES;
   constexpr bool kCluster = PAIR == 2;
@@ -529,6 +542,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   }
   if (warp == 0 && lane == 0) {
     prefetch_map(&mapA);
+    if (p.half_tails) prefetch_map(&mapA64);
     prefetch_map(&mapB0);
     prefetch_map(&mapB1);
   }
@@ -587,11 +601,16 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       bool ok = true;
       for (uint32_t tile = cluster_id; ok && tile < total_tiles; tile += num_clusters) {
         const Tile t = tile_at(tile);
-        // A's row (K-major) or M column (MN-major) of this CTA's half
-        int a_row = (int)(t.m0 + (int64_t)rank * BM);
+        // A's row (K-major) or M column (MN-major) of this CTA's half: 128
+        // rows, or 64 for a half tile
+        int a_row = (int)(t.m0 + (int64_t)rank * (t.half ? BM / 2 : BM));
         if (p.a_row_pad) a_row += (int)(__ldg(p.pad + t.e) - s_off[t.e]);
         const int b0row = t.nb * p.cols_per_tile;
         const int b1row = b0row + p.b1_row_off;
+        // interleaved gate/up B (pairs): this CTA's 64 gate rows and the same 64 up rows
+        const int birow = b0row + (int)rank * 64;
+        const CUtensorMap* ma = t.half ? &mapA64 : &mapA;
+        const uint32_t stage_tx = t.half ? (C::STAGE_BYTES - KS * A_BYTES / 2) * PAIR : C::STAGE_BYTES * PAIR;
         for (int kb = 0; kb < t.nk; ++kb) {
           if (!mbar_wait<kCluster>(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
             ok = false;
@@ -604,16 +623,19 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           const int kx = second ? p.a_k2 + (kb - p.kb_split) * BK : t.kx0 + kb * BK * KS;
           const int kb_b = second ? (kb - p.kb_split) * BK : t.kx0 + kb * BK;
           const CUtensorMap* mb = second ? &mapB1 : &mapB0;
-          if (leader) mbar_expect_tx(full_bar(stage), C::STAGE_BYTES * PAIR);
+          if (leader) mbar_expect_tx(full_bar(stage), stage_tx);
           if constexpr (KS == 2) {  // K-major A and B only: KS sub-blocks of 64
 #pragma unroll
             for (int sub = 0; sub < KS; ++sub) {
               const int kxs = kx + sub * BK;
               const uint32_t sbs = sa + KS * A_BYTES + sub * C::B_BYTES;
-              tma_load_2d<PAIR>(sa + sub * A_BYTES, &mapA, kxs, a_row, fb);
+              tma_load_2d<PAIR>(sa + sub * A_BYTES, ma, kxs, a_row, fb);
               if constexpr (PAIR == 1) {
                 tma_load_3d<PAIR>(sbs, &mapB0, kxs, b0row, t.e, fb);
                 tma_load_3d<PAIR>(sbs + B_HALF_BYTES, &mapB1, kxs, b1row, t.e, fb);
+              } else if (p.b_inter) {
+                tma_load_3d<PAIR>(sbs, &mapB0, kxs, birow, t.e, fb);
+                tma_load_3d<PAIR>(sbs + B_HALF_BYTES / 2, &mapB1, kxs, birow, t.e, fb);
               } else if (leader) {
                 tma_load_3d<PAIR>(sbs, &mapB0, kxs, b0row, t.e, fb);
               } else {
@@ -624,7 +646,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
             tma_load_2d<PAIR>(sa, &mapA, a_row, kx, fb);
             tma_load_2d<PAIR>(sa + MN_BOX_BYTES, &mapA, a_row + 64, kx, fb);
           } else {
-            tma_load_2d<PAIR>(sa, &mapA, kx, a_row, fb);
+            tma_load_2d<PAIR>(sa, ma, kx, a_row, fb);
           }
           if (KS == 2) {
             // loaded above
@@ -632,6 +654,9 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
             if constexpr (PAIR == 1) {
               tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kx, b0row, t.e, fb);
               tma_load_3d<PAIR>(sa + A_BYTES + B_HALF_BYTES, &mapB1, kx, b1row, t.e, fb);
+            } else if (p.b_inter) {
+              tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kx, birow, t.e, fb);
+              tma_load_3d<PAIR>(sa + A_BYTES + B_HALF_BYTES / 2, &mapB1, kx, birow, t.e, fb);
             } else if (leader) {
               tma_load_3d<PAIR>(sa + A_BYTES, &mapB0, kx, b0row, t.e, fb);
             } else {
@@ -669,6 +694,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     if (lane == 0 && leader) {
       const uint32_t idesc = make_idesc(sizeof(T) == 2 && !std::is_same<T, __half>::value, C::TILE_M) |
                              ((uint32_t)(p.a_mn != 0) << 15) | ((uint32_t)(p.b_form != kBKmajor3d) << 16);
+      // half tile: M = 128 over the pair (the M field is bits 24-28, M >> 4)
+      const uint32_t idesc_half = (idesc & ~(0x1Fu << 24)) | ((uint32_t)(C::TILE_M / 2 >> 4) << 24);
       // per 16-deep MMA step: 32 bytes along a K-major row, 16 rows of an MN-major box
       const uint32_t a_step = p.a_mn ? 16u * 128u : UMMA_K * 2u;
       const uint32_t b_step = p.b_form != kBKmajor3d ? 16u * 128u : UMMA_K * 2u;
@@ -679,7 +706,9 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       uint32_t phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (uint32_t tile = cluster_id; ok && tile < total_tiles; tile += num_clusters) {
-        const int nk = tile_at(tile).nk;  // 0 for an expert without rows (weight gradients)
+        const Tile tt = tile_at(tile);
+        const int nk = tt.nk;  // 0 for an expert without rows (weight gradients)
+        const uint32_t id = tt.half ? idesc_half : idesc;
         if (!mbar_wait<kCluster>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -695,7 +724,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           for (int q = 0; q < KS * (BK / UMMA_K); ++q) {
             const int sub = q / (BK / UMMA_K), kk = q % (BK / UMMA_K);
             const uint32_t ak = sa + sub * A_BYTES + kk * a_step, bk = sb + sub * C::B_BYTES + kk * b_step;
-            umma_f16<PAIR>(d_tmem, a_hi | ((ak & 0x3FFFFu) >> 4), b_hi | ((bk & 0x3FFFFu) >> 4), idesc,
+            umma_f16<PAIR>(d_tmem, a_hi | ((ak & 0x3FFFFu) >> 4), b_hi | ((bk & 0x3FFFFu) >> 4), id,
                            (kb | q) != 0 ? 1u : 0u);
           }
           umma_commit<PAIR>(empty_bar(stage));  // ring stage free (in every CTA) once done
@@ -718,13 +747,19 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // this warp may access TMEM lanes 32*quarter .. +31
-    const int row = quarter * 32 + lane;
     uint32_t* stg = staging + quarter * (STG_BYTES_PER_WARP / 4);
     uint32_t acc = 0, acc_phase = 0;
     T* out = static_cast<T*>(p.out);
     for (uint32_t tile = cluster_id; tile < total_tiles; tile += num_clusters) {
       const Tile t = tile_at(tile);
-      const int64_t grow = t.m0 + (int64_t)rank * BM + row;
+      // full tile: lane l of quarter q is row 32q + l of this CTA's 128, all
+      // N columns.  Half tile (M = 128 over the pair): the CTA's 64 rows sit
+      // in lanes 0-63 with N columns 0-127 and again in lanes 64-127 with N
+      // columns 128-255, each in TMEM columns 0-127; quarter q then holds rows
+      // 32*(q & 1) + l and the N-column half q >> 1.
+      const int row = t.half ? (quarter & 1) * 32 + lane : quarter * 32 + lane;
+      const int nhalf = t.half ? quarter >> 1 : 0;
+      const int64_t grow = t.m0 + (int64_t)rank * (t.half ? BM / 2 : BM) + row;
       const bool row_ok = p.wgrad ? grow < p.m_total : grow < (int64_t)s_off[t.e + 1];
       // the weighted epilogue's slot and routing weight: loaded before the
       // accumulator wait so that their latency overlaps the MMAs
@@ -744,20 +779,28 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       if (p.mode == kGateUpSwiglu) {
         // h = silu(g) * u: stored straight from registers (one 16-byte vector
         // per 8 columns); this epilogue is not store-bound, and measured
-        // faster without the staging round trip
-        const int64_t col0 = (int64_t)t.nb * 128;
+        // faster without the staging round trip.  Interleaved B: accumulator
+        // columns [128 b, 128 b + 64) hold gate features 64 b .. 64 b + 63 of
+        // the tile (64 (b + nhalf) for a half tile) and the next 64 columns
+        // the up values of the same features; otherwise gate columns 0-127,
+        // up columns 128-255.
+        const int fw = p.b_inter ? 64 : 128;       // features per block
+        const int nblk = t.half ? 1 : 128 / fw;
+        const int64_t col0 = (int64_t)t.nb * 128 + (int64_t)nhalf * 64;
         T* dst = out + grow * p.n_out + col0;
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
+        for (int i32 = 0; i32 < nblk * fw; i32 += 32) {
+          const int b = i32 / fw, c = i32 - b * fw;
+          const uint32_t gcol = (uint32_t)(b * 2 * fw + c);
           uint32_t g[32], u[32];
-          tmem_ld32(taddr + c, g);
-          tmem_ld32(taddr + 128 + c, u);
+          tmem_ld32(taddr + gcol, g);
+          tmem_ld32(taddr + gcol + fw, u);
           tmem_wait_ld(g);
           reg_fence(u);
           if (row_ok) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              if (col0 + c + v * 8 + 8 <= p.n_out) {
+              if (col0 + i32 + v * 8 + 8 <= p.n_out) {
                 float f[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -766,7 +809,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
                   // 16-bit output: the fast divide's ~2 ulp are far below its rounding
                   f[i] = __fdividef(gg * uu, 1.f + __expf(-gg));
                 }
-                *reinterpret_cast<uint4*>(dst + c + v * 8) = pack8<T>(f);
+                *reinterpret_cast<uint4*>(dst + i32 + v * 8) = pack8<T>(f);
               }
             }
           }
@@ -883,27 +926,30 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         }
       } else {
         // the next 32 columns are read from TMEM while this chunk is scaled,
-        // packed and stored
-        const int64_t col0 = (int64_t)t.nb * 256;
+        // packed and stored.  A half tile's warp holds 128 of the 256 columns.
+        const int64_t col0 = (int64_t)t.nb * 256 + (int64_t)nhalf * 128;
+        const int nchunk = t.half ? 4 : 8;
         uint32_t* rowp = row_ok ? reinterpret_cast<uint32_t*>(out + wslot * p.n_out + col0) : nullptr;
         uint32_t ob[2][32];
         tmem_ld32(taddr, ob[0]);
         tmem_wait_ld(ob[0]);
 #pragma unroll
         for (int ci = 0; ci < 8; ++ci) {
-          const int c = ci * 32;
-          if (ci + 1 < 8) tmem_ld32(taddr + c + 32, ob[(ci + 1) & 1]);
-          const uint32_t* o = ob[ci & 1];
-          uint32_t w[16];
+          if (ci < nchunk) {
+            const int c = ci * 32;
+            if (ci + 1 < nchunk) tmem_ld32(taddr + c + 32, ob[(ci + 1) & 1]);
+            const uint32_t* o = ob[ci & 1];
+            uint32_t w[16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float f[8];
+            for (int v = 0; v < 4; ++v) {
+              float f[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[v * 8 + i]) * wscale;
-            put4(w + 4 * v, pack8<T>(f));
+              for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[v * 8 + i]) * wscale;
+              put4(w + 4 * v, pack8<T>(f));
+            }
+            staged_store<16>(stg, w, rowp ? rowp + c / 2 : nullptr, valid_words<T>(p.n_out - col0 - c), lane);
+            if (ci + 1 < nchunk) tmem_wait_ld(ob[(ci + 1) & 1]);
           }
-          staged_store<16>(stg, w, rowp ? rowp + c / 2 : nullptr, valid_words<T>(p.n_out - col0 - c), lane);
-          if (ci + 1 < 8) tmem_wait_ld(ob[(ci + 1) & 1]);
         }
       }
       tc_fence_before();
@@ -964,27 +1010,28 @@ CUtensorMapDataType tmap_type(moe_dtype dt) {
   return dt == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
-// rows x cols (cols contiguous), box 128 rows x 64 columns
-bool encode_2d(CUtensorMap* m, const void* base, moe_dtype dt, uint64_t rows, uint64_t cols) {
+// rows x cols (cols contiguous), box `box_rows` (128, or 64) rows x 64 columns
+bool encode_2d(CUtensorMap* m, const void* base, moe_dtype dt, uint64_t rows, uint64_t cols,
+               uint32_t box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BK, 128u};
+  cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
   cuuint32_t estr[2] = {1u, 1u};
   return fn(m, tmap_type(dt), 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// experts x rows x cols (cols contiguous), box 1 x 128 x 64
+// experts x rows x cols (cols contiguous), box 1 x `box_rows` (128, or 64) x 64
 bool encode_3d(CUtensorMap* m, const void* base, moe_dtype dt, uint64_t E, uint64_t rows,
-               uint64_t cols) {
+               uint64_t cols, uint32_t box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {cols, rows, E};
   cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
-  cuuint32_t box[3] = {(cuuint32_t)BK, 128u, 1u};
+  cuuint32_t box[3] = {(cuuint32_t)BK, box_rows, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   return fn(m, tmap_type(dt), 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1028,9 +1075,12 @@ cudaError_t resident_clusters(int num_sms, int* out) {
   return err;
 }
 
+// mA64: A with 64-row boxes, for the half tiles of p.half_tails (else unused)
 template <typename T, int PAIR, int KS = 1>
 cudaError_t launch_t(int64_t N, int E, const CUtensorMap& mA, const CUtensorMap& mB0,
-                     const CUtensorMap& mB1, Params p, int num_sms, cudaStream_t s) {
+                     const CUtensorMap& mB1, Params p, int num_sms, cudaStream_t s,
+                     const CUtensorMap* mA64 = nullptr) {
+  if (!mA64 || PAIR != 2) p.half_tails = 0;
   int clusters = 0;
   cudaError_t err = resident_clusters<T, PAIR, KS>(num_sms, &clusters);
   if (err != cudaSuccess) return err;
@@ -1061,7 +1111,7 @@ cudaError_t launch_t(int64_t N, int E, const CUtensorMap& mA, const CUtensorMap&
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc<T, PAIR, KS>, mA, mB0, mB1, p);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc<T, PAIR, KS>, mA, mB0, mB1, mA64 ? *mA64 : mA, p);
 }
 
 template <typename T>
@@ -1268,6 +1318,8 @@ struct TcWeights {
   CUtensorMap gate;  // CUtensorMap carries its own 64-byte alignment
   CUtensorMap up;
   CUtensorMap down;
+  CUtensorMap gate64;  // 64-row boxes: the interleaved gate/up operand of CTA pairs
+  CUtensorMap up64;
   int64_t E, I, H;
 };
 
@@ -1286,7 +1338,8 @@ TcWeights* tc_weights_create(const void* gate, const void* up, const void* down,
   w->I = I;
   w->H = H;
   if (!tc::encode_3d(&w->gate, gate, dt, E, I, H) || !tc::encode_3d(&w->up, up, dt, E, I, H) ||
-      !tc::encode_3d(&w->down, down, dt, E, H, I)) {
+      !tc::encode_3d(&w->down, down, dt, E, H, I) || !tc::encode_3d(&w->gate64, gate, dt, E, I, H, 64) ||
+      !tc::encode_3d(&w->up64, up, dt, E, I, H, 64)) {
     *err = "cuTensorMapEncodeTiled rejected an expert weight tensor";
     delete w;
     return nullptr;
@@ -1302,8 +1355,10 @@ cudaError_t launch_bounded_wait_selftest(uint32_t* status, uint64_t limit_ns, cu
 }
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, cudaStream_t s) {
-  CUtensorMap mA;
-  if (!tc::encode_2d(&mA, a.A, a.dt, (uint64_t)a.N, (uint64_t)a.K)) return cudaErrorInvalidValue;
+  CUtensorMap mA, mA64;
+  if (!tc::encode_2d(&mA, a.A, a.dt, (uint64_t)a.N, (uint64_t)a.K) ||
+      !tc::encode_2d(&mA64, a.A, a.dt, (uint64_t)a.N, (uint64_t)a.K, 64))
+    return cudaErrorInvalidValue;
   tc::Params p{};
   p.offsets = a.offsets;
   p.E = a.E;
@@ -1315,13 +1370,20 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, c
   p.wdt = (int)a.wdt;
   p.status = a.status;
   p.k_blocks = (int)((a.K + tc::BK - 1) / tc::BK);
+  p.half_tails = 1;
+  // CTA pairs halve the B bytes each SM stages per k-block; they pay off when
+  // experts hold at least a full 128-row tile on average.  With fewer rows per
+  // expert (decode-sized batches) the GEMM streams weights from HBM and single
+  // CTAs keep twice as many independent streams in flight.
+  const bool pair = a.N >= (int64_t)tc::BM * a.E;
   const CUtensorMap* b0;
   const CUtensorMap* b1;
   if (a.mode == kGateUpSwiglu) {
     p.cols_per_tile = 128;
     p.b1_row_off = 0;
-    b0 = &w->gate;
-    b1 = &w->up;
+    p.b_inter = pair;
+    b0 = pair ? &w->gate64 : &w->gate;
+    b1 = pair ? &w->up64 : &w->up;
   } else {
     p.cols_per_tile = 256;
     p.b1_row_off = 128;
@@ -1329,22 +1391,17 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, c
     b1 = &w->down;
   }
   p.nb = (int)((a.n_out + p.cols_per_tile - 1) / p.cols_per_tile);
-  // CTA pairs halve the B bytes each SM stages per k-block; they pay off when
-  // experts hold at least a full 128-row tile on average.  With fewer rows per
-  // expert (decode-sized batches) the GEMM streams weights from HBM and single
-  // CTAs keep twice as many independent streams in flight.
-  const bool pair = a.N >= (int64_t)tc::BM * a.E;
   if (pair && a.mode != kGateUpSwiglu) {
     // down projection: six 64-deep stages rather than three 128-deep ones (the
     // same ring bytes); measured equal at K = 1408 and 5 % faster at K = 14336
-    if (a.dt == MOE_BF16) return tc::launch_t<__nv_bfloat16, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
-    return tc::launch_t<__half, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
+    if (a.dt == MOE_BF16) return tc::launch_t<__nv_bfloat16, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s, &mA64);
+    return tc::launch_t<__half, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s, &mA64);
   }
   if (pair) {  // gate/up: 128-deep k-blocks, two 64-deep sub-blocks per ring stage
     p.k_blocks = (int)((a.K + 2 * tc::BK - 1) / (2 * tc::BK));
     if (a.dt == MOE_BF16)
-      return tc::launch_t<__nv_bfloat16, 2, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
-    return tc::launch_t<__half, 2, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
+      return tc::launch_t<__nv_bfloat16, 2, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s, &mA64);
+    return tc::launch_t<__half, 2, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s, &mA64);
   }
   if (a.dt == MOE_BF16) return tc::launch_t<__nv_bfloat16, 1>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
   return tc::launch_t<__half, 1>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
