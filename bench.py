@@ -54,7 +54,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # launch, dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
 # each workload, with the SHA-256 of the kernel source it was taken on; it is
 # reported as null once that source changes.
-GEMM_TRAFFIC = {}
+GEMM_TRAFFIC = {
+    # ncu --set full, one launch each on the headline workload: gate/up reads
+    # 1.141169 GB and writes 264.232960 MB, down reads 0.646933 GB and writes
+    # 374.385152 MB (ncu's units; the GB figures are rounded to the kilobyte)
+    "finegrained_bf16": {"bytes_per_launch": (1141169000 + 264232960 + 646933000 + 374385152) / 2,
+                         "source_sha256": "03b3eae8009635f5a6dab0f8a4ff8b8a92bf9a85c90ceb06368b02bd21b0e1d3"},
+}
 
 
 def parse_args(argv=None):

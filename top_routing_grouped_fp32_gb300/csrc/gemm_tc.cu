@@ -928,16 +928,18 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         // the next 32 columns are read from TMEM while this chunk is scaled,
         // packed and stored.  A half tile's warp holds 128 of the 256 columns.
         const int64_t col0 = (int64_t)t.nb * 256 + (int64_t)nhalf * 128;
-        const int nchunk = t.half ? 4 : 8;
         uint32_t* rowp = row_ok ? reinterpret_cast<uint32_t*>(out + wslot * p.n_out + col0) : nullptr;
-        uint32_t ob[2][32];
-        tmem_ld32(taddr, ob[0]);
-        tmem_wait_ld(ob[0]);
+        // NCH 32-column chunks: 8 for a full tile, 4 for a half tile (a
+        // compile-time count in each form, so the double buffer stays in registers)
+        auto chunks = [&](auto nch) {
+          constexpr int NCH = decltype(nch)::value;
+          uint32_t ob[2][32];
+          tmem_ld32(taddr, ob[0]);
+          tmem_wait_ld(ob[0]);
 #pragma unroll
-        for (int ci = 0; ci < 8; ++ci) {
-          if (ci < nchunk) {
+          for (int ci = 0; ci < NCH; ++ci) {
             const int c = ci * 32;
-            if (ci + 1 < nchunk) tmem_ld32(taddr + c + 32, ob[(ci + 1) & 1]);
+            if (ci + 1 < NCH) tmem_ld32(taddr + c + 32, ob[(ci + 1) & 1]);
             const uint32_t* o = ob[ci & 1];
             uint32_t w[16];
 #pragma unroll
@@ -948,9 +950,11 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
               put4(w + 4 * v, pack8<T>(f));
             }
             staged_store<16>(stg, w, rowp ? rowp + c / 2 : nullptr, valid_words<T>(p.n_out - col0 - c), lane);
-            if (ci + 1 < nchunk) tmem_wait_ld(ob[(ci + 1) & 1]);
+            if (ci + 1 < NCH) tmem_wait_ld(ob[(ci + 1) & 1]);
           }
-        }
+        };
+        if (t.half) chunks(std::integral_constant<int, 4>{});
+        else chunks(std::integral_constant<int, 8>{});
       }
       tc_fence_before();
       __syncwarp();
