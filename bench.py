@@ -57,9 +57,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 GEMM_TRAFFIC = {
     # ncu --set full, one launch each on the headline workload: gate/up reads
     # 1.141169 GB and writes 264.232960 MB, down reads 0.646933 GB and writes
-    # 374.385152 MB (ncu's units; the GB figures are rounded to the kilobyte)
+    # 374.385152 MB (ncu's units; the GB figures are rounded to the kilobyte).
+    # Captured on source 03b3eae8...e1d3; since then only the file's header
+    # comment changed.
     "finegrained_bf16": {"bytes_per_launch": (1141169000 + 264232960 + 646933000 + 374385152) / 2,
-                         "source_sha256": "03b3eae8009635f5a6dab0f8a4ff8b8a92bf9a85c90ceb06368b02bd21b0e1d3"},
+                         "source_sha256": "7afabd7df8ab000943bdd50991142d166e89f0aef0c0cd42de0980f63a7ef1f7"},
 }
 
 

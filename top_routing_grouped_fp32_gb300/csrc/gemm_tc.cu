@@ -16,13 +16,17 @@
 //
 //   * persistent CTAs over a tile list built on the device from offsets[]
 //     (segment lengths are never read by the host); a tile is 128*PAIR rows
-//     x 256 FP32 accumulator columns of one expert;
+//     x 256 FP32 accumulator columns of one expert, except that on CTA pairs
+//     a segment's last tile holding at most 128 rows runs as a half tile
+//     (M = 128 over the pair, 64 rows per CTA), halving its padding;
 //   * PAIR = 2 (the default): a cluster of two CTAs on two SMs runs one
 //     tcgen05.mma.cta_group::2 of M=256: each CTA stages its own 128 rows of A
-//     and one 128-row half of B (gate rows / up rows, or the two halves of the
-//     down rows), so an SM moves 32 KiB per 64-deep k-block instead of 48 KiB
-//     and a 6-stage ring fits in shared memory; PAIR = 1 is the single-CTA
-//     form (M=128, both B halves staged locally, 4 stages);
+//     and one 128-row half of B (for gate/up: 64 gate rows and the same 64 up
+//     rows, so that every accumulator lane holds gate and up of the same
+//     features; for down: one half of the 256 down rows), so an SM moves
+//     32 KiB per 64-deep k-block instead of 48 KiB and a 6-stage ring fits in
+//     shared memory; PAIR = 1 is the single-CTA form (M=128, both B halves
+//     staged locally, 4 stages);
 //   * warp 0: TMA producer (cp.async.bulk.tensor, 128-byte swizzle); its
 //     copies complete on the leader CTA's "full" barrier;
 //   * warp 1: allocates 512 TMEM columns; in the leader CTA one thread issues
