@@ -50,10 +50,12 @@ def test_fp32_roofline_is_the_ffma_pipe():
 
 def test_traffic_is_dropped_when_the_kernel_source_changes(monkeypatch):
     wl = WORKLOADS["finegrained_bf16"]
-    rec = bench.GEMM_TRAFFIC[wl.name]
-    assert bench.gemm_traffic(wl) == rec["bytes_per_launch"]  # the committed capture matches the source
-    monkeypatch.setitem(bench.GEMM_TRAFFIC, wl.name, dict(rec, source_sha256="0" * 64))
+    sha = bench.source_sha256("top_routing_grouped_fp32_gb300/csrc/gemm_tc.cu")
+    monkeypatch.setitem(bench.GEMM_TRAFFIC, wl.name, {"bytes_per_launch": 123.0, "source_sha256": sha})
+    assert bench.gemm_traffic(wl) == 123.0
+    monkeypatch.setitem(bench.GEMM_TRAFFIC, wl.name, {"bytes_per_launch": 123.0, "source_sha256": "0" * 64})
     assert bench.gemm_traffic(wl) is None
+    assert bench.gemm_traffic(WORKLOADS["mixtral_bf16"]) is None  # no capture of that workload
 
 
 def test_launch_count_per_step():

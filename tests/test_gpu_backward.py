@@ -65,6 +65,37 @@ def test_expert_backward(cuda_lib, T, E, k, H, I, dtype, strategy):
         _close(got, r, _wgrad_tol(dtype, strategy), name)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_expert_backward_segment_tails(cuda_lib, dtype):
+    """Tensor-core strategy on CTA-pair tiles with chosen segment lengths: the
+    last tile of a segment holds 1, 63, 64, 65, 127, 128 (half tiles, M = 128
+    over the pair), 129, 255 or 256 rows, plus segments of 1, 64 and 128 rows
+    alone and an empty expert."""
+    counts = [257, 319, 320, 321, 383, 384, 385, 511, 512, 1, 64, 128, 0]
+    E, H, I = len(counts), 264, 200
+    N = sum(counts)
+    assert N >= 128 * E
+    wl = small_workload(64, E, 1, H, I, dtype=dtype, seed=43)
+    inp = make_inputs(wl, device="cuda")
+    experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    g = torch.Generator(device="cuda").manual_seed(44)
+    x_disp = torch.randn((N, H), generator=g, device="cuda").to(TORCH_DTYPES[dtype])
+    dout = torch.randn((N, H), generator=g, device="cuda").to(TORCH_DTYPES[dtype])
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.uint32)
+    offsets = torch.from_numpy(off.view(np.int32)).cuda()
+    dinput, dgate, dup, ddown = experts.backward(x_disp, offsets, dout, strategy="tensor_core")
+    torch.cuda.synchronize()
+    ref = oracle.experts_backward(values(x_disp), off, stored(inp["gate"]), stored(inp["up"]),
+                                  stored(inp["down"]), dtype, values(dout))
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            assert_y_close(dinput[a:b], ref[0][a:b], dtype, f"dinput, expert {e} ({b - a} rows)")
+    for name, got, r in (("dgate", dgate, ref[1]), ("dup", dup, ref[2]), ("ddown", ddown, ref[3])):
+        _close(got, r, 2e-2, name)
+    assert torch.all(dgate[E - 1] == 0) and torch.all(ddown[E - 1] == 0)
+
+
 @pytest.mark.parametrize("strategy", ["scalar", "tensor_core"])
 def test_expert_backward_empty_experts_get_zero(cuda_lib, strategy):
     wl = small_workload(100, 8, 1, 64, 64, dtype="bf16", seed=3, skew=6.0)

@@ -60,6 +60,17 @@
 #include "internal.h"
 
 namespace moe {
+
+// Prebuilt TMA descriptors of one expert-weight set (gate, up [E,I,H]; down [E,H,I]).
+struct TcWeights {
+  CUtensorMap gate;  // CUtensorMap carries its own 64-byte alignment
+  CUtensorMap up;
+  CUtensorMap down;
+  CUtensorMap gate64;  // 64-row boxes: the interleaved gate/up operand of CTA pairs
+  CUtensorMap up64;
+  int64_t E, I, H;
+};
+
 namespace tc {
 
 constexpr int BM = 128;        // rows per CTA
@@ -824,8 +835,11 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         // dg = da * u * silu'(g), du = da * silu(g) and the activation
         // a = silu(g) * u, stored in the 16-bit dtype in the 64-padded row
         // space (row - offsets[e] + pad[e]); the padding rows after an
-        // expert's last row are written as zeros
-        const int64_t col0 = (int64_t)t.nb * 128;
+        // expert's last row are written as zeros (a segment's padding ends
+        // inside its last tile, half tiles included).  The gate and up
+        // accumulator columns are laid out as in the forward gate/up product.
+        const int fw = p.b_inter ? 64 : 128;
+        const int64_t col0 = (int64_t)t.nb * 128 + (int64_t)nhalf * 64;  // this warp's first feature
         const int64_t I = p.n_out;
         const int64_t local = grow - (int64_t)s_off[t.e];
         const uint32_t pe = __ldg(p.pad + t.e);
@@ -851,15 +865,20 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
             d[v * 8 + 4] = d1.x; d[v * 8 + 5] = d1.y; d[v * 8 + 6] = d1.z; d[v * 8 + 7] = d1.w;
           }
         };
+        // NF features of this warp: 128 (full tile) or 64 (half tile)
+        auto features = [&](auto nf) {
+        constexpr int NF = decltype(nf)::value;
         float dcur[32];
         load_da(0, dcur);
 #pragma unroll
-        for (int c = 0; c < 128; c += 32) {
+        for (int c = 0; c < NF; c += 32) {
           float dnext[32];
-          if (c + 32 < 128) load_da(c + 32, dnext);
+          if (c + 32 < NF) load_da(c + 32, dnext);
+          const int b = c / fw;
+          const uint32_t gcol = (uint32_t)(b * 2 * fw + (c - b * fw));
           uint32_t g[32], u[32], wdg[16], wdu[16], wa[16];
-          tmem_ld32(taddr + c, g);
-          tmem_ld32(taddr + 128 + c, u);
+          tmem_ld32(taddr + gcol, g);
+          tmem_ld32(taddr + gcol + fw, u);
           tmem_wait_ld(g);
           reg_fence(u);
 #pragma unroll
@@ -885,16 +904,19 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           staged_store<16>(stg, wdg, dgp ? dgp + c / 2 : nullptr, vw, lane);
           staged_store<16>(stg, wdu, dup_p ? dup_p + c / 2 : nullptr, vw, lane);
           staged_store<16>(stg, wa, ap ? ap + c / 2 : nullptr, vw, lane);
-          if (c + 32 < 128) {
+          if (c + 32 < NF) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) dcur[i] = dnext[i];
           }
         }
+        };
+        if (t.half) features(std::integral_constant<int, 64>{});
+        else features(std::integral_constant<int, 128>{});
       } else if (p.mode == kPlainF32 || p.mode == kWgrad) {
         // FP32 accumulator rows: da in dispatch order, or a weight-gradient
         // tile (rows at or past `split` go to out2; an expert without rows
-        // gets zeros)
-        const int64_t col0 = (int64_t)t.nb * 256;
+        // gets zeros).  A half tile's warp holds 128 of the 256 columns.
+        const int64_t col0 = (int64_t)t.nb * 256 + (int64_t)nhalf * 128;
         float* rowf = nullptr;
         if (row_ok) {
           if (p.mode == kPlainF32)
@@ -916,17 +938,22 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
             staged_store<32>(stg, z, rowp ? rowp + c : nullptr, valid_words<float>(p.n_out - col0 - c), lane);
         } else {
           // the next 32 columns are read from TMEM while this chunk is stored
-          uint32_t ob[2][32];
-          tmem_ld32(taddr, ob[0]);
-          tmem_wait_ld(ob[0]);
+          auto chunks = [&](auto nch) {
+            constexpr int NCH = decltype(nch)::value;
+            uint32_t ob[2][32];
+            tmem_ld32(taddr, ob[0]);
+            tmem_wait_ld(ob[0]);
 #pragma unroll
-          for (int ci = 0; ci < 8; ++ci) {
-            const int c = ci * 32;
-            if (ci + 1 < 8) tmem_ld32(taddr + c + 32, ob[(ci + 1) & 1]);
-            staged_store<32>(stg, ob[ci & 1], rowp ? rowp + c : nullptr,
-                             valid_words<float>(p.n_out - col0 - c), lane);
-            if (ci + 1 < 8) tmem_wait_ld(ob[(ci + 1) & 1]);
-          }
+            for (int ci = 0; ci < NCH; ++ci) {
+              const int c = ci * 32;
+              if (ci + 1 < NCH) tmem_ld32(taddr + c + 32, ob[(ci + 1) & 1]);
+              staged_store<32>(stg, ob[ci & 1], rowp ? rowp + c : nullptr,
+                               valid_words<float>(p.n_out - col0 - c), lane);
+              if (ci + 1 < NCH) tmem_wait_ld(ob[(ci + 1) & 1]);
+            }
+          };
+          if (t.half) chunks(std::integral_constant<int, 4>{});
+          else chunks(std::integral_constant<int, 8>{});
         }
       } else {
         // the next 32 columns are read from TMEM while this chunk is scaled,
@@ -1124,8 +1151,9 @@ cudaError_t launch_t(int64_t N, int E, const CUtensorMap& mA, const CUtensorMap&
 
 template <typename T>
 cudaError_t launch_any(bool pair, int64_t N, int E, const CUtensorMap& mA, const CUtensorMap& mB0,
-                       const CUtensorMap& mB1, const Params& p, int num_sms, cudaStream_t s) {
-  return pair ? launch_t<T, 2>(N, E, mA, mB0, mB1, p, num_sms, s)
+                       const CUtensorMap& mB1, const Params& p, int num_sms, cudaStream_t s,
+                       const CUtensorMap* mA64 = nullptr) {
+  return pair ? launch_t<T, 2>(N, E, mA, mB0, mB1, p, num_sms, s, mA64)
               : launch_t<T, 1>(N, E, mA, mB0, mB1, p, num_sms, s);
 }
 
@@ -1208,6 +1236,10 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
 #define MOE_TC_TRY(x) \
   if ((err = (x)) != cudaSuccess) return err
   CUtensorMap mX, mDo, mDgduP, mWdMN, mWgMN, mWuMN, mDgduMN, mXMN, mDoMN, mActMN;
+  CUtensorMap mX64, mDo64, mDgduP64;  // 64-row A boxes: half tiles of products 1-3
+  if (!encode_2d(&mX64, a.x_disp, dt, N, H, 64) || !encode_2d(&mDo64, a.dout, dt, N, H, 64) ||
+      !encode_2d(&mDgduP64, dgduP, dt, L.npad, 2 * I, 64))
+    return cudaErrorInvalidValue;
   if (!encode_2d(&mX, a.x_disp, dt, N, H) || !encode_2d(&mDo, a.dout, dt, N, H) ||
       !encode_2d(&mDgduP, dgduP, dt, L.npad, 2 * I) || !encode_3d_mn(&mWdMN, a.down, dt, E, H, I) ||
       !encode_3d_mn(&mWgMN, a.gate, dt, E, I, H) || !encode_3d_mn(&mWuMN, a.up, dt, E, I, H) ||
@@ -1264,7 +1296,8 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   p.n_out = I;
   p.nb = (int)((I + 255) / 256);
   p.out = da;
-  MOE_TC_TRY(launch_any<T>(pair, N, E, mDo, mWdMN, mWdMN, p, num_sms, s));
+  p.half_tails = 1;
+  MOE_TC_TRY(launch_any<T>(pair, N, E, mDo, mWdMN, mWdMN, p, num_sms, s, &mDo64));
   // 2. g, u recomputed; epilogue: dg, du, a (padded rows)
   p = base;
   p.mode = kSwigluBwd;
@@ -1276,7 +1309,10 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   p.out = dgduP;
   p.out2 = actP;
   p.da = da;
-  MOE_TC_TRY(launch_any<T>(pair, N, E, mX, w->gate, w->up, p, num_sms, s));
+  p.half_tails = 1;
+  p.b_inter = pair;  // gate/up staged as in the forward's CTA-pair product
+  MOE_TC_TRY(launch_any<T>(pair, N, E, mX, pair ? w->gate64 : w->gate, pair ? w->up64 : w->up, p, num_sms, s,
+                           &mX64));
   // 3. dinput
   const int kbI = (int)((I + BK - 1) / BK);
   p = base;
@@ -1290,7 +1326,8 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   p.n_out = H;
   p.nb = (int)((H + 255) / 256);
   p.out = a.dinput;
-  MOE_TC_TRY(launch_any<T>(pair, N, E, mDgduP, mWgMN, mWuMN, p, num_sms, s));
+  p.half_tails = 1;
+  MOE_TC_TRY(launch_any<T>(pair, N, E, mDgduP, mWgMN, mWuMN, p, num_sms, s, &mDgduP64));
   // 4-5. weight gradients over the padded rows (after the side stream's copies)
   if (join) MOE_TC_TRY(cudaStreamWaitEvent(s, join, 0));
   constexpr int TM = Cfg<2>::TILE_M;
@@ -1321,15 +1358,6 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
 }
 
 }  // namespace tc
-
-struct TcWeights {
-  CUtensorMap gate;  // CUtensorMap carries its own 64-byte alignment
-  CUtensorMap up;
-  CUtensorMap down;
-  CUtensorMap gate64;  // 64-row boxes: the interleaved gate/up operand of CTA pairs
-  CUtensorMap up64;
-  int64_t E, I, H;
-};
 
 bool tc_supported(moe_dtype dt, int64_t I, int64_t H) {
   return (dt == MOE_BF16 || dt == MOE_F16) && I % 8 == 0 && H % 8 == 0;
@@ -1399,13 +1427,14 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, c
     b1 = &w->down;
   }
   p.nb = (int)((a.n_out + p.cols_per_tile - 1) / p.cols_per_tile);
-  if (pair && a.mode != kGateUpSwiglu) {
-    // down projection: six 64-deep stages rather than three 128-deep ones (the
-    // same ring bytes); measured equal at K = 1408 and 5 % faster at K = 14336
+  if (pair && a.mode != kGateUpSwiglu && a.K > 4096) {
+    // long-K down projection: six 64-deep stages rather than three 128-deep
+    // ones (the same ring bytes); 0.5-5 % faster at K = 14336, 3 % slower at
+    // K = 1408 (same-box A/B)
     if (a.dt == MOE_BF16) return tc::launch_t<__nv_bfloat16, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s, &mA64);
     return tc::launch_t<__half, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s, &mA64);
   }
-  if (pair) {  // gate/up: 128-deep k-blocks, two 64-deep sub-blocks per ring stage
+  if (pair) {  // 128-deep k-blocks, two 64-deep sub-blocks per ring stage
     p.k_blocks = (int)((a.K + 2 * tc::BK - 1) / (2 * tc::BK));
     if (a.dt == MOE_BF16)
       return tc::launch_t<__nv_bfloat16, 2, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s, &mA64);
