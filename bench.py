@@ -56,12 +56,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # reported as null once that source changes.
 GEMM_TRAFFIC = {
     # ncu --set full, one launch each on the headline workload: gate/up reads
-    # 1.141169 GB and writes 264.232960 MB, down reads 0.646933 GB and writes
-    # 374.385152 MB (ncu's units; the GB figures are rounded to the kilobyte).
-    # Captured on source 03b3eae8...e1d3; since then only the file's header
-    # comment changed.
-    "finegrained_bf16": {"bytes_per_launch": (1141169000 + 264232960 + 646933000 + 374385152) / 2,
-                         "source_sha256": "7afabd7df8ab000943bdd50991142d166e89f0aef0c0cd42de0980f63a7ef1f7"},
+    # 1.141320 GB and writes 264.859392 MB, down reads 0.646916 GB and writes
+    # 374.054912 MB (ncu's units; the GB figures are rounded to the kilobyte)
+    "finegrained_bf16": {"bytes_per_launch": (1141320000 + 264859392 + 646916000 + 374054912) / 2,
+                         "source_sha256": "d055feb2d31d781df2e42722c95d9a50b3ff5b52eadc442cf7e2764d6ba4dfee"},
 }
 
 
