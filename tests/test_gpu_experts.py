@@ -93,6 +93,26 @@ def test_experts_segment_tails(cuda_lib, dtype):
             assert_y_close(out[a:b], ref[a:b], dtype, f"expert {e} ({b - a} rows)")
 
 
+def test_experts_output_alignment_fallback(cuda_lib):
+    """moe_experts_forward into an output that is 16- but not 32-byte aligned:
+    the epilogues then store 16-byte vectors instead of 32-byte sectors, with
+    the same bits as an aligned output."""
+    wl = small_workload(1000, 4, 2, 256, 384, dtype="bf16", seed=77)
+    inp = make_inputs(wl, device="cuda")
+    experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    idx, _ = cuda_lib.moe_route(inp["logits"], 2, True)
+    d = cuda_lib.moe_dispatch(idx, wl.E, x=inp["x"])
+    N = d.x_disp.shape[0]
+    aligned = experts.forward_dispatched(d.x_disp, d.offsets)
+    buf = torch.empty(N * wl.H + 8, dtype=torch.bfloat16, device="cuda")
+    off = buf[8:].view(N, wl.H)  # 16 bytes past a 512-byte-aligned allocation
+    assert off.data_ptr() % 32 == 16
+    experts.forward_dispatched(d.x_disp, d.offsets, out=off)
+    torch.cuda.synchronize()
+    n = int(d.offsets[-1].item())
+    assert torch.equal(off[:n].view(torch.int16), aligned[:n].view(torch.int16))
+
+
 def test_experts_deterministic(cuda_lib):
     experts, d, out = _run(cuda_lib, 500, 8, 2, 256, 384, "bf16", seed=4)
     again = experts.forward_dispatched(d.x_disp, d.offsets)

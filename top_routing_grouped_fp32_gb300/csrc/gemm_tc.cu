@@ -136,6 +136,7 @@ struct Params {
   // mapB1 then have 64-row boxes), so that every accumulator lane holds the
   // gate and up values of the same features in both tile forms
   int b_inter;
+  int v8_out;  // out rows are 32-byte aligned segments (n_out % 16 == 0, 32-byte base)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -379,6 +380,13 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
         "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
       :
       : "memory");
+}
+
+// 32 bytes (8 words) to a 32-byte-aligned global address: a whole sector per lane
+__device__ __forceinline__ void st_v8(uint32_t* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
 }
 
 // ---------------------------------------------------------------- epilogue stores
@@ -813,19 +821,29 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           tmem_wait_ld(g);
           reg_fence(u);
           if (row_ok) {
+            uint32_t hw[16];
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              if (col0 + i32 + v * 8 + 8 <= p.n_out) {
-                float f[8];
+              float f[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const float gg = __uint_as_float(g[v * 8 + i]);
-                  const float uu = __uint_as_float(u[v * 8 + i]);
-                  // 16-bit output: the fast divide's ~2 ulp are far below its rounding
-                  f[i] = __fdividef(gg * uu, 1.f + __expf(-gg));
-                }
-                *reinterpret_cast<uint4*>(dst + i32 + v * 8) = pack8<T>(f);
+              for (int i = 0; i < 8; ++i) {
+                const float gg = __uint_as_float(g[v * 8 + i]);
+                const float uu = __uint_as_float(u[v * 8 + i]);
+                // 16-bit output: the fast divide's ~2 ulp are far below its rounding
+                f[i] = __fdividef(gg * uu, 1.f + __expf(-gg));
               }
+              put4(hw + 4 * v, pack8<T>(f));
+            }
+            if (p.v8_out && col0 + i32 + 32 <= p.n_out) {
+              uint32_t* d32 = reinterpret_cast<uint32_t*>(dst + i32);
+              st_v8(d32, hw);
+              st_v8(d32 + 8, hw + 8);
+            } else {
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                if (col0 + i32 + v * 8 + 8 <= p.n_out)
+                  *reinterpret_cast<uint4*>(dst + i32 + v * 8) =
+                      make_uint4(hw[4 * v], hw[4 * v + 1], hw[4 * v + 2], hw[4 * v + 3]);
             }
           }
         }
@@ -980,7 +998,14 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
               for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[v * 8 + i]) * wscale;
               put4(w + 4 * v, pack8<T>(f));
             }
-            staged_store<16>(stg, w, rowp ? rowp + c / 2 : nullptr, valid_words<T>(p.n_out - col0 - c), lane);
+            if (p.v8_out && col0 + c + 32 <= p.n_out) {  // warp-uniform: whole 64-byte row segments
+              if (rowp) {
+                st_v8(rowp + c / 2, w);
+                st_v8(rowp + c / 2 + 8, w + 8);
+              }
+            } else {
+              staged_store<16>(stg, w, rowp ? rowp + c / 2 : nullptr, valid_words<T>(p.n_out - col0 - c), lane);
+            }
             if (ci + 1 < NCH) tmem_wait_ld(ob[(ci + 1) & 1]);
           }
         };
@@ -1407,6 +1432,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, c
   p.status = a.status;
   p.k_blocks = (int)((a.K + tc::BK - 1) / tc::BK);
   p.half_tails = 1;
+  p.v8_out = a.n_out % 16 == 0 && reinterpret_cast<uintptr_t>(a.out) % 32 == 0;
   // CTA pairs halve the B bytes each SM stages per k-block; they pay off when
   // experts hold at least a full 128-row tile on average.  With fewer rows per
   // expert (decode-sized batches) the GEMM streams weights from HBM and single
