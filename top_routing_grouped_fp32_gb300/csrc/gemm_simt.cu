@@ -8,7 +8,8 @@
 // shapes the tcgen05 path cannot take (rows not a multiple of 16 bytes).
 //
 // Tiles of 64 rows x 64 columns, 16-deep K slices staged in shared memory as
-// FP32; 256 threads each own a 4x4 block (two of them for gate/up).  Epilogues:
+// FP32 (the next slice loaded into registers while the current one is
+// multiplied); 256 threads each own a 4x4 block (two of them for gate/up).  Epilogues:
 //   gate/up : h = silu(g) * u, with silu(z) = z / (1 + exp(-z))
 //   down    : out[r,:] = o                           (moe_experts_forward)
 //   weighted: slots[perm[r],:] = w[perm[r]] * o      (fused forward)
@@ -53,6 +54,8 @@ grouped_gemm_simt(const T* __restrict__ A, const T* __restrict__ B0, const T* __
   __shared__ uint32_t s_pref[1025];
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[kDual ? 2 : 1][BK][BN + 4];
+  pdl_wait();  // launched while the previous kernel finishes; its outputs are read below
+  pdl_trigger();
 
   // prefix of per-expert tile counts (E <= 1024)
   if (threadIdx.x < 32) {
@@ -95,24 +98,37 @@ grouped_gemm_simt(const T* __restrict__ A, const T* __restrict__ B0, const T* __
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[q][i][j] = 0.f;
 
-  for (int64_t k0 = 0; k0 < K; k0 += BK) {
-    // stage A[m0 .. m0+63][k0 .. k0+15] and W[n0 .. n0+63][k0 .. k0+15], transposed
+  // A[m0 .. m0+63][k0 .. k0+15] and W[n0 .. n0+63][k0 .. k0+15]: each thread
+  // loads 4 elements of each; the next slice is loaded into registers while
+  // the current one is multiplied from shared memory
+  constexpr int PER = (BM * BK) / 256;
+  float ra[PER], rb0[PER], rb1[PER];
+  auto load_slice = [&](int64_t k0) {
 #pragma unroll
-    for (int it = 0; it < (BM * BK) / 256; ++it) {
+    for (int it = 0; it < PER; ++it) {
       const int li = it * 256 + threadIdx.x;
       const int r = li / BK, kk = li % BK;
-      float a = 0.f;
-      if (r < rows && k0 + kk < K) a = to_f32<T>(A[(m0 + r) * K + k0 + kk]);
-      As[kk][r] = a;
-      float b0 = 0.f, b1 = 0.f;
+      ra[it] = (r < rows && k0 + kk < K) ? to_f32<T>(A[(m0 + r) * K + k0 + kk]) : 0.f;
+      rb0[it] = rb1[it] = 0.f;
       if (n0 + r < n_out && k0 + kk < K) {
-        b0 = to_f32<T>(W0[(n0 + r) * K + k0 + kk]);
-        if (kDual) b1 = to_f32<T>(W1[(n0 + r) * K + k0 + kk]);
+        rb0[it] = to_f32<T>(W0[(n0 + r) * K + k0 + kk]);
+        if (kDual) rb1[it] = to_f32<T>(W1[(n0 + r) * K + k0 + kk]);
       }
-      Bs[0][kk][r] = b0;
-      if (kDual) Bs[kDual ? 1 : 0][kk][r] = b1;
+    }
+  };
+  load_slice(0);
+  for (int64_t k0 = 0; k0 < K; k0 += BK) {
+    // stage the loaded slice, transposed
+#pragma unroll
+    for (int it = 0; it < PER; ++it) {
+      const int li = it * 256 + threadIdx.x;
+      const int r = li / BK, kk = li % BK;
+      As[kk][r] = ra[it];
+      Bs[0][kk][r] = rb0[it];
+      if (kDual) Bs[kDual ? 1 : 0][kk][r] = rb1[it];
     }
     __syncthreads();
+    if (k0 + BK < K) load_slice(k0 + BK);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       float a[4], b[4], c[4];
@@ -171,21 +187,18 @@ cudaError_t launch_t(const GemmArgs& a, cudaStream_t s) {
   const T* B0 = static_cast<const T*>(a.B0);
   const T* B1 = static_cast<const T*>(a.B1);
   T* out = static_cast<T*>(a.out);
+  const T* none = nullptr;
   switch (a.mode) {
     case kGateUpSwiglu:
-      grouped_gemm_simt<T, kGateUpSwiglu><<<grid, 256, 0, s>>>(A, B0, B1, a.E, a.K, a.n_out, a.offsets,
-                                                              out, a.perm, a.weights, (int)a.wdt);
-      break;
+      return launch_pdl(grouped_gemm_simt<T, kGateUpSwiglu>, grid, dim3(256), 0, s, A, B0, B1, a.E, a.K,
+                        a.n_out, a.offsets, out, a.perm, a.weights, (int)a.wdt);
     case kDownPlain:
-      grouped_gemm_simt<T, kDownPlain><<<grid, 256, 0, s>>>(A, B0, nullptr, a.E, a.K, a.n_out, a.offsets,
-                                                           out, a.perm, a.weights, (int)a.wdt);
-      break;
+      return launch_pdl(grouped_gemm_simt<T, kDownPlain>, grid, dim3(256), 0, s, A, B0, none, a.E, a.K,
+                        a.n_out, a.offsets, out, a.perm, a.weights, (int)a.wdt);
     default:
-      grouped_gemm_simt<T, kDownWeighted><<<grid, 256, 0, s>>>(A, B0, nullptr, a.E, a.K, a.n_out,
-                                                              a.offsets, out, a.perm, a.weights,
-                                                              (int)a.wdt);
+      return launch_pdl(grouped_gemm_simt<T, kDownWeighted>, grid, dim3(256), 0, s, A, B0, none, a.E, a.K,
+                        a.n_out, a.offsets, out, a.perm, a.weights, (int)a.wdt);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace
