@@ -113,7 +113,7 @@ struct Params {
   uint32_t* status;
   // backward products
   void* out2;          // second output (kSwigluBwd: a; kWgrad: rows >= split)
-  const void* da;      // kSwigluBwd: da = dout W_down, FP32 [rows, n_out]
+  const void* da;      // kSwigluBwd: da = dout W_down, 16-bit [rows, n_out]
   const uint32_t* pad; // pad[e] = sum over e' < e of roundup(rows of e', 64)
   // operand forms: A K-major (rows x K) or MN-major (K rows x M columns);
   // B K-major 3-D, MN-major 3-D (experts x K rows x N columns) or MN-major 2-D
@@ -849,7 +849,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         }
       } else if (p.mode == kSwigluBwd) {
         // accumulators g = x . W_gate[e]^T, u = x . W_up[e]^T (recomputed); with
-        // da = dout . W_down[e] (FP32, from the previous product):
+        // da = dout . W_down[e] (16-bit, from the previous product):
         // dg = da * u * silu'(g), du = da * silu(g) and the activation
         // a = silu(g) * u, stored in the 16-bit dtype in the 64-padded row
         // space (row - offsets[e] + pad[e]); the padding rows after an
@@ -863,24 +863,20 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         const uint32_t pe = __ldg(p.pad + t.e);
         const bool zero_row = !row_ok && local < (int64_t)(__ldg(p.pad + t.e + 1) - pe);
         const int64_t prow = (int64_t)pe + local;
-        const float* dasrc = static_cast<const float*>(p.da) + grow * I + col0;
+        const T* dasrc = static_cast<const T*>(p.da) + grow * I + col0;
         const bool store = row_ok || zero_row;
         uint32_t* dgp = store ? reinterpret_cast<uint32_t*>(out + prow * 2 * I + col0) : nullptr;
         uint32_t* dup_p = store ? reinterpret_cast<uint32_t*>(out + prow * 2 * I + I + col0) : nullptr;
         uint32_t* ap = store ? reinterpret_cast<uint32_t*>(static_cast<T*>(p.out2) + prow * I + col0) : nullptr;
-        // da of this row, 32 columns per chunk; the next chunk's loads are
-        // issued before the current chunk is computed so that their latency
+        // da of this row (16-bit), 32 columns per chunk; the next chunk's loads
+        // are issued before the current chunk is computed so that their latency
         // overlaps the TMEM reads and the arithmetic
         auto load_da = [&](int c, float (&d)[32]) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            float4 d0 = make_float4(0.f, 0.f, 0.f, 0.f), d1 = d0;
-            if (row_ok && col0 + c + v * 8 + 8 <= I) {
-              d0 = __ldg(reinterpret_cast<const float4*>(dasrc + c + v * 8));
-              d1 = __ldg(reinterpret_cast<const float4*>(dasrc + c + v * 8 + 4));
-            }
-            d[v * 8 + 0] = d0.x; d[v * 8 + 1] = d0.y; d[v * 8 + 2] = d0.z; d[v * 8 + 3] = d0.w;
-            d[v * 8 + 4] = d1.x; d[v * 8 + 5] = d1.y; d[v * 8 + 6] = d1.z; d[v * 8 + 7] = d1.w;
+            uint4 q = make_uint4(0u, 0u, 0u, 0u);
+            if (row_ok && col0 + c + v * 8 + 8 <= I) q = __ldg(reinterpret_cast<const uint4*>(dasrc + c + v * 8));
+            unpack8<T>(q, d + v * 8);
           }
         };
         // NF features of this warp: 128 (full tile) or 64 (half tile)
@@ -1200,7 +1196,7 @@ BwdLayout bwd_layout(int64_t N, int E, int64_t H, int64_t I) {
     return at;
   };
   L.pad = take((size_t)(E + 1) * 4);
-  L.da = take((size_t)N * I * 4);
+  L.da = take((size_t)N * I * 2);
   L.dgduP = take((size_t)L.npad * 2 * I * 2);
   L.actP = take((size_t)L.npad * I * 2);
   L.xP = take((size_t)L.npad * H * 2);
@@ -1238,7 +1234,7 @@ bool encode_3d_mn(CUtensorMap* m, const void* base, moe_dtype dt, uint64_t E, ui
 
 // Products of the backward, each one launch of grouped_gemm_tc, every weight
 // read in its stored layout (MN-major where the product needs it transposed):
-//   1. da     = dout W_down (W_down MN-major), FP32
+//   1. da     = dout W_down (W_down MN-major), in the 16-bit dtype
 //   2. g, u   = x W_gate^T, x W_up^T recomputed; the epilogue forms dg, du
 //               and a from them and da, in the padded row space
 //   3. dinput = dg W_gate + du W_up (weights MN-major; one accumulator over
@@ -1252,7 +1248,7 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   const moe_dtype dt = a.dt;
   const BwdLayout L = bwd_layout(N, E, H, I);
   uint32_t* pad = reinterpret_cast<uint32_t*>(ws + L.pad);
-  float* da = reinterpret_cast<float*>(ws + L.da);
+  void* da = ws + L.da;
   void* dgduP = ws + L.dgduP;
   void* actP = ws + L.actP;
   void* xP = ws + L.xP;
@@ -1312,9 +1308,9 @@ cudaError_t backward_t(const ExpertsBwdArgs& a, const TcWeights* w, char* ws, in
   base.status = a.status;
   base.wdt = (int)MOE_F32;
   base.pad = pad;
-  // 1. da = dout W_down (FP32)
+  // 1. da = dout W_down, stored in the 16-bit dtype
   Params p = base;
-  p.mode = kPlainF32;
+  p.mode = kDownPlain;
   p.b_form = kBMNmajor3d;
   p.k_blocks = (int)((H + BK - 1) / BK);
   p.cols_per_tile = 256;
