@@ -137,6 +137,11 @@ struct Params {
   // gate and up values of the same features in both tile forms
   int b_inter;
   int v8_out;  // out rows are 32-byte aligned segments (n_out % 16 == 0, 32-byte base)
+  // single CTAs (decode-sized batches): a tile of at most 32 rows loads A
+  // through a 32-row box (the mapA64 slot); the MMA still runs M = 128, and
+  // its other 96 rows multiply whatever the ring stage held before -- rows
+  // that are never stored
+  int thin_a;
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -474,6 +479,7 @@ struct Tile {
   int kx0;     // first K coordinate (0, or pad[e] for weight gradients)
   int nk;      // k-blocks of this tile
   bool half;   // M = 128 pair tile (64 rows per CTA): see Params::half_tails
+  bool thin;   // single-CTA tile of at most 32 rows: see Params::thin_a
 };
 
 __device__ __forceinline__ Tile decode_tile(uint32_t tile, const Params& p, const uint32_t* s_pref,
@@ -497,6 +503,7 @@ __device__ __forceinline__ Tile decode_tile(uint32_t tile, const Params& p, cons
   t.kx0 = 0;
   t.nk = p.k_blocks;
   t.half = p.half_tails && (int64_t)s_off[lo + 1] - t.m0 <= BM;
+  t.thin = p.thin_a && (int64_t)s_off[lo + 1] - t.m0 <= 32;
   return t;
 }
 
@@ -513,6 +520,7 @@ __device__ __forceinline__ Tile decode_wgrad(uint32_t tile, const Params& p, int
   t.kx0 = (int)k0;
   t.nk = (int)((k1 - k0) / BK);
   t.half = false;
+  t.thin = false;
   return t;
 }
 
@@ -565,7 +573,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   }
   if (warp == 0 && lane == 0) {
     prefetch_map(&mapA);
-    if (p.half_tails) prefetch_map(&mapA64);
+    if (p.half_tails || p.thin_a) prefetch_map(&mapA64);
     prefetch_map(&mapB0);
     prefetch_map(&mapB1);
   }
@@ -632,8 +640,10 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         const int b1row = b0row + p.b1_row_off;
         // interleaved gate/up B (pairs): this CTA's 64 gate rows and the same 64 up rows
         const int birow = b0row + (int)rank * 64;
-        const CUtensorMap* ma = t.half ? &mapA64 : &mapA;
-        const uint32_t stage_tx = t.half ? (C::STAGE_BYTES - KS * A_BYTES / 2) * PAIR : C::STAGE_BYTES * PAIR;
+        const CUtensorMap* ma = (t.half || t.thin) ? &mapA64 : &mapA;
+        const uint32_t stage_tx = t.half   ? (C::STAGE_BYTES - KS * A_BYTES / 2) * PAIR
+                                  : t.thin ? (C::STAGE_BYTES - KS * (A_BYTES - A_BYTES / 4)) * PAIR
+                                           : C::STAGE_BYTES * PAIR;
         for (int kb = 0; kb < t.nk; ++kb) {
           if (!mbar_wait<kCluster>(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
             ok = false;
@@ -1137,6 +1147,7 @@ cudaError_t launch_t(int64_t N, int E, const CUtensorMap& mA, const CUtensorMap&
                      const CUtensorMap& mB1, Params p, int num_sms, cudaStream_t s,
                      const CUtensorMap* mA64 = nullptr) {
   if (!mA64 || PAIR != 2) p.half_tails = 0;
+  if (!mA64 || PAIR != 1) p.thin_a = 0;
   int clusters = 0;
   cudaError_t err = resident_clusters<T, PAIR, KS>(num_sms, &clusters);
   if (err != cudaSuccess) return err;
@@ -1462,8 +1473,11 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights* w, int num_sms, c
       return tc::launch_t<__nv_bfloat16, 2, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s, &mA64);
     return tc::launch_t<__half, 2, 2>(a.N, a.E, mA, *b0, *b1, p, num_sms, s, &mA64);
   }
-  if (a.dt == MOE_BF16) return tc::launch_t<__nv_bfloat16, 1>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
-  return tc::launch_t<__half, 1>(a.N, a.E, mA, *b0, *b1, p, num_sms, s);
+  CUtensorMap mA32;
+  if (!tc::encode_2d(&mA32, a.A, a.dt, (uint64_t)a.N, (uint64_t)a.K, 32)) return cudaErrorInvalidValue;
+  p.thin_a = 1;
+  if (a.dt == MOE_BF16) return tc::launch_t<__nv_bfloat16, 1>(a.N, a.E, mA, *b0, *b1, p, num_sms, s, &mA32);
+  return tc::launch_t<__half, 1>(a.N, a.E, mA, *b0, *b1, p, num_sms, s, &mA32);
 }
 
 size_t experts_backward_tc_workspace(int64_t N, int E, int64_t H, int64_t I) {
