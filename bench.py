@@ -56,10 +56,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # reported as null once that source changes.
 GEMM_TRAFFIC = {
     # ncu --set full, one launch each on the headline workload: gate/up reads
-    # 1.141128 GB and writes 265.879040 MB, down reads 0.646934 GB and writes
-    # 374.243584 MB (ncu's units; the GB figures are rounded to the kilobyte)
-    "finegrained_bf16": {"bytes_per_launch": (1141128000 + 265879040 + 646934000 + 374243584) / 2,
-                         "source_sha256": "2f78a242694d6fe971fdb5c3ff13b2350540ecd348149483844eb278639fa517"},
+    # 1.141188 GB and writes 266.153472 MB, down reads 0.646926 GB and writes
+    # 374.187264 MB (ncu's units; the GB figures are rounded to the kilobyte)
+    "finegrained_bf16": {"bytes_per_launch": (1141188000 + 266153472 + 646926000 + 374187264) / 2,
+                         "source_sha256": "c428245e659ac7c743f21a7bbcc8124b7bb5526996ef31258dfabff46463b20b"},
 }
 
 
