@@ -636,13 +636,19 @@ def run_backward(args, rank, world, local):
         ev[4].record()
 
     K = max(1, args.steps)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K + 2)]
-    for _ in range(2):
+    W = max(3, args.warmup)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K + 1)]
+    for _ in range(W):
         step(evs[-1])
     torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    w0 = time.time()
     for i in range(K):
         step(evs[i])
     torch.cuda.synchronize(dev)
+    clock_info = clocks.stop(w0, time.time())
     names = ["combine_backward", "experts_backward", "dispatch_backward", "router_backward"]
     st = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
           for j, n in enumerate(names)}
@@ -652,11 +658,11 @@ def run_backward(args, rank, world, local):
     tensor = args.bwd_strategy == "tensor_core" or (args.bwd_strategy == "auto" and wl.dtype != "f32")
     if tensor:
         peaks, peaks_src = load_peaks()
+        peak, psrc = tensor_peak(peaks, peaks_src, clock_info)
         sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
         roof = {"bound": "tensor", "kernel": "experts backward (tcgen05 chain)", "achieved": ach,
-                "peak": sus, "unit": "TFLOP/s", "frac": ach / sus,
-                "peak_source": f"{peaks_src} bf16_tflops_sustained (timed inside the step loop)",
-                "frac_of_burst": ach / float(peaks["bf16_tflops"])}
+                "peak": peak, "unit": "TFLOP/s", "frac": ach / peak, "peak_source": psrc,
+                "frac_of_burst": ach / float(peaks["bf16_tflops"]), "frac_of_sustained": ach / sus}
     else:
         peak = 152 * 128 * 2 * 2.07e9 / 1e12
         roof = {"bound": "alu", "kernel": "experts backward (FP32 FMA)", "achieved": ach,
@@ -664,10 +670,10 @@ def run_backward(args, rank, world, local):
                 "peak_source": "152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz"}
     roof["algorithmic_per_launch"] = f"16*N*H*I = {flops:.4e} FLOP"
     line = {"metric": "MoE first-order backward tokens/s", "value": wl.T / (total * 1e-3),
-            "unit": "tokens/s", "n_gpus": 1, "steps": K, "mode": "backward",
+            "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": W, "mode": "backward",
             "bwd_strategy": "tensor_core" if tensor else "scalar",
             "ms_per_step": total, "higher_is_better": True, "dtype": wl.dtype, "data": "synthetic",
-            "config": workload_config(wl), "stages_ms": st, "roofline": roof}
+            "config": workload_config(wl), "stages_ms": st, "roofline": roof, "clocks": clock_info}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
