@@ -218,3 +218,53 @@ def test_tensor_core_backward_full_size(cuda_lib, name):
         _close(got, r, 2e-2, nm)
     for z in np.where(cnt == 0)[0]:
         assert torch.all(dgate[z] == 0) and torch.all(dup[z] == 0) and torch.all(ddown[z] == 0)
+
+
+@pytest.mark.slow
+def test_expert_backward_beyond_2g_elements(cuda_lib):
+    """Tensor-core backward over N = 1.12 M dispatched rows of H = 2048 (2.29 G
+    elements in x_disp, dout, dinput and the padded row copies), so every
+    element offset past 2^31 must be computed in 64 bits.  The first and the
+    last expert hold a few hundred rows (the last one's rows, and its padded
+    rows, lie past 2^31 elements) and are checked in full against the oracle:
+    dinput on all their rows and all three weight gradients.  dinput is also
+    checked on a sample of rows of every other expert (first, last and random
+    rows), which the oracle evaluates row by row."""
+    E, H, I = 16, 2048, 128
+    rng = np.random.default_rng(61)
+    mid = rng.integers(79000, 81000, size=E - 2)
+    counts = np.concatenate([[200], mid, [300]]).astype(np.int64)
+    N = int(counts.sum())
+    assert N * H > 2 ** 31
+    wl = small_workload(64, E, 1, H, I, dtype="bf16", seed=62)
+    inp = make_inputs(wl, device="cuda")
+    experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    g = torch.Generator(device="cuda").manual_seed(63)
+    x_disp = torch.randn((N, H), generator=g, device="cuda").to(torch.bfloat16)
+    dout = torch.randn((N, H), generator=g, device="cuda").to(torch.bfloat16)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.uint32)
+    offsets = torch.from_numpy(off.view(np.int32)).cuda()
+    dinput, dgate, dup, ddown = experts.backward(x_disp, offsets, dout, strategy="tensor_core")
+    torch.cuda.synchronize()
+    gate, up, down = stored(inp["gate"]), stored(inp["up"]), stored(inp["down"])
+    for e in (0, E - 1):
+        a, b = int(off[e]), int(off[e + 1])
+        sub = np.array([0, b - a], dtype=np.uint32)
+        ref = oracle.experts_backward(values(x_disp[a:b]), sub, gate[e:e + 1], up[e:e + 1], down[e:e + 1],
+                                      "bf16", values(dout[a:b]))
+        assert_y_close(dinput[a:b], ref[0], "bf16", f"dinput, expert {e}")
+        for name, got, r in (("dgate", dgate[e:e + 1], ref[1]), ("dup", dup[e:e + 1], ref[2]),
+                             ("ddown", ddown[e:e + 1], ref[3])):
+            _close(got, r, 2e-2, f"{name}, expert {e}")
+    # sampled rows of the other experts, each expert's sample its own sub-problem
+    for e in range(1, E - 1):
+        a, b = int(off[e]), int(off[e + 1])
+        rows = np.unique(np.concatenate([[a, b - 1], rng.integers(a, b, size=30)]))
+        sel = torch.as_tensor(rows, device="cuda")
+        sub = np.array([0, len(rows)], dtype=np.uint32)
+        ref = oracle.experts_backward(values(x_disp[sel]), sub, gate[e:e + 1], up[e:e + 1], down[e:e + 1],
+                                      "bf16", values(dout[sel]))
+        assert_y_close(dinput[sel], ref[0], "bf16", f"dinput rows of expert {e}")
+        assert torch.isfinite(dgate[e]).all() and torch.isfinite(ddown[e]).all()
+    del x_disp, dout, dinput, dgate, dup, ddown, experts, inp
+    torch.cuda.empty_cache()

@@ -164,6 +164,50 @@ def test_forward_full_workloads(cuda_lib, name, dtype):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.slow
+def test_forward_beyond_2g_elements(cuda_lib):
+    """More than 2^31 elements in the dispatched rows and in the slot buffer
+    (N = 1.12 M rows of H = 2048: 2.29 G elements), so every element offset
+    past 2^31 must be computed in 64 bits: the gather, the GEMMs' row
+    addressing, the weighted slot stores and the combine.  Routing and
+    dispatch over every token and x_disp in full; y bit for bit the slot sum
+    on every element; y against the oracle on a token sample that reaches
+    every 128-row block of every segment and the last tokens (whose slots lie
+    past 2^31 elements); the staged path (expert_out [N, H], moe_combine)
+    against the oracle on the same sample."""
+    T, E, k, H, I = 140000, 16, 8, 2048, 128
+    assert T * k * H > 2 ** 31
+    wl = small_workload(T, E, k, H, I, dtype="bf16", renormalize=True, seed=31)
+    inp = make_inputs(wl, device="cuda")
+    experts, ws, y = _forward(cuda_lib, wl, inp)
+    o_idx, o_off = _check_routing_and_dispatch(experts, ws, wl, inp["logits"], inp["x"])
+    lay = experts.forward_layout(T, k, inp["logits"].dtype)
+    slots = ws[lay["slots"]:lay["slots"] + T * k * H * 2].view(torch.bfloat16).view(T, k, H)
+    acc = torch.zeros((T, H), dtype=torch.float32, device="cuda")
+    for j in range(k):
+        acc += slots[:, j].float()
+    assert torch.equal(y.view(torch.int16), acc.to(torch.bfloat16).view(torch.int16))
+    assert cuda_lib.moe_get_device_status(ws) == 0
+    del acc, slots, ws
+    torch.cuda.empty_cache()
+    _, _, o_perm, _ = oracle.dispatch(o_idx, wl.E)
+    toks = _tile_cover_tokens(wl, o_off, o_perm) | set(range(T - 8, T)) | {0}
+    _assert_every_tile_hit(wl, o_off, o_perm, toks)
+    toks = np.array(sorted(toks))
+    _, _, ref = oracle_forward_sample(inp, k, True, toks, "bf16")
+    assert_y_close(y[torch.as_tensor(toks, device="cuda")], ref, "bf16")
+    # the staged calls: route, dispatch, expert forward into [N, H], combine
+    idx, w = cuda_lib.moe_route(inp["logits"], k, True)
+    d = cuda_lib.moe_dispatch(idx, wl.E, x=inp["x"])
+    out = experts.forward_dispatched(d.x_disp, d.offsets)
+    assert out.shape == (T * k, H)
+    y2 = cuda_lib.moe_combine(out, d.perm, w, k)
+    torch.cuda.synchronize()
+    assert_y_close(y2[torch.as_tensor(toks, device="cuda")], ref, "bf16")
+    del experts, y, y2, out, d, inp
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("T,E,k,H,I,dtype", [
     (1000, 16, 4, 512, 256, "bf16"),   # CTA-pair tiles
     (700, 3, 3, 72, 64, "f16"),        # a 72-column row
