@@ -52,14 +52,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic per grouped_gemm_tc launch (mean of the gate/up and the down
 # launch, dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
-# each workload, with the SHA-256 of the kernel source it was taken on; it is
-# reported as null once that source changes.
+# each workload, with the SHA-256 of the kernel source's code (comments and
+# white space left out) it was taken on; it is reported as null once that
+# code changes.
 GEMM_TRAFFIC = {
     # ncu --set full, one launch each on the headline workload: gate/up reads
     # 1.141188 GB and writes 266.153472 MB, down reads 0.646926 GB and writes
     # 374.187264 MB (ncu's units; the GB figures are rounded to the kilobyte)
     "finegrained_bf16": {"bytes_per_launch": (1141188000 + 266153472 + 646926000 + 374187264) / 2,
-                         "source_sha256": "c428245e659ac7c743f21a7bbcc8124b7bb5526996ef31258dfabff46463b20b"},
+                         "code_sha256": "abad0710fabf29ebf59ffffcfa619bc73f8d2bcb79ca4d222b98e3b54a4f1bdb"},
 }
 
 
@@ -146,9 +147,34 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_sha256(rel: str) -> str:
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def code_sha256(rel: str) -> str:
+    """SHA-256 of a C/C++/CUDA source with its comments removed and every run
+    of white space collapsed to one blank: editing a comment leaves it
+    unchanged, editing code does not.  String and character literals are
+    copied as they stand."""
+    with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+        text = f.read()
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    code = " ".join("".join(out).split())
+    return hashlib.sha256(code.encode()).hexdigest()
 
 
 class ClockSampler:
@@ -385,7 +411,7 @@ def gemm_traffic(wl):
     """Mean DRAM bytes per grouped_gemm_tc launch from the committed ncu capture
     of this workload, or None once the kernel source has changed."""
     rec = GEMM_TRAFFIC.get(wl.name)
-    if not rec or rec["source_sha256"] != source_sha256("top_routing_grouped_fp32_gb300/csrc/gemm_tc.cu"):
+    if not rec or rec["code_sha256"] != code_sha256("top_routing_grouped_fp32_gb300/csrc/gemm_tc.cu"):
         return None
     return rec["bytes_per_launch"]
 

@@ -50,10 +50,10 @@ def test_fp32_roofline_is_the_ffma_pipe():
 
 def test_traffic_is_dropped_when_the_kernel_source_changes(monkeypatch):
     wl = WORKLOADS["finegrained_bf16"]
-    sha = bench.source_sha256("top_routing_grouped_fp32_gb300/csrc/gemm_tc.cu")
-    monkeypatch.setitem(bench.GEMM_TRAFFIC, wl.name, {"bytes_per_launch": 123.0, "source_sha256": sha})
+    sha = bench.code_sha256("top_routing_grouped_fp32_gb300/csrc/gemm_tc.cu")
+    monkeypatch.setitem(bench.GEMM_TRAFFIC, wl.name, {"bytes_per_launch": 123.0, "code_sha256": sha})
     assert bench.gemm_traffic(wl) == 123.0
-    monkeypatch.setitem(bench.GEMM_TRAFFIC, wl.name, {"bytes_per_launch": 123.0, "source_sha256": "0" * 64})
+    monkeypatch.setitem(bench.GEMM_TRAFFIC, wl.name, {"bytes_per_launch": 123.0, "code_sha256": "0" * 64})
     assert bench.gemm_traffic(wl) is None
     assert bench.gemm_traffic(WORKLOADS["mixtral_bf16"]) is None  # no capture of that workload
 
@@ -63,3 +63,21 @@ def test_launch_count_per_step():
     assert bench.launches_per_step(16384, 64) == 7
     # a large chunk-histogram table adds the scan kernel
     assert bench.launches_per_step(65536 * 4, 1024) == 8
+
+
+def test_code_fingerprint_ignores_comments_not_code(tmp_path, monkeypatch):
+    src = 'int f(int a) {  // add one\n  /* "x" */ return a + 1; }\nconst char* s = "// kept";\n'
+    (tmp_path / "a.cu").write_text(src)
+    (tmp_path / "b.cu").write_text(src.replace("// add one", "// adds one, see below").replace("  ", " "))
+    (tmp_path / "c.cu").write_text(src.replace("a + 1", "a + 2"))
+    (tmp_path / "d.cu").write_text(src.replace('"// kept"', '"// changed"'))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    a, b, c, d = (bench.code_sha256(n) for n in ("a.cu", "b.cu", "c.cu", "d.cu"))
+    assert a == b
+    assert a != c and a != d
+
+
+def test_traffic_record_matches_the_committed_kernel():
+    """The committed capture was taken on the code now in gemm_tc.cu."""
+    rec = bench.GEMM_TRAFFIC["finegrained_bf16"]
+    assert rec["code_sha256"] == bench.code_sha256("top_routing_grouped_fp32_gb300/csrc/gemm_tc.cu")

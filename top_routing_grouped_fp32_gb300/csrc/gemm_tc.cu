@@ -24,9 +24,11 @@
 //     and one 128-row half of B (for gate/up: 64 gate rows and the same 64 up
 //     rows, so that every accumulator lane holds gate and up of the same
 //     features; for down: one half of the 256 down rows), so an SM moves
-//     32 KiB per 64-deep k-block instead of 48 KiB and a 6-stage ring fits in
-//     shared memory; PAIR = 1 is the single-CTA form (M=128, both B halves
-//     staged locally, 4 stages);
+//     32 KiB per 64-deep k-block instead of 48 KiB; the forward products
+//     ring three 128-deep stages of 64 KiB (KS = 2), the backward products
+//     and long-K down projections six 64-deep ones; PAIR = 1 is the
+//     single-CTA form (M=128, both B halves staged locally, 4 stages; a tile
+//     of at most 32 rows loads A through a 32-row box);
 //   * warp 0: TMA producer (cp.async.bulk.tensor, 128-byte swizzle); its
 //     copies complete on the leader CTA's "full" barrier;
 //   * warp 1: allocates 512 TMEM columns; in the leader CTA one thread issues
