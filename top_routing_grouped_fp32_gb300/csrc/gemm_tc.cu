@@ -103,7 +103,7 @@ struct Params {
   int E;
   int nb;             // n-blocks per m-tile
   int panel;          // n-blocks per raster panel
-  int k_blocks;
+  int k_blocks;       // k-blocks per tile: 64-deep, 128-deep when KS = 2
   int mode;
   int cols_per_tile;  // output columns per tile: 128 (gate/up) or 256 (down)
   int b1_row_off;     // row offset of the second B box inside the n-block
