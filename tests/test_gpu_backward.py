@@ -191,8 +191,10 @@ def test_router_weights_and_backward(cuda_lib, scoring, renorm, scale, dtype, E,
 @pytest.mark.parametrize("name", ["finegrained_bf16", "skewed_bf16"])
 def test_tensor_core_backward_full_size(cuda_lib, name):
     """Full-size workload through the tensor-core strategy; the oracle checks the
-    smallest non-empty expert completely (its rows' dinput and its three weight
-    gradients, as a one-expert problem) and every empty expert is all zeros."""
+    smallest and the largest non-empty expert completely (their rows' dinput and
+    their three weight gradients, each as a one-expert problem), dinput on a
+    sample of rows of every other non-empty expert (first, last and random
+    rows, evaluated row by row), and every empty expert is all zeros."""
     wl = WORKLOADS[name]
     inp = make_inputs(wl, device="cuda")
     experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
@@ -207,15 +209,32 @@ def test_tensor_core_backward_full_size(cuda_lib, name):
     dinput, dgate, dup, ddown = experts.backward(d.x_disp[:N], d.offsets, dout[:N], strategy="tensor_core")
     torch.cuda.synchronize()
     cnt = np.diff(off)
-    e = int(np.argmin(np.where(cnt > 0, cnt, np.iinfo(np.int64).max)))
-    r0, r1 = int(off[e]), int(off[e + 1])
-    sel = torch.as_tensor([e], device="cuda")
-    ref = oracle.experts_backward(xd[r0:r1], np.array([0, r1 - r0], np.uint32),
-                                  stored(inp["gate"].index_select(0, sel)), stored(inp["up"].index_select(0, sel)),
-                                  stored(inp["down"].index_select(0, sel)), wl.dtype, values(dout[r0:r1]))
-    assert_y_close(dinput[r0:r1], ref[0], wl.dtype, "dinput")
-    for nm, got, r in (("dgate", dgate[e], ref[1][0]), ("dup", dup[e], ref[2][0]), ("ddown", ddown[e], ref[3][0])):
-        _close(got, r, 2e-2, nm)
+    small = int(np.argmin(np.where(cnt > 0, cnt, np.iinfo(np.int64).max)))
+    large = int(np.argmax(cnt))
+
+    def one_expert(e, rows):
+        sel = torch.as_tensor([e], device="cuda")
+        return oracle.experts_backward(xd[rows], np.array([0, len(rows)], np.uint32),
+                                       stored(inp["gate"].index_select(0, sel)),
+                                       stored(inp["up"].index_select(0, sel)),
+                                       stored(inp["down"].index_select(0, sel)), wl.dtype,
+                                       values(dout[torch.as_tensor(rows, device="cuda")]))
+
+    for e in sorted({small, large}):
+        rows = np.arange(int(off[e]), int(off[e + 1]))
+        ref = one_expert(e, rows)
+        assert_y_close(dinput[int(off[e]):int(off[e + 1])], ref[0], wl.dtype, f"dinput, expert {e}")
+        for nm, got, r in (("dgate", dgate[e], ref[1][0]), ("dup", dup[e], ref[2][0]),
+                           ("ddown", ddown[e], ref[3][0])):
+            _close(got, r, 2e-2, f"{nm}, expert {e}")
+    rng = np.random.default_rng(18)
+    for e in np.where(cnt > 0)[0]:
+        if e in (small, large):
+            continue
+        a, b = int(off[e]), int(off[e + 1])
+        rows = np.unique(np.concatenate([[a, b - 1], rng.integers(a, b, size=6)]))
+        ref = one_expert(int(e), rows)
+        assert_y_close(dinput[torch.as_tensor(rows, device="cuda")], ref[0], wl.dtype, f"dinput rows of expert {e}")
     for z in np.where(cnt == 0)[0]:
         assert torch.all(dgate[z] == 0) and torch.all(dup[z] == 0) and torch.all(ddown[z] == 0)
 
