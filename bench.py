@@ -12,10 +12,12 @@ ranks need no data exchange: weak scaling); the time is the max over ranks.
 Exactly K steps are timed between a barrier and device synchronisations; when
 K steps take less than --min-seconds (0.5 s), that timed loop is repeated so
 that the nvidia-smi sampler (50 ms) records at least ~10 clock samples inside
-the window, and the per-step figures are the mean over all repetitions.  The
-roofline's peak follows that clock record: the burst BF16 figure when the
-median SM clock sat at its maximum with no sw_power_cap sample, else the
-sustained one.  The default run then measures the other four workloads and
+the window.  There are at least two repetitions: the step time is the mean
+over all but the last, which also records the per-stage events (an event
+between two launches stops their programmatic-launch overlap) and gives the
+stage times and the roofline.  The roofline's peak follows the window's clock
+record: the burst BF16 figure when the median SM clock sat at its maximum with
+no sw_power_cap sample, else the sustained one.  The default run then measures the other four workloads and
 the headline in FP16 the same way, under the line's "workloads" key.
 
 ``--impl reference`` times the FP64 CPU oracle (the only reference this
@@ -420,8 +422,10 @@ def measure_forward(moe, wl, args, world, dev, min_seconds, K, warmup, keep=Fals
     """Warm-up, then repetitions of exactly K timed forward steps (each between
     a barrier and device synchronisations, events on the launching stream)
     until at least `min_seconds` of timed work, so that the clock sampler sees
-    at least ~10 samples inside the window.  Returns per-step figures over all
-    repetitions."""
+    at least ~10 samples inside the window.  The step time is the mean over
+    the plain repetitions; the last repetition also records events between
+    the launches, and the per-stage times (so the roofline) come from it, under
+    the same clocks."""
     import torch
     from top_routing_grouped_fp32_gb300.inputs import make_inputs
     inp = make_inputs(wl, device=dev)
@@ -448,47 +452,58 @@ def measure_forward(moe, wl, args, world, dev, min_seconds, K, warmup, keep=Fals
     torch.cuda.synchronize(dev)
 
     stage_sum = {n: 0.0 for n in STAGES}
-    span_sum = 0.0  # route start -> combine end, summed over steps (flush excluded)
+    span_sum = 0.0  # route start -> combine end, summed over instrumented steps (flush excluded)
     rep_ms = []
+    inst_reps = []
     clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.3)  # let the sampler start before the timed region
     w0 = time.time()
-    reps = 1
+    reps = 2
     r = 0
     while r < reps:
+        # Stage events between launches stop the programmatic-launch overlap of
+        # the kernels they separate, so only the last repetition (every one
+        # under --l2-flush, whose step time is the event span) records them;
+        # the others time K plain steps.
+        inst = flush is not None or r == reps - 1
         barrier(world, dev)
         torch.cuda.synchronize(dev)
         start.record(stream)
         for i in range(K):
-            step(ev[i], i)
+            step(ev[i] if inst else None, i)
         end.record(stream)
         torch.cuda.synchronize(dev)
         rep_ms.append(max_over_ranks(start.elapsed_time(end), world, dev))
-        for i in range(K):
-            for j, n in enumerate(STAGES):
-                stage_sum[n] += ev[i][j].elapsed_time(ev[i][j + 1])
-            span_sum += ev[i][0].elapsed_time(ev[i][5])
-        if r == 0:  # the same repetition count on every rank
-            reps = max(1, int(math.ceil(min_seconds * 1e3 / max(rep_ms[0], 1e-3))))
+        inst_reps.append(inst)
+        if inst:
+            for i in range(K):
+                for j, n in enumerate(STAGES):
+                    stage_sum[n] += ev[i][j].elapsed_time(ev[i][j + 1])
+                span_sum += ev[i][0].elapsed_time(ev[i][5])
+        if r == 0:  # the same repetition count on every rank; at least one plain and one instrumented
+            reps = max(2, int(math.ceil(min_seconds * 1e3 / max(rep_ms[0], 1e-3))))
             reps = int(max_over_ranks(float(reps), world, dev))
         r += 1
     w1 = time.time()
     clock_info = clocks.stop(w0, w1)
     status = moe.moe_get_device_status(ws)
-    steps = K * reps
-    stage = {n: v / steps for n, v in stage_sum.items()}
+    n_inst = K * sum(inst_reps)
+    stage = {n: v / n_inst for n, v in stage_sum.items()}
     if flush is not None:
         # the flush is outside the forward: the per-step time is its event span
-        ms_step = max_over_ranks(span_sum / steps, world, dev)
+        ms_step = max_over_ranks(span_sum / n_inst, world, dev)
+        steps = K * reps
     else:
-        ms_step = sum(rep_ms) / steps
+        plain = [m for m, i in zip(rep_ms, inst_reps) if not i]
+        steps = K * len(plain)
+        ms_step = sum(plain) / steps
     lay = experts.forward_layout(wl.T, wl.top_k, inp["logits"].dtype)
     off = ws[lay["offsets"]:lay["offsets"] + 4 * (wl.E + 1)].view(torch.int32).cpu()
     touched = int(((off[1:] - off[:-1]) != 0).sum().item())
     res = {"value": wl.T * world / (ms_step * 1e-3), "ms_per_step": ms_step, "repeats": reps,
-           "rep_ms_per_step": [m / K for m in rep_ms], "stages_ms": stage, "clocks": clock_info,
-           "touched": touched, "device_status": status,
+           "rep_ms_per_step": [m / K for m in rep_ms], "rep_stage_events": inst_reps,
+           "stages_ms": stage, "clocks": clock_info, "touched": touched, "device_status": status,
            "gpu_launches": launches_per_step(wl.T, wl.E) * steps}
     if keep:
         res["_state"] = (inp, experts, ws, y, stream)
@@ -576,7 +591,7 @@ def run_native(args, rank, world, local):
         line = {
             "metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "repeats": res["repeats"],
-            "rep_ms_per_step": res["rep_ms_per_step"],
+            "rep_ms_per_step": res["rep_ms_per_step"], "rep_stage_events": res["rep_stage_events"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
             "data": "synthetic (seeded randn, BF16 weights ~N(0,1/fan_in)); no dataset, random-init weights",
             "config": workload_config(wl, args.l2_flush),
