@@ -645,9 +645,11 @@ def run_native(args, rank, world, local):
 def run_backward(args, rank, world, local):
     """Times the first-order backward chain (user guide section 12) after a
     staged forward: combine backward -> expert backward -> dispatch backward
-    -> router backward.  The expert backward's roofline is the tensor pipe
-    (measured bf16 peak) for the tensor-core strategy, else the FP32 FMA pipe:
-    152 SMs x 128 lanes x 2 FLOP x the max SM clock."""
+    -> router backward.  The step time is K plain steps between two events;
+    K more steps record events between the stages for the split.  The expert
+    backward's roofline is the tensor pipe (measured bf16 peak) for the
+    tensor-core strategy, else the FP32 FMA pipe: 152 SMs x 128 lanes x 2 FLOP
+    x the max SM clock."""
     import torch
     import top_routing_grouped_fp32_gb300 as moe
     from top_routing_grouped_fp32_gb300.inputs import WORKLOADS, make_inputs, with_dtype
@@ -664,28 +666,39 @@ def run_backward(args, rank, world, local):
     N = wl.T * wl.top_k
     bws = moe._workspace(ex._lib.moe_experts_backward_workspace_size(ex.handle, N), dev)
 
-    def step(ev):
-        ev[0].record()
+    def step(ev=None):
+        rec = (lambda j: ev[j].record()) if ev else (lambda j: None)
+        rec(0)
         dex, dwt = moe.moe_combine_backward(eo, d.perm, w, dy, wl.top_k)
-        ev[1].record()
+        rec(1)
         dinput, dgate, dup, ddown = ex.backward(d.x_disp, d.offsets, dex, workspace=bws,
                                                 strategy=args.bwd_strategy)
-        ev[2].record()
+        rec(2)
         moe.moe_dispatch_backward(dinput, d.perm, wl.T, wl.top_k)
-        ev[3].record()
+        rec(3)
         moe.moe_router_backward(inp["logits"], idx, dwt, "softmax", wl.renormalize, 1.0)
-        ev[4].record()
+        rec(4)
 
     K = max(1, args.steps)
     W = max(3, args.warmup)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K + 1)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     for _ in range(W):
-        step(evs[-1])
+        step()
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     w0 = time.time()
+    # K plain steps give the step time; K more with events between the stages
+    # (which stop the overlap of the launches they separate) give the split
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    start.record()
+    for i in range(K):
+        step()
+    end.record()
+    torch.cuda.synchronize(dev)
+    total = start.elapsed_time(end) / K
     for i in range(K):
         step(evs[i])
     torch.cuda.synchronize(dev)
@@ -693,7 +706,6 @@ def run_backward(args, rank, world, local):
     names = ["combine_backward", "experts_backward", "dispatch_backward", "router_backward"]
     st = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
           for j, n in enumerate(names)}
-    total = sum(st.values())
     flops = 16.0 * N * wl.H * wl.I  # recompute g,u (4) + da (2) + dinput (4) + 3 weight grads (6)
     ach = flops / (st["experts_backward"] * 1e-3) / 1e12
     tensor = args.bwd_strategy == "tensor_core" or (args.bwd_strategy == "auto" and wl.dtype != "f32")
