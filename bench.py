@@ -645,8 +645,9 @@ def run_native(args, rank, world, local):
 def run_backward(args, rank, world, local):
     """Times the first-order backward chain (user guide section 12) after a
     staged forward: combine backward -> expert backward -> dispatch backward
-    -> router backward.  The step time is K plain steps between two events;
-    K more steps record events between the stages for the split.  The expert
+    -> router backward.  The step time is K plain steps timed in blocks; K more
+    steps, in blocks alternating with those, record events between the stages
+    for the split.  The expert
     backward's roofline is the tensor pipe (measured bf16 peak) for the
     tensor-core strategy, else the FP32 FMA pipe: 152 SMs x 128 lanes x 2 FLOP
     x the max SM clock."""
@@ -690,18 +691,26 @@ def run_backward(args, rank, world, local):
     time.sleep(0.3)
     w0 = time.time()
     # K plain steps give the step time; K more with events between the stages
-    # (which stop the overlap of the launches they separate) give the split
+    # (which stop the overlap of the launches they separate) give the split.
+    # The two kinds alternate in blocks, so that both see the same clocks.
+    nblk = min(5, K)
+    plain_ms, plain_steps, done = 0.0, 0, 0
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for b in range(nblk):
+        n = (K - done) // (nblk - b)
+        torch.cuda.synchronize(dev)
+        start.record()
+        for _ in range(n):
+            step()
+        end.record()
+        torch.cuda.synchronize(dev)
+        plain_ms += start.elapsed_time(end)
+        plain_steps += n
+        for i in range(done, done + n):
+            step(evs[i])
+        done += n
     torch.cuda.synchronize(dev)
-    start.record()
-    for i in range(K):
-        step()
-    end.record()
-    torch.cuda.synchronize(dev)
-    total = start.elapsed_time(end) / K
-    for i in range(K):
-        step(evs[i])
-    torch.cuda.synchronize(dev)
+    total = plain_ms / plain_steps
     clock_info = clocks.stop(w0, time.time())
     names = ["combine_backward", "experts_backward", "dispatch_backward", "router_backward"]
     st = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
