@@ -89,6 +89,8 @@ def parse_args(argv=None):
                    help="steps of the host-buffer legs (default: the device loop's steps x repeats, so "
                         "that they run as long and see the same clocks)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-graph", action="store_true",
+                   help="skip the extra measurement of the step replayed from a captured CUDA graph")
     p.add_argument("--no-workloads", action="store_true",
                    help="skip the other workloads measured after the headline in the default run")
     p.add_argument("--min-seconds", type=float, default=0.5,
@@ -505,12 +507,45 @@ def measure_forward(moe, wl, args, world, dev, min_seconds, K, warmup, keep=Fals
            "rep_ms_per_step": [m / K for m in rep_ms], "rep_stage_events": inst_reps,
            "stages_ms": stage, "clocks": clock_info, "touched": touched, "device_status": status,
            "gpu_launches": launches_per_step(wl.T, wl.E) * steps}
+    if not args.no_graph and flush is None:
+        res["graph"] = measure_graph(experts, inp, wl, y, ws, stream, K, steps, world, dev)
     if keep:
         res["_state"] = (inp, experts, ws, y, stream)
     else:
         del inp, experts, ws, y, flush
         torch.cuda.empty_cache()
     return res
+
+
+def measure_graph(experts, inp, wl, y, ws, stream, K, steps, world, dev):
+    """The same step captured once into a CUDA graph (the library's calls only
+    enqueue work, so they capture) and replayed: as many replays as the plain
+    timed steps, K per event pair.  An extra figure beside the call a user
+    makes; it shows how much of a launch-bound step is host work."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        experts.forward(inp["x"], inp["logits"], wl.top_k, wl.renormalize, y=y, workspace=ws)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    total, done = 0.0, 0
+    while done < steps:
+        n = min(K, steps - done)
+        barrier(world, dev)
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for _ in range(n):
+            g.replay()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        total += max_over_ranks(start.elapsed_time(end), world, dev)
+        done += n
+    ms = total / done
+    del g
+    return {"value": wl.T * world / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": done,
+            "what": "the step replayed from one captured CUDA graph"}
 
 
 def measure_e2e(wl, world, dev, inp, experts, stream, Ke):
@@ -598,7 +633,7 @@ def run_native(args, rank, world, local):
             "stages_ms": res["stages_ms"],
             "roofline": roof,
             "e2e": e2e, "e2e_serial": e2e_serial,
-            "gpu_launches": res["gpu_launches"],
+            "gpu_launches": res["gpu_launches"], "graph": res.get("graph"),
             "clocks": res["clocks"],
             "device_status": res["device_status"],
         }
@@ -616,7 +651,7 @@ def run_native(args, rank, world, local):
                              "repeats": r["repeats"], "stages_ms": r["stages_ms"],
                              "roofline": roofline_for(swl, r["stages_ms"], r["touched"], r["clocks"],
                                                       peaks, peaks_src, gemm_traffic(swl)),
-                             "touched_experts": r["touched"], "clocks": r["clocks"],
+                             "touched_experts": r["touched"], "clocks": r["clocks"], "graph": r.get("graph"),
                              "device_status": r["device_status"]}
         if rank == 0:
             line["workloads"] = side
