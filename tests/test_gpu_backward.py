@@ -96,6 +96,35 @@ def test_expert_backward_segment_tails(cuda_lib, dtype):
     assert torch.all(dgate[E - 1] == 0) and torch.all(ddown[E - 1] == 0)
 
 
+def test_expert_backward_single_cta_segment_tails(cuda_lib):
+    """Tensor-core strategy on single-CTA tiles (N < 128 E) with chosen segment
+    lengths: 1, 31, 32, 33, 64, 127, 128, 129 and 200 rows and an empty
+    expert, K and N ragged."""
+    counts = [1, 31, 32, 33, 64, 127, 128, 129, 200, 0]
+    E, H, I = len(counts), 264, 200
+    N = sum(counts)
+    assert N < 128 * E
+    wl = small_workload(64, E, 1, H, I, dtype="bf16", seed=47)
+    inp = make_inputs(wl, device="cuda")
+    experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    g = torch.Generator(device="cuda").manual_seed(48)
+    x_disp = torch.randn((N, H), generator=g, device="cuda").to(torch.bfloat16)
+    dout = torch.randn((N, H), generator=g, device="cuda").to(torch.bfloat16)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.uint32)
+    offsets = torch.from_numpy(off.view(np.int32)).cuda()
+    dinput, dgate, dup, ddown = experts.backward(x_disp, offsets, dout, strategy="tensor_core")
+    torch.cuda.synchronize()
+    ref = oracle.experts_backward(values(x_disp), off, stored(inp["gate"]), stored(inp["up"]),
+                                  stored(inp["down"]), "bf16", values(dout))
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            assert_y_close(dinput[a:b], ref[0][a:b], "bf16", f"dinput, expert {e} ({b - a} rows)")
+    for name, got, r in (("dgate", dgate, ref[1]), ("dup", dup, ref[2]), ("ddown", ddown, ref[3])):
+        _close(got, r, 2e-2, name)
+    assert torch.all(dgate[E - 1] == 0) and torch.all(ddown[E - 1] == 0)
+
+
 @pytest.mark.parametrize("strategy", ["scalar", "tensor_core"])
 def test_expert_backward_empty_experts_get_zero(cuda_lib, strategy):
     wl = small_workload(100, 8, 1, 64, 64, dtype="bf16", seed=3, skew=6.0)

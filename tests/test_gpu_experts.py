@@ -93,6 +93,34 @@ def test_experts_segment_tails(cuda_lib, dtype):
             assert_y_close(out[a:b], ref[a:b], dtype, f"expert {e} ({b - a} rows)")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_experts_single_cta_segment_tails(cuda_lib, dtype):
+    """Chosen segment lengths on single-CTA tiles (N < 128 E): segments of
+    1, 31 and 32 rows (thin tiles: A through a 32-row box), 33, 64, 127 and 128
+    rows (full 128-row boxes), 129 and 200 rows (two tiles, the second holding
+    1 or 72 rows, thin or not) and an empty expert; K = 264 and N = 200 leave
+    ragged k-blocks and columns."""
+    counts = [1, 31, 32, 33, 64, 127, 128, 129, 200, 0]
+    E, H, I = len(counts), 264, 200
+    N = sum(counts)
+    assert N < 128 * E
+    wl = small_workload(64, E, 1, H, I, dtype=dtype, seed=45)
+    inp = make_inputs(wl, device="cuda")
+    experts = cuda_lib.SwiGluExperts(inp["gate"], inp["up"], inp["down"])
+    g = torch.Generator(device="cuda").manual_seed(46)
+    x_disp = torch.randn((N, H), generator=g, device="cuda").to(inp["x"].dtype)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.uint32)
+    offsets = torch.from_numpy(off.view(np.int32)).cuda()
+    out = experts.forward_dispatched(x_disp, offsets)
+    torch.cuda.synchronize()
+    ref = oracle.experts(values(x_disp), off, stored(inp["gate"]), stored(inp["up"]), stored(inp["down"]),
+                         dtype)
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            assert_y_close(out[a:b], ref[a:b], dtype, f"expert {e} ({b - a} rows)")
+
+
 def test_experts_output_alignment_fallback(cuda_lib):
     """moe_experts_forward into an output that is 16- but not 32-byte aligned:
     the epilogues then store 16-byte vectors instead of 32-byte sectors, with
