@@ -59,10 +59,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # code changes.
 GEMM_TRAFFIC = {
     # ncu --set full, one launch each on the headline workload: gate/up reads
-    # 1.141188 GB and writes 266.153472 MB, down reads 0.646926 GB and writes
-    # 374.187264 MB (ncu's units; the GB figures are rounded to the kilobyte)
-    "finegrained_bf16": {"bytes_per_launch": (1141188000 + 266153472 + 646926000 + 374187264) / 2,
-                         "code_sha256": "abad0710fabf29ebf59ffffcfa619bc73f8d2bcb79ca4d222b98e3b54a4f1bdb"},
+    # 1.141058 GB and writes 265.725696 MB, down reads 0.646926 GB and writes
+    # 373.762816 MB (ncu's units; the GB figures are rounded to the kilobyte)
+    "finegrained_bf16": {"bytes_per_launch": (1141058000 + 265725696 + 646926000 + 373762816) / 2,
+                         "code_sha256": "e15a00f4548dfbd7a723e0d81565253554c1d21e59cb26ec407440f0a3802ee4"},
 }
 
 

@@ -938,23 +938,21 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         };
         if (t.half) features(std::integral_constant<int, 64>{});
         else features(std::integral_constant<int, 128>{});
-      } else if (p.mode == kPlainF32 || p.mode == kWgrad) {
-        // FP32 accumulator rows: da in dispatch order, or a weight-gradient
-        // tile (rows at or past `split` go to out2; an expert without rows
-        // gets zeros).  A half tile's warp holds 128 of the 256 columns.
+      } else if (p.mode == kWgrad) {
+        // FP32 rows of a weight-gradient tile (rows at or past `split` go to
+        // out2; an expert without rows gets zeros).  A half tile's warp holds
+        // 128 of the 256 columns.
         const int64_t col0 = (int64_t)t.nb * 256 + (int64_t)nhalf * 128;
         float* rowf = nullptr;
         if (row_ok) {
-          if (p.mode == kPlainF32)
-            rowf = static_cast<float*>(p.out) + grow * p.n_out + col0;
-          else if (grow < p.split)
+          if (grow < p.split)
             rowf = static_cast<float*>(p.out) + ((int64_t)t.e * p.split + grow) * p.n_out + col0;
           else
             rowf = static_cast<float*>(p.out2) +
                    ((int64_t)t.e * (p.m_total - p.split) + grow - p.split) * p.n_out + col0;
         }
         uint32_t* rowp = reinterpret_cast<uint32_t*>(rowf);
-        const bool empty = p.mode == kWgrad && t.nk == 0;
+        const bool empty = t.nk == 0;
         if (empty) {
           uint32_t z[32];
 #pragma unroll

@@ -61,8 +61,7 @@ enum GemmMode {
   kGateUpSwiglu = 0,
   kDownPlain = 1,
   kDownWeighted = 2,
-  // backward products (tcgen05 path only)
-  kPlainF32 = 3,    // the accumulator in FP32 (da = dout W_down)
+  // backward products (tcgen05 path only; da = dout W_down and dinput use kDownPlain)
   kSwigluBwd = 4,   // g, u recomputed, then [dg | du] (out) and a (out2), 16-bit
   kWgrad = 5,       // per-expert FP32 weight-gradient tiles over the padded rows
 };
