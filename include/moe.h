@@ -206,8 +206,13 @@ void moe_experts_destroy(moe_experts_t experts);
  *   expert_out[r] = h . W_down[e]^T  (FP32 accumulation, stored in the
  *   weight dtype).
  * x_disp [N,H] and expert_out [N,H] are in the weight dtype; offsets [E+1]
- * on the device (never read by the host).  Rows at or beyond offsets[E] are
- * not written.  workspace: moe_experts_workspace_size(experts, N) bytes. */
+ * on the device (never read by the host), non-decreasing with offsets[E] <=
+ * N.  Rows at or beyond offsets[E] are not written.  The call checks the
+ * offsets on the device: an entry below its predecessor or above N is
+ * clamped (to the predecessor, or to N) and MOE_ERR_INVALID_INDEX is set in
+ * the workspace status word (moe_get_device_status); the outputs are then
+ * undefined, and no access leaves the buffers.  workspace:
+ * moe_experts_workspace_size(experts, N) bytes. */
 size_t moe_experts_workspace_size(moe_experts_t experts, int64_t N);
 moe_status moe_experts_forward(moe_experts_t experts, const void* x_disp, int64_t N,
                                const uint32_t* offsets, void* expert_out,
@@ -334,9 +339,10 @@ moe_status moe_forward_layout(moe_experts_t experts, int64_t T, int32_t top_k,
 
 /* Reads the device status word at the start of `workspace` after
  * synchronising `stream`: MOE_OK, MOE_ERR_INVALID_INDEX (dispatch met an
- * index >= E) or MOE_ERR_DEVICE_TIMEOUT (a kernel's bounded wait expired and
- * the kernel returned early; its outputs are undefined).  MOE_ERR_CUDA if
- * the synchronisation itself fails. */
+ * index >= E, or a staged expert call met offsets that are not
+ * non-decreasing within N) or MOE_ERR_DEVICE_TIMEOUT (a kernel's bounded wait
+ * expired and the kernel returned early; its outputs are undefined).
+ * MOE_ERR_CUDA if the synchronisation itself fails. */
 moe_status moe_get_device_status(const void* workspace, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
@@ -348,7 +354,8 @@ moe_status moe_get_device_status(const void* workspace, cudaStream_t stream);
 /* Combine backward: for the row r holding slot s = t*top_k + j (perm[r] = s),
  *   dexpert[r,:] = weights[s] * dy[t,:]            ([T*k, H], in `dtype`)
  *   dweights[s]  = sum_h expert_out[r,h] * dy[t,h] ([T,k], FP32)
- * Rows holding no slot get dexpert = 0; slots held by no row get NaN. */
+ * Rows holding no slot (perm[r] = 0xFFFFFFFF, or any entry >= T*top_k) get
+ * dexpert = 0; slots held by no row get NaN. */
 moe_status moe_combine_backward(const void* expert_out, moe_dtype dtype, const uint32_t* perm,
                                 const void* weights, moe_dtype weights_dtype, const void* dy,
                                 int64_t T, int32_t top_k, int64_t H, void* dexpert,
@@ -368,7 +375,9 @@ moe_status moe_dispatch_backward(const void* dinput, moe_dtype dtype, const uint
  *   dinput = dg W_gate + du W_up        ([N,H], weight dtype)
  *   ddown = sum_r dout_r^T a_r, dgate = sum_r dg_r^T x_r, dup = sum_r du_r^T x_r
  * (FP32 [E,H,I], [E,I,H], [E,I,H]; experts without rows get zeros).
- * FP32 accumulation throughout.  workspace:
+ * FP32 accumulation throughout.  offsets as for moe_experts_forward, checked
+ * and clamped on the device in the same way (MOE_ERR_INVALID_INDEX in the
+ * workspace status word).  workspace:
  * moe_experts_backward_workspace_size(experts, N) bytes (enough for every
  * strategy of moe_experts_backward_with_strategy). */
 size_t moe_experts_backward_workspace_size(moe_experts_t experts, int64_t N);

@@ -456,9 +456,12 @@ void moe_experts_destroy(moe_experts_t x) {
   delete x;
 }
 
+// the checked copy of a staged call's offsets, at the end of its workspace
+static size_t offsets_copy_bytes(const moe_experts* x) { return align_up((size_t)(x->E + 1) * 4, 1024); }
+
 size_t moe_experts_workspace_size(moe_experts_t x, int64_t N) {
   if (!x || N < 0) return 0;
-  return kWsHeader + align_up((size_t)N * x->I * dtype_size(x->dt), 1024);
+  return kWsHeader + align_up((size_t)N * x->I * dtype_size(x->dt), 1024) + offsets_copy_bytes(x);
 }
 
 moe_status moe_experts_forward(moe_experts_t x, const void* x_disp, int64_t N, const uint32_t* offsets,
@@ -473,7 +476,11 @@ moe_status moe_experts_forward(moe_experts_t x, const void* x_disp, int64_t N, c
     return fail(MOE_ERR_INVALID_ARG, "x_disp and expert_out must be 16-byte aligned");
   if ((st = check_ws(ws, ws_bytes, moe_experts_workspace_size(x, N))) != MOE_OK) return st;
   MOE_TRY_CUDA(cudaMemsetAsync(ws, 0, 4, stream), "cudaMemsetAsync");
-  st = run_experts(x, x_disp, N, offsets, static_cast<char*>(ws) + kWsHeader, expert_out,
+  uint32_t* off_ok = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + kWsHeader +
+                                                 align_up((size_t)N * x->I * dtype_size(x->dt), 1024));
+  MOE_TRY_CUDA(moe::launch_sanitize_offsets(offsets, (int)x->E, N, off_ok, status_word(ws), stream),
+               "offsets check launch");
+  st = run_experts(x, x_disp, N, off_ok, static_cast<char*>(ws) + kWsHeader, expert_out,
                    moe::kDownPlain, nullptr, nullptr, MOE_F32, status_word(ws), stream, nullptr);
   return st == MOE_OK ? ok() : st;
 }
@@ -791,12 +798,17 @@ static bool bwd_tc_ok(const moe_experts* x, int64_t N) {
   return x->tc && N + 63 * x->E < (int64_t)INT32_MAX;
 }
 
-size_t moe_experts_backward_workspace_size(moe_experts_t x, int64_t N) {
-  if (!x || N < 0) return 0;
+// scratch of either strategy: five FP32 [N, I] buffers, or the tensor-core layout
+static size_t bwd_scratch_bytes(const moe_experts* x, int64_t N) {
   size_t need = 5 * align_up((size_t)N * x->I * 4, 1024);
   if (bwd_tc_ok(x, N))
     need = std::max(need, moe::experts_backward_tc_workspace(N, (int)x->E, x->H, x->I));
-  return kWsHeader + need;
+  return need;
+}
+
+size_t moe_experts_backward_workspace_size(moe_experts_t x, int64_t N) {
+  if (!x || N < 0) return 0;
+  return kWsHeader + bwd_scratch_bytes(x, N) + offsets_copy_bytes(x);
 }
 
 moe_status moe_experts_backward_with_strategy(moe_experts_t x, const void* x_disp, int64_t N,
@@ -833,7 +845,8 @@ moe_status moe_experts_backward_with_strategy(moe_experts_t x, const void* x_dis
   a.gate = x->gate;
   a.up = x->up;
   a.down = x->down;
-  a.offsets = offsets;
+  uint32_t* off_ok = reinterpret_cast<uint32_t*>(base + bwd_scratch_bytes(x, N));
+  a.offsets = off_ok;
   a.g = reinterpret_cast<float*>(base);
   a.u = reinterpret_cast<float*>(base + part);
   a.act = reinterpret_cast<float*>(base + 2 * part);
@@ -851,8 +864,10 @@ moe_status moe_experts_backward_with_strategy(moe_experts_t x, const void* x_dis
     MOE_TRY_CUDA(cudaMemsetAsync(ddown, 0, wb, stream), "cudaMemsetAsync");
     return ok();
   }
+  MOE_TRY_CUDA(cudaMemsetAsync(ws, 0, 4, stream), "cudaMemsetAsync");
+  MOE_TRY_CUDA(moe::launch_sanitize_offsets(offsets, (int)x->E, N, off_ok, a.status, stream),
+               "offsets check launch");
   if (tc) {
-    MOE_TRY_CUDA(cudaMemsetAsync(ws, 0, 4, stream), "cudaMemsetAsync");
     MOE_TRY_CUDA(moe::launch_experts_backward_tc(a, x->tc, base, x->num_sms, stream),
                  "tensor-core expert backward launch");
   } else {

@@ -201,8 +201,9 @@ cudaError_t launch_combine_t(const void* src, const uint32_t* slot_row, const vo
 // FP32 dweights): one warp per dispatched row r holding slot s = t*k+j:
 //   dexpert[r,:] = w[s] * dy[t,:]      dweights[s] = sum_h expert_out[r,h] dy[t,h]
 // The dot product is summed per lane in column order, then by a butterfly
-// (a fixed order).  Rows holding no slot get dexpert = 0; slots no row holds
-// keep the NaN the caller's buffer was filled with.
+// (a fixed order).  Rows holding no slot (perm entry kInvalid or >= T*k) get
+// dexpert = 0; slots no row holds keep the NaN the caller's buffer was filled
+// with.
 // VEC (H % 8 == 0, 16-byte aligned rows): each lane takes 8-column vectors
 // lane, lane+32, ..., four in flight; its dot product runs over its vectors in
 // order and over the 8 columns of each in order, then the butterfly.
@@ -218,7 +219,7 @@ combine_backward_kernel(const T* __restrict__ eo, const uint32_t* __restrict__ p
   if (r >= N) return;
   const uint32_t s = __ldg(perm + r);
   T* dst = dexpert + r * H;
-  if (s == kInvalid) {
+  if ((uint64_t)s >= (uint64_t)N) {  // no slot (kInvalid, or an entry past the T*k slots)
     for (int64_t c = lane; c < H; c += 32) dst[c] = from_f32<T>(0.f);
     return;
   }

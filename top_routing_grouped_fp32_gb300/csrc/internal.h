@@ -108,6 +108,10 @@ struct ExpertsBwdArgs {
 };
 cudaError_t launch_experts_backward(const ExpertsBwdArgs& a, cudaStream_t s);
 
+// offsets of a staged expert call, clamped to [previous, N] (rowpad.cu); a
+// clamped entry sets MOE_ERR_INVALID_INDEX in *status
+cudaError_t launch_sanitize_offsets(const uint32_t* offsets, int E, int64_t N, uint32_t* out,
+                                   uint32_t* status, cudaStream_t s);
 // The 64-padded row space of the tensor-core backward (rowpad.cu)
 cudaError_t launch_pad_offsets(const uint32_t* offsets, int E, uint32_t* pad, cudaStream_t s);
 cudaError_t launch_pad_rows(const void* src, int64_t C, const uint32_t* offsets, const uint32_t* pad,

@@ -1,5 +1,6 @@
 // rowpad.cu -- the 64-padded row space of the tensor-core expert backward
-// (ExpertTrainingCache::backward in src/moe/experts.rs).
+// (ExpertTrainingCache::backward in src/moe/experts.rs), and the check of the
+// offsets a caller passes to the staged expert calls.
 //
 // The weight gradients are per-expert sums over that expert's dispatched
 // rows.  The tcgen05 engine reads them 64 rows per k-block; if each expert's
@@ -41,6 +42,46 @@ __global__ void pad_offsets_kernel(const uint32_t* __restrict__ offsets, int E, 
   if (lane == 31) pad[E] = incl;
 }
 
+// The offsets of a staged expert call as its kernels read them: each clamped
+// to [previous, N], so that no segment runs backwards or past the N rows of
+// the buffers; a clamped entry marks the status word MOE_ERR_INVALID_INDEX.
+// One warp: per-lane serial running maxima, then a warp max-scan (E <= 1024).
+__global__ void sanitize_offsets_kernel(const uint32_t* __restrict__ in, int E, int64_t N,
+                                        uint32_t* __restrict__ out, uint32_t* __restrict__ status) {
+  const int lane = threadIdx.x;
+  const int n = E + 1;
+  const int per = (n + 31) / 32;
+  const uint32_t cap = N < (int64_t)0xFFFFFFFFu ? (uint32_t)N : 0xFFFFFFFEu;
+  uint32_t run = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = lane * per + i;
+    if (e < n) {
+      const uint32_t v = in[e];
+      run = max(run, v < cap ? v : cap);
+    }
+  }
+  uint32_t incl = run;  // max over this lane's entries and every earlier lane's
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl = max(incl, o);
+  }
+  uint32_t prev = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) prev = 0;
+  bool bad = false;
+  for (int i = 0; i < per; ++i) {
+    const int e = lane * per + i;
+    if (e < n) {
+      const uint32_t v = in[e];
+      const uint32_t c = max(prev, v < cap ? v : cap);
+      out[e] = c;
+      bad |= c != v;
+      prev = c;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, (uint32_t)MOE_ERR_INVALID_INDEX);
+}
+
 constexpr int kRowsPerBlock = 8;  // one warp per row
 
 __global__ void __launch_bounds__(32 * kRowsPerBlock)
@@ -65,6 +106,12 @@ pad_rows_kernel(const uint4* __restrict__ src, int64_t vecs, const uint32_t* __r
 }
 
 }  // namespace
+
+cudaError_t launch_sanitize_offsets(const uint32_t* offsets, int E, int64_t N, uint32_t* out,
+                                   uint32_t* status, cudaStream_t s) {
+  sanitize_offsets_kernel<<<1, 32, 0, s>>>(offsets, E, N, out, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pad_offsets(const uint32_t* offsets, int E, uint32_t* pad, cudaStream_t s) {
   pad_offsets_kernel<<<1, 32, 0, s>>>(offsets, E, pad);
